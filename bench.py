@@ -1,0 +1,497 @@
+#!/usr/bin/env python3
+"""Benchmark of the GGUF Q4_0 / Q8_0 decode DMMV on GB300.
+
+Workload (default): the dense Q4_0 4096 x 4096 decode DMMV, batch 1. One STEP is
+one decode token through a stack of LAYERS distinct weight matrices of that
+shape (each layer: quantize the fp32 activation to Q8_0, then the DMMV), i.e.
+every step streams LAYERS x 9.44 MB of weights. The stack (605 MB at 64 layers)
+is larger than 4x the 129 MB L2, so no layer's weights are L2-resident when it
+runs. Inputs are resident in HBM before the timed region; the step is captured
+once in a CUDA graph and replayed (decode chains are replayed as graphs: "RTX
+5090: Batched Prefill & CUDA Graphs in ZINC", "CUDA graphs -- the structural
+answer to launch latency").
+
+Printed: one JSON line (rank 0) with value = algorithmic GB/s over the whole job
+(weights read once + Q8_0 activation blocks + fp32 outputs), the
+roofline of the dominant kernel (the DMMV) against the measured HBM copy
+bandwidth, the CPU oracle as baseline, the end-to-end number through the
+host-buffer C-ABI call, clocks sampled during the timed region, and per-workload
+measurements of the other four decode workloads.
+
+--impl reference times the CPU oracle on the same workload and metric: with no
+upstream code to run, the oracle is the reference implementation of the method.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "Q4_0/Q8_0 DMMV achieved HBM GB/s and % of GB300 peak; rows/s"
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=2000)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["zdmmv", "reference"], default="zdmmv")
+    p.add_argument("--layers", type=int, default=64, help="distinct weight matrices per step")
+    p.add_argument("--no-extra", action="store_true", help="skip the other four workloads")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--eager", action="store_true", help="launch eagerly instead of graph replay")
+    return p.parse_args()
+
+
+# --------------------------------------------------------------------- helpers
+def peaks():
+    try:
+        with open(PEAKS_FILE) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_sources_sha() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "gguf_block_quant_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per launch of the dominant kernel from a committed ncu summary,
+    or None if there is none or the kernel sources changed since it was taken."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            d = json.load(f)
+        e = d[workload]
+        if e.get("src_sha") != kernel_sources_sha():
+            return None
+        return float(e["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, interval_ms: int = 20):
+        self.proc = None
+        self.gpu = gpu_index
+        self.interval = interval_ms
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", str(self.interval)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm),
+                "power_w_max": max(power) if power else None}
+
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def reduce_max(value: float, world: int, device) -> float:
+    """Max of a per-rank scalar over all ranks (timing only; no data-path collective)."""
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ------------------------------------------------------------------ CPU oracle
+def cpu_baseline_dense(cfg, layers_budget_s: float = 12.0):
+    """Time the oracle (as it stands, single thread) on a bounded sample of the
+    dense workload: whole layers (quantize + DMMV of one 4096 x 4096 matrix)
+    until about layers_budget_s of CPU work."""
+    import oracle
+    from gguf_block_quant_gb300 import synth
+    w = synth.weight_blocks(cfg.fmt, cfg.rows, cfg.cols, seed=cfg.seed)
+    x = synth.activations(cfg.cols, seed=cfg.seed, scale=cfg.x_scale)
+    oracle.lib()
+    done = 0
+    t0 = time.perf_counter()
+    while True:
+        xq = oracle.quantize_q8_0(x)
+        oracle.dmmv(cfg.fmt, w, cfg.rows, cfg.cols, xq)
+        done += 1
+        el = time.perf_counter() - t0
+        if el >= layers_budget_s or done >= 2000:
+            break
+    gbs = done * cfg.algorithmic_bytes() / el / 1e9
+    return {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{done} layers ({cfg.name}: quantize + DMMV each) in {el:.1f} s, single-threaded C",
+            "rows_per_s": done * cfg.rows / el}
+
+
+# ----------------------------------------------------------------- GPU arm
+def graph_or_eager(fn, eager: bool):
+    import torch
+    if eager:
+        return fn
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        fn()
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    torch.cuda.synchronize()
+    return g.replay
+
+
+def time_fn(run, steps: int, warmup: int, world: int, device, sampler=None):
+    import torch
+    for _ in range(warmup):
+        run()
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    if sampler:
+        sampler.start()
+        time.sleep(0.05)
+    e0.record(stream)
+    for _ in range(steps):
+        run()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop() if sampler else None
+    barrier(world)
+    ms = e0.elapsed_time(e1)
+    return reduce_max(ms, world, device), clocks
+
+
+class DensePool:
+    """LAYERS distinct copies of one dense workload's tensors, resident in HBM."""
+
+    def __init__(self, cfg, layers: int):
+        import numpy as np
+        import torch
+        from gguf_block_quant_gb300 import synth
+        from gguf_block_quant_gb300 import zdmmv as Z
+        self.cfg, self.layers = cfg, layers
+        w = torch.from_numpy(synth.weight_blocks(cfg.fmt, cfg.rows, cfg.cols, seed=cfg.seed)).cuda()
+        self.w = [w] + [w.clone() for _ in range(layers - 1)]
+        x = synth.activations(cfg.cols, seed=cfg.seed, scale=cfg.x_scale, batch=max(cfg.batch, 1))
+        x = torch.from_numpy(np.ascontiguousarray(x).reshape(-1)).cuda()
+        self.x = [x] + [x.clone() for _ in range(layers - 1)]
+        nq = cfg.batch * cfg.nb * 34
+        self.xq = [torch.empty(nq, dtype=torch.uint8, device="cuda") for _ in range(layers)]
+        self.y = [torch.empty(cfg.batch * cfg.rows, dtype=torch.float32, device="cuda") for _ in range(layers)]
+        self.Z = Z
+        self.step()   # activations quantized once so the DMMV-only pass reads valid blocks
+        torch.cuda.synchronize()
+
+    def step(self):
+        Z, c = self.Z, self.cfg
+        for l in range(self.layers):
+            Z.quantize_act_q8_0(self.x[l], self.xq[l])
+            if c.batch == 1:
+                Z.dmmv(c.fmt, self.w[l], c.rows, c.cols, self.xq[l], y=self.y[l])
+            else:
+                Z.dmmv_batched(c.fmt, self.w[l], c.rows, c.cols, self.xq[l], c.batch, y=self.y[l])
+
+    def dmmv_only(self):
+        Z, c = self.Z, self.cfg
+        for l in range(self.layers):
+            if c.batch == 1:
+                Z.dmmv(c.fmt, self.w[l], c.rows, c.cols, self.xq[l], y=self.y[l])
+            else:
+                Z.dmmv_batched(c.fmt, self.w[l], c.rows, c.cols, self.xq[l], c.batch, y=self.y[l])
+
+
+def layers_for(cfg, l2_bytes: int, min_layers: int = 2) -> int:
+    per = cfg.weight_bytes
+    return max(min_layers, -(-4 * l2_bytes // per))
+
+
+def measure_dense(cfg, layers, steps, warmup, world, device, eager):
+    import torch
+    pool = DensePool(cfg, layers)
+    run = graph_or_eager(pool.dmmv_only, eager)
+    pool_step = graph_or_eager(pool.step, eager)
+    ms_dmmv, _ = time_fn(run, steps, warmup, world, device)
+    ms_step, _ = time_fn(pool_step, steps, warmup, world, device)
+    per_launch_s = ms_dmmv / 1e3 / (steps * layers)
+    per_step_s = ms_step / 1e3 / steps
+    nbytes = cfg.algorithmic_bytes()
+    del pool
+    torch.cuda.empty_cache()
+    return {"layers": layers, "dmmv_us": per_launch_s * 1e6, "dmmv_gbs": nbytes / per_launch_s / 1e9,
+            "step_gbs": layers * nbytes / per_step_s / 1e9, "rows_per_s": cfg.batch * cfg.rows / per_launch_s,
+            "algorithmic_bytes": nbytes}
+
+
+def measure_moe(steps, warmup, world, device, eager, l2_bytes):
+    """Config: 9 selected experts (8 routed + shared) of a 129-slot stack; one
+    step = gate, up (Q4_0 512x2048) and down (Q8_0 2048x512) gathers, each ONE
+    launch; stacks rotated over copies so that > 4x L2 is touched per pass."""
+    import numpy as np
+    import torch
+    from gguf_block_quant_gb300 import synth
+    from gguf_block_quant_gb300 import zdmmv as Z
+    m = synth.MOE
+    gate = torch.from_numpy(synth.weight_blocks(synth.Q4_0, m.n_slots * m.ffn, m.hidden, seed=m.seed)).cuda()
+    up = torch.from_numpy(synth.weight_blocks(synth.Q4_0, m.n_slots * m.ffn, m.hidden, seed=m.seed,
+                                              stream=synth.S_WEIGHT2)).cuda()
+    down = torch.from_numpy(synth.weight_blocks(synth.Q8_0, m.n_slots * m.hidden, m.ffn, seed=m.seed,
+                                                stream=synth.S_WEIGHT3)).cuda()
+    # different routing per layer so touched experts differ; stacks are 296 MB per layer set
+    n_sets = 2
+    stacks = [(gate, up, down)] + [(gate.clone(), up.clone(), down.clone()) for _ in range(n_sets - 1)]
+    idxs = [torch.from_numpy(synth.expert_indices(m.seed + 100 * i, m.n_routed, m.top_k)).cuda()
+            for i in range(8)]
+    x = torch.from_numpy(synth.activations(m.hidden, seed=m.seed)).cuda()
+    xd = torch.from_numpy(np.ascontiguousarray(
+        synth.activations(m.ffn, seed=m.seed, stream=synth.S_ACT2, batch=m.n_sel)).reshape(-1)).cuda()
+    xq = Z.quantize_act_q8_0(x)
+    xqd = Z.quantize_act_q8_0(xd)
+    yg = torch.empty(m.n_sel, m.ffn, device="cuda")
+    yu = torch.empty(m.n_sel, m.ffn, device="cuda")
+    yd = torch.empty(m.n_sel, m.hidden, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    gu, dn = m.gate_up_bytes(), m.down_bytes()
+    layers = 16
+
+    def step():
+        for l in range(layers):
+            g, u, d = stacks[l % n_sets]
+            idx = idxs[l % len(idxs)]
+            Z.expert_gather(Z.Q4_0, g, gu, m.ffn, m.hidden, idx, m.n_slots, xq, 0, y=yg, status=st)
+            Z.expert_gather(Z.Q4_0, u, gu, m.ffn, m.hidden, idx, m.n_slots, xq, 0, y=yu, status=st)
+            Z.expert_gather(Z.Q8_0, d, dn, m.hidden, m.ffn, idx, m.n_slots, xqd, (m.ffn // 32) * 34, y=yd,
+                            status=st)
+
+    run = graph_or_eager(step, eager)
+    ms, _ = time_fn(run, steps, warmup, world, device)
+    per_layer = ms / 1e3 / (steps * layers)
+    nbytes = m.algorithmic_bytes()
+    return {"layers": layers, "us_per_token_layer": per_layer * 1e6, "gbs": nbytes / per_layer / 1e9,
+            "rows_per_s": m.n_sel * (2 * m.ffn + m.hidden) / per_layer, "algorithmic_bytes": nbytes,
+            "launches_per_layer": 3,
+            "note": "touched experts differ per layer; stack copies alternate (some L2 reuse possible)"}
+
+
+def e2e_dense(cfg, layers, steps, warmup, world, device):
+    """Through the public host-buffer C-ABI call: per layer, H2D of the fp32
+    activation from pinned memory, quantize, DMMV, D2H of y to pinned memory."""
+    import numpy as np
+    import torch
+    from gguf_block_quant_gb300 import synth
+    from gguf_block_quant_gb300 import zdmmv as Z
+    w = torch.from_numpy(synth.weight_blocks(cfg.fmt, cfg.rows, cfg.cols, seed=cfg.seed)).cuda()
+    ws_ = [w] + [w.clone() for _ in range(layers - 1)]
+    x = synth.activations(cfg.cols, seed=cfg.seed, scale=cfg.x_scale)
+    xh = [torch.from_numpy(np.ascontiguousarray(x)).pin_memory() for _ in range(layers)]
+    yh = [torch.empty(cfg.rows, dtype=torch.float32).pin_memory() for _ in range(layers)]
+    wsb = Z.host_step_workspace_bytes(cfg.rows, cfg.cols, 1)
+    work = [torch.empty(wsb, dtype=torch.uint8, device="cuda") for _ in range(layers)]
+
+    def step():
+        for l in range(layers):
+            Z.host_step(cfg.fmt, ws_[l], cfg.rows, cfg.cols, xh[l], yh[l], work[l])
+
+    ms, _ = time_fn(step, steps, warmup, world, device)
+    per_step = ms / 1e3 / steps
+    h2d = layers * cfg.cols * 4
+    d2h = layers * cfg.rows * 4
+    return {"value": layers * cfg.algorithmic_bytes() * world / per_step / 1e9, "unit": "GB/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "ms_per_step": ms / steps, "launch": "eager C-ABI zdmmv_host_step per layer"}
+
+
+def gpu_arm(args):
+    import torch
+    world, rank, local = dist_setup(args)
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    from gguf_block_quant_gb300 import synth
+    from gguf_block_quant_gb300 import zdmmv as Z
+    Z.lib()
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    cfg = synth.DENSE_Q4_0
+    layers = max(args.layers, layers_for(cfg, l2))
+    pool = DensePool(cfg, layers)
+    hbm_peak, peak_kind = peaks()
+
+    # the DMMV kernel alone (activations pre-quantized): its average launch duration
+    run_dmmv = graph_or_eager(pool.dmmv_only, args.eager)
+    ms_dmmv, _ = time_fn(run_dmmv, args.steps, args.warmup, world, device)
+    per_launch = ms_dmmv / 1e3 / (args.steps * layers)
+    nbytes = cfg.algorithmic_bytes()
+    achieved = nbytes / per_launch / 1e9
+
+    # the headline: whole steps (quantize + DMMV per layer), clocks sampled meanwhile
+    run_step = graph_or_eager(pool.step, args.eager)
+    sampler = ClockSampler(local)
+    ms, clocks = time_fn(run_step, args.steps, args.warmup, world, device, sampler)
+    ms_per_step = ms / args.steps
+    value = world * layers * nbytes / (ms_per_step / 1e3) / 1e9
+    rows_per_s = world * layers * cfg.rows / (ms_per_step / 1e3)
+    del pool, run_dmmv, run_step
+    torch.cuda.empty_cache()
+
+    e2e = e2e_dense(cfg, min(layers, 64), max(3, args.steps // 10), args.warmup, world, device)
+
+    workloads = {}
+    if not args.no_extra:
+        for c in (synth.SSM_ALPHA_BETA, synth.LM_HEAD_Q4_0, *synth.BATCHED_Q8_0.values()):
+            workloads[c.name] = measure_dense(c, layers_for(c, l2), max(5, args.steps // 4), args.warmup,
+                                              world, device, args.eager)
+            workloads[c.name]["pct_of_peak"] = 100 * workloads[c.name]["dmmv_gbs"] / hbm_peak
+        workloads["moe_experts_top8_plus_shared"] = measure_moe(max(5, args.steps // 4), args.warmup, world,
+                                                                device, args.eager, l2)
+
+    out = None
+    if rank == 0:
+        cpu = None
+        if not args.no_cpu_baseline:
+            cpu = cpu_baseline_dense(cfg)
+        traffic = recorded_traffic(cfg.name)
+        out = {
+            "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "int8", "data": "synthetic",
+            "config": {"workload": cfg.name, "rows": cfg.rows, "cols": cfg.cols, "format": "Q4_0", "batch": 1,
+                       "layers_per_step": layers, "step": "quantize_act_q8_0 + DMMV per layer",
+                       "l2": f"inputs larger than L2: {layers} distinct weight matrices "
+                             f"({layers * cfg.weight_bytes / 1e6:.0f} MB) per step, L2 {l2 / 1e6:.0f} MB",
+                       "launch": "eager" if args.eager else "cuda_graph replay", "parallelism": f"replicas x{world}"},
+            "pct_of_peak": round(100 * value / world / hbm_peak, 2),
+            "rows_per_s": rows_per_s,
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
+                         "frac": round(achieved / hbm_peak, 4), "traffic": traffic,
+                         "kernel": "dmmv_tma_kernel (Q4_0, GGUF layout)",
+                         "algorithmic_bytes_per_launch": nbytes, "us_per_launch": round(per_launch * 1e6, 3),
+                         "peak_kind": f"{peak_kind} HBM copy bandwidth"},
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": 2 * layers * args.steps,
+            "clocks": clocks,
+            "workloads": workloads,
+        }
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+    if out is not None:
+        print(json.dumps(out), flush=True)
+
+
+# ------------------------------------------------------------ reference arm
+def reference_arm(args):
+    world, rank, _ = dist_setup(args)
+    if rank != 0:
+        return
+    import oracle
+    from gguf_block_quant_gb300 import synth
+    cfg = synth.DENSE_Q4_0
+    w = synth.weight_blocks(cfg.fmt, cfg.rows, cfg.cols, seed=cfg.seed)
+    x = synth.activations(cfg.cols, seed=cfg.seed, scale=cfg.x_scale)
+    oracle.lib()
+    layers_per_step = 2   # a bounded sample of the 64-layer step, so K steps finish in minutes
+
+    def step():
+        for _ in range(layers_per_step):
+            xq = oracle.quantize_q8_0(x)
+            oracle.dmmv(cfg.fmt, w, cfg.rows, cfg.cols, xq)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    el = time.perf_counter() - t0
+    ms_per_step = el * 1e3 / args.steps
+    value = layers_per_step * cfg.algorithmic_bytes() / (el / args.steps) / 1e9
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "int8", "data": "synthetic",
+        "config": {"workload": cfg.name, "rows": cfg.rows, "cols": cfg.cols, "format": "Q4_0", "batch": 1,
+                   "layers_per_step": layers_per_step, "step": "quantize_act_q8_0 + DMMV per layer"},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{layers_per_step} layers per step of {cfg.name}, single-threaded C oracle"},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        reference_arm(args)
+    else:
+        gpu_arm(args)
+
+
+if __name__ == "__main__":
+    main()

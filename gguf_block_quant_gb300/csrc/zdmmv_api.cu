@@ -1,0 +1,562 @@
+// zdmmv_api.cu -- the C ABI of libzdmmv.so: argument checks, launch planning and
+// the small kernels (activation quantizer, repack, plain DMMV, debug sums, dp4a
+// self-test). The TMA-pipelined DMMV kernels live in zdmmv_tma_q8.cu /
+// zdmmv_tma_q4.cu. The library allocates no device memory.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "zdmmv.h"
+#include "zdmmv_device.cuh"
+#include "zdmmv_internal.h"
+
+namespace zdmmv {
+
+// ------------------------------------------------------------- fault word
+// One word per device that kernels OR fault bits into (bounded waits that gave
+// up). Read and cleared by zdmmv_device_status.
+__device__ uint32_t g_fault_word;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+    bool ready = false;
+    int sms = 0;
+    uint32_t *fault = nullptr;
+};
+DeviceInfo g_devices[kMaxDevices];
+std::mutex g_mu;
+
+cudaError_t device_info(const DeviceInfo **out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lk(g_mu);
+    DeviceInfo &d = g_devices[dev];
+    if (!d.ready) {
+        e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_fault_word);
+        if (e != cudaSuccess) return e;
+        d.fault = static_cast<uint32_t *>(p);
+        d.ready = true;
+    }
+    *out = &d;
+    return cudaSuccess;
+}
+
+bool pdl_enabled() {
+    static const bool on = [] {
+        const char *v = std::getenv("ZDMMV_PDL");
+        return !(v && v[0] == '0');
+    }();
+    return on;
+}
+
+inline bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+inline int block_bytes(int fmt) { return fmt == kFmtQ8 ? 34 : (fmt == kFmtQ4 ? 18 : 0); }
+inline int64_t round_up(int64_t v, int64_t m) { return (v + m - 1) / m * m; }
+
+zdmmv_status from_cuda(cudaError_t e) { return e == cudaSuccess ? ZDMMV_OK : ZDMMV_ERR_CUDA; }
+
+}  // namespace
+
+// ------------------------------------------------------------ planning
+bool tma_shape_ok(int fmt, int64_t cols) {
+    if (block_bytes(fmt) == 0 || cols <= 0 || cols % kQK) return false;
+    const int64_t nb = cols / kQK;
+    // rows must be 16-byte multiples (bulk copies) and the activation must fit
+    // the register budget: at most 4 pairs per lane with 32 lanes per row
+    return nb % 8 == 0 && nb / 2 <= 128;
+}
+
+TmaPlan tma_plan(int fmt, int layout, int64_t cols) {
+    (void)layout;
+    TmaPlan p{};
+    const int nb = static_cast<int>(cols / kQK);
+    const int npairs = nb / 2;
+    if (npairs <= 8) {
+        p.lpr = 8; p.ppl = 1;
+    } else if (npairs <= 16) {
+        p.lpr = 16; p.ppl = 1;
+    } else if (npairs <= 32) {
+        p.lpr = 32; p.ppl = 1;
+    } else if (npairs <= 64) {
+        p.lpr = 32; p.ppl = 2;
+    } else {
+        p.lpr = 32; p.ppl = 4;
+    }
+    const int rows_par = kConsumerThreads / p.lpr;
+    const int row_bytes = nb * block_bytes(fmt);
+    const int unit = rows_par * row_bytes;        // bytes of one pass of the row groups
+    constexpr int kStageTarget = 24 * 1024;
+    const int m = unit >= kStageTarget ? 1 : kStageTarget / unit;
+    p.tile_rows = rows_par * m;
+    p.stage_bytes = static_cast<int>(round_up(static_cast<int64_t>(p.tile_rows) * row_bytes, 128));
+    p.x_bytes_padded = static_cast<int>(round_up(static_cast<int64_t>(nb) * 34, 128));
+    p.stages = 4;
+    if (kBarrierBytes + p.x_bytes_padded + 4 * p.stage_bytes > 112 * 1024) p.stages = 3;
+    p.smem_bytes = kBarrierBytes + p.x_bytes_padded + p.stages * p.stage_bytes;
+    return p;
+}
+
+// ------------------------------------------------------------- kernels
+__device__ __forceinline__ void pdl_wait_api() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger_api() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// One warp per Q8_0 block: lane j owns element j.
+__global__ void __launch_bounds__(256) quantize_q8_0_kernel(const float *__restrict__ x, int64_t nblocks,
+                                                            uint8_t *__restrict__ xq) {
+    pdl_wait_api();
+    pdl_trigger_api();
+    const int lane = threadIdx.x & 31;
+    const int64_t blk = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (blk >= nblocks) return;
+    const float v = x[blk * kQK + lane];
+    // max of |x| over the block; for non-negative floats the bit patterns order like the values
+    const uint32_t amax_bits = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(v)));
+    const float amax = __uint_as_float(amax_bits);
+    const float d = amax / 127.0f;                 // IEEE division (no fast-math in this build)
+    const float id = d != 0.0f ? 1.0f / d : 0.0f;  // IEEE reciprocal
+    const float q = roundf(__fmul_rn(v, id));      // round half away from zero
+    uint8_t *out = xq + blk * 34;
+    out[2 + lane] = static_cast<uint8_t>(static_cast<int8_t>(static_cast<int>(q)));
+    if (lane == 0) {
+        const unsigned short hb = __half_as_ushort(__float2half_rn(d));
+        out[0] = static_cast<uint8_t>(hb & 0xffu);
+        out[1] = static_cast<uint8_t>(hb >> 8);
+    }
+}
+
+// One thread per block: GGUF block -> quant stream slot + scale slot.
+template <int FMT>
+__global__ void __launch_bounds__(256) repack_kernel(const uint8_t *__restrict__ src, int64_t nblocks,
+                                                     uint8_t *__restrict__ dst) {
+    constexpr int kBB = Fmt<FMT>::kBlockBytes;
+    constexpr int kQB = Fmt<FMT>::kQuantBytes;
+    const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (i >= nblocks) return;
+    const uint16_t *h = reinterpret_cast<const uint16_t *>(src + i * kBB);
+    uint32_t q[kQB / 4];
+#pragma unroll
+    for (int k = 0; k < kQB / 4; ++k) q[k] = ld_u16_pair(h + 1 + 2 * k);
+    uint4 *dq = reinterpret_cast<uint4 *>(dst + i * kQB);
+#pragma unroll
+    for (int k = 0; k < kQB / 16; ++k) dq[k] = make_uint4(q[4 * k], q[4 * k + 1], q[4 * k + 2], q[4 * k + 3]);
+    reinterpret_cast<uint16_t *>(dst + nblocks * kQB)[i] = h[0];
+}
+
+__global__ void selftest_dp4a_kernel(const int32_t *a, const int32_t *b, const int32_t *c, int32_t *out, int n) {
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i < n) out[i] = dp4a_ss(static_cast<uint32_t>(a[i]), static_cast<uint32_t>(b[i]), c[i]);
+}
+
+// Plain DMMV for the shapes the pipelined kernel does not take (rows that are
+// not 16-byte multiples, very long rows): one warp per row, lanes stride over
+// blocks with 16-bit loads. Same block arithmetic, fp32 accumulation and
+// xor-shuffle reduction. Handles `batch` vectors per slot and expert slots.
+template <int FMT, int LAYOUT>
+__global__ void __launch_bounds__(256) dmmv_plain_kernel(const DmmvArgs a) {
+    pdl_wait_api();
+    pdl_trigger_api();
+    constexpr int kBB = Fmt<FMT>::kBlockBytes;
+    constexpr int kQB = Fmt<FMT>::kQuantBytes;
+    const int lane = threadIdx.x & 31;
+    const int64_t row = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const int slot = blockIdx.y;
+    if (row >= a.rows) return;
+    float *y = a.y + slot * a.y_stride;
+    const uint8_t *w = a.w;
+    if (a.idx != nullptr) {
+        const int e = a.idx[slot];
+        if (e < 0 || e >= a.n_experts) {
+            if (lane == 0) {
+                y[row] = __int_as_float(0x7fc00000);
+                if (a.status != nullptr) atomicExch(a.status, 1);
+            }
+            return;
+        }
+        w += static_cast<int64_t>(e) * a.expert_stride;
+    }
+    const int nb = a.nb;
+    const uint8_t *xq0 = a.xq + slot * a.xq_stride;
+    for (int v = 0; v < a.batch; ++v) {
+        const uint8_t *xq = xq0 + static_cast<int64_t>(v) * nb * 34;
+        float acc = 0.0f;
+        for (int b = lane; b < nb; b += 32) {
+            uint32_t q[8], xw[8];
+            float dw, dx;
+            const int64_t blk = row * nb + b;
+            if constexpr (LAYOUT == kLayoutGguf)
+                Block<FMT>::load_gguf(w + blk * kBB, q, dw);
+            else
+                Block<FMT>::load_repacked(w + blk * kQB, w + a.rows * nb * kQB + blk * 2, q, dw);
+            load_x_block(xq + static_cast<int64_t>(b) * 34, xw, dx);
+            const int s = Block<FMT>::dot(q, xw);
+            acc = __fmaf_rn(static_cast<float>(s), __fmul_rn(dw, dx), acc);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+        if (lane == 0) y[static_cast<int64_t>(v) * a.rows + row] = acc;
+    }
+}
+
+// Debug: the int32 block sums with the device functions of the kernel that the
+// DMMV entry points pick for this shape. PAIRS: one thread per (row, pair) via
+// Pair<>::sums (pipelined kernel); else one thread per (row, block) via Block<>.
+template <int FMT, int LAYOUT, bool PAIRS>
+__global__ void __launch_bounds__(256) block_sums_kernel(const uint8_t *__restrict__ w, int64_t rows, int nb,
+                                                         const uint8_t *__restrict__ xq, int32_t *__restrict__ sums) {
+    constexpr int kBB = Fmt<FMT>::kBlockBytes;
+    constexpr int kQB = Fmt<FMT>::kQuantBytes;
+    const int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if constexpr (PAIRS) {
+        const int npairs = nb / 2;
+        if (t >= rows * npairs) return;
+        const int64_t row = t / npairs;
+        const int p = static_cast<int>(t % npairs);
+        uint32_t v[17];
+        load_x_pair_words(xq, p, v);
+        Pair<FMT, LAYOUT> pr;
+        pr.set(v);
+        constexpr int kW = Pair<FMT, LAYOUT>::kWords;
+        uint32_t ww[kW];
+        const uint32_t *src;
+        if constexpr (LAYOUT == kLayoutGguf)
+            src = reinterpret_cast<const uint32_t *>(w + row * nb * kBB + static_cast<int64_t>(p) * 2 * kBB);
+        else
+            src = reinterpret_cast<const uint32_t *>(w + (row * nb + 2 * p) * kQB);
+#pragma unroll
+        for (int k = 0; k < kW; ++k) ww[k] = src[k];
+        int sa, sb;
+        pr.sums(ww, sa, sb);
+        sums[row * nb + 2 * p] = sa;
+        sums[row * nb + 2 * p + 1] = sb;
+    } else {
+        if (t >= rows * nb) return;
+        const int64_t row = t / nb;
+        const int b = static_cast<int>(t % nb);
+        uint32_t q[8], xw[8];
+        float dw, dx;
+        if constexpr (LAYOUT == kLayoutGguf)
+            Block<FMT>::load_gguf(w + t * kBB, q, dw);
+        else
+            Block<FMT>::load_repacked(w + t * kQB, w + rows * nb * kQB + t * 2, q, dw);
+        load_x_block(xq + static_cast<int64_t>(b) * 34, xw, dx);
+        (void)row;
+        sums[t] = Block<FMT>::dot(q, xw);
+    }
+}
+
+// --------------------------------------------------------- launch helpers
+namespace {
+
+cudaError_t launch_plain(int fmt, int layout, const DmmvArgs &a, int slots, cudaStream_t st) {
+    if (a.rows == 0 || slots == 0) return cudaSuccess;
+    const int64_t blocks = (a.rows + 7) / 8;
+    if (blocks > 0x7fffffff) return cudaErrorInvalidConfiguration;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(blocks), static_cast<unsigned>(slots), 1);
+    cfg.blockDim = dim3(256, 1, 1);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl_enabled() ? 1 : 0;
+    if (fmt == kFmtQ8)
+        return layout == kLayoutGguf ? cudaLaunchKernelEx(&cfg, dmmv_plain_kernel<kFmtQ8, kLayoutGguf>, a)
+                                     : cudaLaunchKernelEx(&cfg, dmmv_plain_kernel<kFmtQ8, kLayoutRepacked>, a);
+    return layout == kLayoutGguf ? cudaLaunchKernelEx(&cfg, dmmv_plain_kernel<kFmtQ4, kLayoutGguf>, a)
+                                 : cudaLaunchKernelEx(&cfg, dmmv_plain_kernel<kFmtQ4, kLayoutRepacked>, a);
+}
+
+// Run the DMMV over `slots` slots (expert gather / batch through slots).
+zdmmv_status run_dmmv(int fmt, int layout, DmmvArgs a, int slots, cudaStream_t st) {
+    const DeviceInfo *dev = nullptr;
+    cudaError_t e = device_info(&dev);
+    if (e != cudaSuccess) return ZDMMV_ERR_CUDA;
+    a.fault = dev->fault;
+    if (a.rows == 0 || slots == 0) return ZDMMV_OK;
+    const int64_t cols = static_cast<int64_t>(a.nb) * kQK;
+    if (tma_shape_ok(fmt, cols) && a.batch == 1) {
+        const TmaPlan p = tma_plan(fmt, layout, cols);
+        a.tile_rows = p.tile_rows;
+        a.stage_bytes = p.stage_bytes;
+        a.x_bytes_padded = p.x_bytes_padded;
+        const int per_sm = fmt == kFmtQ8 ? tma_ctas_per_sm_q8(layout, p) : tma_ctas_per_sm_q4(layout, p);
+        const int64_t total = static_cast<int64_t>(dev->sms) * per_sm;
+        int64_t ctas = total / slots;
+        if (ctas < 1) ctas = 1;
+        if (ctas > a.rows) ctas = a.rows;
+        if (ctas > 65535) ctas = 65535;
+        e = fmt == kFmtQ8 ? launch_tma_q8(a, p, layout, static_cast<int>(ctas), slots, st, pdl_enabled())
+                          : launch_tma_q4(a, p, layout, static_cast<int>(ctas), slots, st, pdl_enabled());
+        return from_cuda(e);
+    }
+    return from_cuda(launch_plain(fmt, layout, a, slots, st));
+}
+
+zdmmv_status check_matrix(int fmt, const void *w, int layout, int64_t rows, int64_t cols, const void *xq,
+                          const float *y) {
+    if (block_bytes(fmt) == 0) return ZDMMV_ERR_FORMAT;
+    if (layout != ZDMMV_LAYOUT_GGUF && layout != ZDMMV_LAYOUT_REPACKED) return ZDMMV_ERR_LAYOUT;
+    if (rows < 0 || cols <= 0 || cols % kQK) return ZDMMV_ERR_SHAPE;
+    if (cols / kQK > 0x3fffffff) return ZDMMV_ERR_SHAPE;
+    if (rows == 0) return ZDMMV_OK;
+    if (!w || !xq || !y) return ZDMMV_ERR_NULL;
+    if (!aligned(w, 16) || !aligned(xq, 16) || !aligned(y, 4)) return ZDMMV_ERR_ALIGN;
+    return ZDMMV_OK;
+}
+
+zdmmv_status dmmv_entry(int fmt, const void *w, zdmmv_layout layout, int64_t rows, int64_t cols, const void *xq,
+                        int batch, float *y, cudaStream_t st) {
+    zdmmv_status s = check_matrix(fmt, w, layout, rows, cols, xq, y);
+    if (s != ZDMMV_OK) return s;
+    if (batch < 1 || batch > ZDMMV_MAX_BATCH) return ZDMMV_ERR_SHAPE;
+    if (rows == 0) return ZDMMV_OK;
+    DmmvArgs a{};
+    a.w = static_cast<const uint8_t *>(w);
+    a.xq = static_cast<const uint8_t *>(xq);
+    a.y = y;
+    a.rows = rows;
+    a.nb = static_cast<int32_t>(cols / kQK);
+    const int64_t cols_pad = cols;
+    (void)cols_pad;
+    if (tma_shape_ok(fmt, cols)) {
+        // batch vectors as slots of the pipelined kernel: slot v reads
+        // activation v and writes output row block v
+        a.batch = 1;
+        a.xq_stride = static_cast<int64_t>(a.nb) * 34;
+        a.y_stride = rows;
+        return run_dmmv(fmt, layout, a, batch, st);
+    }
+    a.batch = batch;
+    return run_dmmv(fmt, layout, a, 1, st);
+}
+
+}  // namespace
+}  // namespace zdmmv
+
+using namespace zdmmv;
+
+// =================================================================== C ABI
+extern "C" {
+
+const char *zdmmv_status_str(zdmmv_status st) {
+    switch (st) {
+    case ZDMMV_OK: return "ok";
+    case ZDMMV_ERR_NULL: return "null pointer";
+    case ZDMMV_ERR_SHAPE: return "bad shape";
+    case ZDMMV_ERR_ALIGN: return "misaligned pointer or stride";
+    case ZDMMV_ERR_LAYOUT: return "unknown layout";
+    case ZDMMV_ERR_FORMAT: return "unknown block format";
+    case ZDMMV_ERR_SIZE: return "buffer too small";
+    case ZDMMV_ERR_CUDA: return "CUDA runtime error";
+    case ZDMMV_ERR_DEVICE: return "device fault reported";
+    }
+    return "unknown status";
+}
+
+const char *zdmmv_version(void) { return "zdmmv 0.1 (sm_103a)"; }
+
+size_t zdmmv_block_bytes(zdmmv_fmt fmt) { return static_cast<size_t>(block_bytes(fmt)); }
+
+zdmmv_status zdmmv_quantize_act_q8_0(const float *x, int64_t k, void *xq, zdmmv_stream_t stream) {
+    if (k < 0 || k % kQK) return ZDMMV_ERR_SHAPE;
+    if (k == 0) return ZDMMV_OK;
+    if (!x || !xq) return ZDMMV_ERR_NULL;
+    if (!aligned(x, 4)) return ZDMMV_ERR_ALIGN;
+    const int64_t nblocks = k / kQK;
+    const int64_t ctas = (nblocks + 7) / 8;
+    if (ctas > 0x7fffffff) return ZDMMV_ERR_SHAPE;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(ctas), 1, 1);
+    cfg.blockDim = dim3(256, 1, 1);
+    cfg.stream = reinterpret_cast<cudaStream_t>(stream);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl_enabled() ? 1 : 0;
+    return from_cuda(cudaLaunchKernelEx(&cfg, quantize_q8_0_kernel, x, nblocks, static_cast<uint8_t *>(xq)));
+}
+
+zdmmv_status zdmmv_q8_0(const void *w, zdmmv_layout layout, int64_t rows, int64_t cols, const void *xq, float *y,
+                        zdmmv_stream_t stream) {
+    return dmmv_entry(kFmtQ8, w, layout, rows, cols, xq, 1, y, reinterpret_cast<cudaStream_t>(stream));
+}
+
+zdmmv_status zdmmv_q4_0(const void *w, zdmmv_layout layout, int64_t rows, int64_t cols, const void *xq, float *y,
+                        zdmmv_stream_t stream) {
+    return dmmv_entry(kFmtQ4, w, layout, rows, cols, xq, 1, y, reinterpret_cast<cudaStream_t>(stream));
+}
+
+zdmmv_status zdmmv_q8_0_batched(const void *w, zdmmv_layout layout, int64_t rows, int64_t cols, const void *xq,
+                                int batch, float *y, zdmmv_stream_t stream) {
+    return dmmv_entry(kFmtQ8, w, layout, rows, cols, xq, batch, y, reinterpret_cast<cudaStream_t>(stream));
+}
+
+zdmmv_status zdmmv_q4_0_batched(const void *w, zdmmv_layout layout, int64_t rows, int64_t cols, const void *xq,
+                                int batch, float *y, zdmmv_stream_t stream) {
+    return dmmv_entry(kFmtQ4, w, layout, rows, cols, xq, batch, y, reinterpret_cast<cudaStream_t>(stream));
+}
+
+zdmmv_status zdmmv_expert_gather(zdmmv_fmt fmt, const void *w_stack, int64_t expert_stride_bytes,
+                                 zdmmv_layout layout, int64_t rows, int64_t cols, const int32_t *idx, int n,
+                                 int n_experts, const void *xq, int64_t xq_stride_bytes, float *y,
+                                 int32_t *status_dev, zdmmv_stream_t stream) {
+    zdmmv_status s = check_matrix(fmt, w_stack, layout, rows, cols, xq, y);
+    if (s != ZDMMV_OK) return s;
+    if (n < 0 || n > 65535 || n_experts < 0) return ZDMMV_ERR_SHAPE;
+    if (n == 0 || rows == 0) return ZDMMV_OK;
+    if (!idx) return ZDMMV_ERR_NULL;
+    if (!aligned(idx, 4) || (status_dev && !aligned(status_dev, 4))) return ZDMMV_ERR_ALIGN;
+    const int64_t nb = cols / kQK;
+    const int64_t mat_bytes = rows * nb * block_bytes(fmt);
+    if (expert_stride_bytes < 0 || xq_stride_bytes < 0) return ZDMMV_ERR_SHAPE;
+    if (n_experts > 1 && expert_stride_bytes < mat_bytes) return ZDMMV_ERR_SHAPE;
+    if (xq_stride_bytes != 0 && xq_stride_bytes < nb * 34) return ZDMMV_ERR_SHAPE;
+    if (expert_stride_bytes % 16 || xq_stride_bytes % 16) return ZDMMV_ERR_ALIGN;
+    DmmvArgs a{};
+    a.w = static_cast<const uint8_t *>(w_stack);
+    a.expert_stride = expert_stride_bytes;
+    a.idx = idx;
+    a.n_experts = n_experts;
+    a.status = status_dev;
+    a.xq = static_cast<const uint8_t *>(xq);
+    a.xq_stride = xq_stride_bytes;
+    a.y = y;
+    a.y_stride = rows;
+    a.rows = rows;
+    a.nb = static_cast<int32_t>(nb);
+    a.batch = 1;
+    return run_dmmv(fmt, layout, a, n, reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t zdmmv_repacked_bytes(zdmmv_fmt fmt, int64_t rows, int64_t cols) {
+    if (block_bytes(fmt) == 0 || rows < 0 || cols <= 0 || cols % kQK) return 0;
+    return static_cast<size_t>(rows * (cols / kQK) * block_bytes(fmt));
+}
+
+zdmmv_status zdmmv_repack(zdmmv_fmt fmt, const void *src, int64_t rows, int64_t cols, void *dst, size_t dst_bytes,
+                          zdmmv_stream_t stream) {
+    if (block_bytes(fmt) == 0) return ZDMMV_ERR_FORMAT;
+    if (rows < 0 || cols <= 0 || cols % kQK) return ZDMMV_ERR_SHAPE;
+    if (rows == 0) return ZDMMV_OK;
+    if (!src || !dst) return ZDMMV_ERR_NULL;
+    if (!aligned(src, 16) || !aligned(dst, 16)) return ZDMMV_ERR_ALIGN;
+    const size_t need = zdmmv_repacked_bytes(fmt, rows, cols);
+    if (dst_bytes < need) return ZDMMV_ERR_SIZE;
+    const uint8_t *s8 = static_cast<const uint8_t *>(src);
+    uint8_t *d8 = static_cast<uint8_t *>(dst);
+    if (s8 < d8 + need && d8 < s8 + need) return ZDMMV_ERR_SHAPE;  // overlapping buffers
+    const int64_t nblocks = rows * (cols / kQK);
+    const int64_t ctas = (nblocks + 255) / 256;
+    if (ctas > 0x7fffffff) return ZDMMV_ERR_SHAPE;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (fmt == ZDMMV_Q8_0)
+        repack_kernel<kFmtQ8><<<static_cast<unsigned>(ctas), 256, 0, st>>>(s8, nblocks, d8);
+    else
+        repack_kernel<kFmtQ4><<<static_cast<unsigned>(ctas), 256, 0, st>>>(s8, nblocks, d8);
+    return from_cuda(cudaGetLastError());
+}
+
+size_t zdmmv_host_step_workspace_bytes(int64_t rows, int64_t cols, int batch) {
+    if (rows < 0 || cols <= 0 || cols % kQK || batch < 1 || batch > ZDMMV_MAX_BATCH) return 0;
+    const int64_t xb = round_up(static_cast<int64_t>(batch) * cols * 4, 256);
+    const int64_t qb = round_up(static_cast<int64_t>(batch) * (cols / kQK) * 34, 256);
+    const int64_t yb = round_up(static_cast<int64_t>(batch) * rows * 4, 256);
+    return static_cast<size_t>(xb + qb + yb);
+}
+
+zdmmv_status zdmmv_host_step(zdmmv_fmt fmt, const void *w, zdmmv_layout layout, int64_t rows, int64_t cols,
+                             const float *x_host, int batch, float *y_host, void *workspace_dev,
+                             size_t workspace_bytes, zdmmv_stream_t stream) {
+    if (block_bytes(fmt) == 0) return ZDMMV_ERR_FORMAT;
+    if (rows < 0 || cols <= 0 || cols % kQK || batch < 1 || batch > ZDMMV_MAX_BATCH) return ZDMMV_ERR_SHAPE;
+    if (!w || !x_host || !y_host || !workspace_dev) return ZDMMV_ERR_NULL;
+    if (!aligned(workspace_dev, 16)) return ZDMMV_ERR_ALIGN;
+    if (workspace_bytes < zdmmv_host_step_workspace_bytes(rows, cols, batch)) return ZDMMV_ERR_SIZE;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    uint8_t *ws = static_cast<uint8_t *>(workspace_dev);
+    const int64_t xb = round_up(static_cast<int64_t>(batch) * cols * 4, 256);
+    const int64_t qb = round_up(static_cast<int64_t>(batch) * (cols / kQK) * 34, 256);
+    float *xd = reinterpret_cast<float *>(ws);
+    uint8_t *xqd = ws + xb;
+    float *yd = reinterpret_cast<float *>(ws + xb + qb);
+    cudaError_t e = cudaMemcpyAsync(xd, x_host, static_cast<size_t>(batch) * cols * 4, cudaMemcpyHostToDevice, st);
+    if (e != cudaSuccess) return ZDMMV_ERR_CUDA;
+    zdmmv_status s = zdmmv_quantize_act_q8_0(xd, static_cast<int64_t>(batch) * cols, xqd, stream);
+    if (s != ZDMMV_OK) return s;
+    s = dmmv_entry(fmt, w, layout, rows, cols, xqd, batch, yd, st);
+    if (s != ZDMMV_OK) return s;
+    if (rows > 0) {
+        e = cudaMemcpyAsync(y_host, yd, static_cast<size_t>(batch) * rows * 4, cudaMemcpyDeviceToHost, st);
+        if (e != cudaSuccess) return ZDMMV_ERR_CUDA;
+    }
+    return ZDMMV_OK;
+}
+
+zdmmv_status zdmmv_debug_block_sums(zdmmv_fmt fmt, const void *w, zdmmv_layout layout, int64_t rows, int64_t cols,
+                                    const void *xq, int32_t *sums, zdmmv_stream_t stream) {
+    zdmmv_status s = check_matrix(fmt, w, layout, rows, cols, xq, reinterpret_cast<const float *>(sums));
+    if (s != ZDMMV_OK) return s;
+    if (rows == 0) return ZDMMV_OK;
+    const int nb = static_cast<int>(cols / kQK);
+    const bool pairs = tma_shape_ok(fmt, cols);
+    const int64_t threads = pairs ? rows * (nb / 2) : rows * nb;
+    const int64_t ctas = (threads + 255) / 256;
+    if (ctas > 0x7fffffff) return ZDMMV_ERR_SHAPE;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const uint8_t *w8 = static_cast<const uint8_t *>(w);
+    const uint8_t *x8 = static_cast<const uint8_t *>(xq);
+    const unsigned g = static_cast<unsigned>(ctas);
+#define ZDMMV_SUMS(F, L, PR) block_sums_kernel<F, L, PR><<<g, 256, 0, st>>>(w8, rows, nb, x8, sums)
+    if (fmt == ZDMMV_Q8_0) {
+        if (layout == ZDMMV_LAYOUT_GGUF) {
+            if (pairs) ZDMMV_SUMS(kFmtQ8, kLayoutGguf, true); else ZDMMV_SUMS(kFmtQ8, kLayoutGguf, false);
+        } else {
+            if (pairs) ZDMMV_SUMS(kFmtQ8, kLayoutRepacked, true); else ZDMMV_SUMS(kFmtQ8, kLayoutRepacked, false);
+        }
+    } else {
+        if (layout == ZDMMV_LAYOUT_GGUF) {
+            if (pairs) ZDMMV_SUMS(kFmtQ4, kLayoutGguf, true); else ZDMMV_SUMS(kFmtQ4, kLayoutGguf, false);
+        } else {
+            if (pairs) ZDMMV_SUMS(kFmtQ4, kLayoutRepacked, true); else ZDMMV_SUMS(kFmtQ4, kLayoutRepacked, false);
+        }
+    }
+#undef ZDMMV_SUMS
+    return from_cuda(cudaGetLastError());
+}
+
+zdmmv_status zdmmv_selftest_dp4a(const int32_t *a, const int32_t *b, const int32_t *c, int32_t *out, int n,
+                                 zdmmv_stream_t stream) {
+    if (n < 0) return ZDMMV_ERR_SHAPE;
+    if (n == 0) return ZDMMV_OK;
+    if (!a || !b || !c || !out) return ZDMMV_ERR_NULL;
+    selftest_dp4a_kernel<<<(n + 255) / 256, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(a, b, c, out, n);
+    return from_cuda(cudaGetLastError());
+}
+
+zdmmv_status zdmmv_device_status(uint32_t *bits_out, int clear) {
+    if (!bits_out) return ZDMMV_ERR_NULL;
+    if (cudaDeviceSynchronize() != cudaSuccess) return ZDMMV_ERR_CUDA;
+    uint32_t v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_fault_word, sizeof(v)) != cudaSuccess) return ZDMMV_ERR_CUDA;
+    if (clear) {
+        const uint32_t z = 0;
+        if (cudaMemcpyToSymbol(g_fault_word, &z, sizeof(z)) != cudaSuccess) return ZDMMV_ERR_CUDA;
+    }
+    *bits_out = v;
+    return ZDMMV_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,448 @@
+// zdmmv_device.cuh -- device building blocks of the GB300 (sm_103a) decode DMMV.
+//
+// * inline-PTX wrappers for mbarriers, the bulk (TMA) global->shared copy and
+//   the mixed-signedness packed int8x4 dot product;
+// * the block arithmetic: for every (format, layout) pair a "Pair" type that
+//   holds one lane's slice of the Q8_0 activation in registers and turns the
+//   weight words of two consecutive blocks into the two int32 block sums and
+//   their fp32 contribution.
+//
+// Block arithmetic (per 32-element block, int32, exact):
+//   Q8_0:  s = sum_i qw_i * qx_i                        (8 x dp4a)
+//   Q4_0:  s = sum_i (q_i - 8) * qx_i
+//            = sum_{j<16} lo(qs_j)*qx_j + sum_{j<16} hi(qs_j)*qx_{j+16} - 8*sum_i qx_i
+// and per block the fp32 update acc = fma(float(s), d_w*d_x, acc) where
+// d_w*d_x of two fp16 values is exact in fp32 and |s| <= 32*128*127 < 2^24 is
+// exact as a float. The int8x4 dot is the operation the pages build every
+// quantized matvec on ("Bringing ZINC to NVIDIA: a CUDA backend", section "The
+// reassuring result: ZINC's matmuls are __dp4a, not tensor cores"); the -8
+// offset of Q4_0 is the Q4 unpack in the habr ZINC article, "Что такое DMMV".
+//
+// GGUF array-of-blocks rows put a block every 34 (Q8_0) or 18 (Q4_0) bytes, so
+// half the blocks start 2 bytes off a 4-byte boundary. Instead of realigning the
+// weight words (a byte permute per word), a lane owns PAIRS of blocks (68 or 36
+// bytes, always 4-byte aligned when the row is) and holds its activation words
+// pre-shifted to the weight words' alignment, with zero bytes facing the fp16
+// scale bytes: the dp4a of a scale byte with a zero contributes nothing, so the
+// unaligned block needs no permutes at all.
+#pragma once
+
+#include <cstdint>
+#include <cuda_fp16.h>
+
+namespace zdmmv {
+
+constexpr int kQK = 32;
+constexpr int kFmtQ4 = 2;
+constexpr int kFmtQ8 = 8;
+constexpr int kLayoutGguf = 0;
+constexpr int kLayoutRepacked = 1;
+
+template <int FMT> struct Fmt;
+template <> struct Fmt<kFmtQ8> { static constexpr int kBlockBytes = 34; static constexpr int kQuantBytes = 32; };
+template <> struct Fmt<kFmtQ4> { static constexpr int kBlockBytes = 18; static constexpr int kQuantBytes = 16; };
+
+// ------------------------------------------------------------------ PTX
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// unsigned bytes of a times signed bytes of b, accumulated into c (int32)
+__device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
+    int d;
+    asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+__device__ __forceinline__ int dp4a_ss(uint32_t a, uint32_t b, int c) {
+    return __dp4a(static_cast<int>(a), static_cast<int>(b), c);
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_barrier_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+__device__ __forceinline__ uint64_t global_timer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Every wait in this library is bounded: after this long the waiter gives up,
+// the kernel records ZDMMV_FAULT_WAIT_TIMEOUT and returns instead of hanging.
+constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s
+
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+    }
+    return true;
+}
+
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+__device__ __forceinline__ uint64_t l2_evict_last_policy() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+// Bulk (non-tensor) TMA copy global -> this CTA's shared memory, completing
+// `bytes` of transaction count on `bar`. dst, src 16-byte aligned, bytes a
+// multiple of 16.
+__device__ __forceinline__ void bulk_copy_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar,
+                                              uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1], %2, [%3], %4;" ::"r"(smem_addr(dst)),
+        "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
+        : "memory");
+}
+
+// fp16 bits held in the low / high half of a 32-bit word, as float (exact)
+__device__ __forceinline__ float half_lo(uint32_t w) {
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(w & 0xffffu)));
+}
+__device__ __forceinline__ float half_hi(uint32_t w) {
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(w >> 16)));
+}
+
+// bytes 2,3 of a followed by bytes 0,1 of b: a 4-byte window shifted by 2 bytes
+__device__ __forceinline__ uint32_t shift2(uint32_t a, uint32_t b) { return __byte_perm(a, b, 0x5432); }
+
+constexpr uint32_t kLoNib = 0x0f0f0f0fu;
+constexpr uint32_t kHiNib = 0xf0f0f0f0u;
+constexpr uint32_t kOnes = 0x01010101u;
+
+// Sum of the 32 int8 codes of an activation block, times -8 (the Q4_0 offset
+// term), from its eight aligned code words.
+__device__ __forceinline__ int q4_offset_term(const uint32_t (&xw)[8]) {
+    int s = 0;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) s = dp4a_ss(xw[k], kOnes, s);
+    return -8 * s;
+}
+
+// Load the 17 words of the activation pair p (blocks 2p, 2p+1; 68 bytes at a
+// 4-byte aligned offset) from Q8_0 activation blocks at `xq`.
+__device__ __forceinline__ void load_x_pair_words(const uint8_t *xq, int p, uint32_t (&v)[17]) {
+    const uint32_t *src = reinterpret_cast<const uint32_t *>(xq + 68 * p);
+#pragma unroll
+    for (int k = 0; k < 17; ++k) v[k] = src[k];
+}
+
+// Aligned code words of the two activation blocks of a pair:
+// block A's 32 codes start at byte 2, block B's at byte 36 of the pair.
+__device__ __forceinline__ void x_aligned_words(const uint32_t (&v)[17], uint32_t (&xa)[8], uint32_t (&xb)[8]) {
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        xa[k] = shift2(v[k], v[k + 1]);
+        xb[k] = v[9 + k];
+    }
+}
+
+// -------------------------------------------------------------- Pair types
+// Pair<FMT, LAYOUT>: one lane's registers for one pair of blocks and the update
+//   acc = fma(float(sA), dwA*dxA, acc); acc = fma(float(sB), dwB*dxB, acc)
+// in that order. `sums()` returns the two int32 block sums (debug path).
+template <int FMT, int LAYOUT> struct Pair;
+
+// Q8_0, GGUF layout. Weight pair words w[0..16] (68 bytes):
+//   w0 = [dA dA a0 a1], w1..w7 = a2..a29, w8 = [a30 a31 dB dB], w9..w16 = b0..b31
+template <> struct Pair<kFmtQ8, kLayoutGguf> {
+    static constexpr int kWords = 17;
+    uint32_t x[17];  // x[0..8]: block A codes at w's alignment (zeros facing dA, dB); x[9..16]: block B
+    float dxa, dxb;
+
+    __device__ __forceinline__ void set(const uint32_t (&v)[17]) {
+        x[0] = v[0] & 0xffff0000u;
+#pragma unroll
+        for (int k = 1; k < 8; ++k) x[k] = v[k];
+        x[8] = v[8] & 0x0000ffffu;
+#pragma unroll
+        for (int k = 9; k < 17; ++k) x[k] = v[k];
+        dxa = half_lo(v[0]);
+        dxb = half_hi(v[8]);
+    }
+    __device__ __forceinline__ void sums(const uint32_t *w, int &sa, int &sb) const {
+        sa = 0;
+        sb = 0;
+#pragma unroll
+        for (int k = 0; k < 9; ++k) sa = dp4a_ss(w[k], x[k], sa);
+#pragma unroll
+        for (int k = 9; k < 17; ++k) sb = dp4a_ss(w[k], x[k], sb);
+    }
+    // w: the pair's 17 weight words (shared memory)
+    __device__ __forceinline__ float fma_pair(const uint32_t *w, float acc) const {
+        uint32_t r[17];
+#pragma unroll
+        for (int k = 0; k < 17; ++k) r[k] = w[k];
+        int sa, sb;
+        sums(r, sa, sb);
+        acc = __fmaf_rn(static_cast<float>(sa), __fmul_rn(half_lo(r[0]), dxa), acc);
+        acc = __fmaf_rn(static_cast<float>(sb), __fmul_rn(half_hi(r[8]), dxb), acc);
+        return acc;
+    }
+};
+
+// Q4_0, GGUF layout. Weight pair words w[0..8] (36 bytes):
+//   w0 = [dA dA qa0 qa1], w1..w3 = qa2..qa13, w4 = [qa14 qa15 dB dB], w5..w8 = qb0..qb15
+// low nibble of qa_j is element j, high nibble element j+16.
+template <> struct Pair<kFmtQ4, kLayoutGguf> {
+    static constexpr int kWords = 9;
+    uint32_t xlo[9];  // [0..4]: codes facing the low nibbles of w0..w4 (block A), [5..8]: w5..w8 (block B)
+    uint32_t xhi[9];  // the same for the high nibbles
+    int inita, initb; // -8 * sum of the block's codes
+    float dxa, dxb;
+
+    __device__ __forceinline__ void set(const uint32_t (&v)[17]) {
+        // activation pair bytes: v0 = [dxA dxA x0 x1], v_k = x(4k-2)..x(4k+1), v8 = [x30 x31 dxB dxB]
+        xlo[0] = v[0] & 0xffff0000u;         // [0 0 x0 x1]
+        xlo[1] = v[1];                       // x2..x5
+        xlo[2] = v[2];
+        xlo[3] = v[3];
+        xlo[4] = v[4] & 0x0000ffffu;         // [x14 x15 0 0]
+        xhi[0] = v[4] & 0xffff0000u;         // [0 0 x16 x17]
+        xhi[1] = v[5];
+        xhi[2] = v[6];
+        xhi[3] = v[7];
+        xhi[4] = v[8] & 0x0000ffffu;         // [x30 x31 0 0]
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            xlo[5 + k] = v[9 + k];           // block B codes 0..15
+            xhi[5 + k] = v[13 + k];          // block B codes 16..31
+        }
+        uint32_t xa[8], xb[8];
+        x_aligned_words(v, xa, xb);
+        inita = q4_offset_term(xa);
+        initb = q4_offset_term(xb);
+        dxa = half_lo(v[0]);
+        dxb = half_hi(v[8]);
+    }
+    __device__ __forceinline__ void sums(const uint32_t *w, int &sa, int &sb) const {
+        int la = inita, ha = 0, lb = initb, hb = 0;
+#pragma unroll
+        for (int k = 0; k < 5; ++k) {
+            la = dp4a_ss(w[k] & kLoNib, xlo[k], la);
+            ha = dp4a_us(w[k] & kHiNib, xhi[k], ha);
+        }
+#pragma unroll
+        for (int k = 5; k < 9; ++k) {
+            lb = dp4a_ss(w[k] & kLoNib, xlo[k], lb);
+            hb = dp4a_us(w[k] & kHiNib, xhi[k], hb);
+        }
+        // high nibbles were multiplied in place (16*q): exact division by 16
+        sa = la + (ha >> 4);
+        sb = lb + (hb >> 4);
+    }
+    __device__ __forceinline__ float fma_pair(const uint32_t *w, float acc) const {
+        uint32_t r[9];
+#pragma unroll
+        for (int k = 0; k < 9; ++k) r[k] = w[k];
+        int sa, sb;
+        sums(r, sa, sb);
+        acc = __fmaf_rn(static_cast<float>(sa), __fmul_rn(half_lo(r[0]), dxa), acc);
+        acc = __fmaf_rn(static_cast<float>(sb), __fmul_rn(half_hi(r[4]), dxb), acc);
+        return acc;
+    }
+};
+
+// Q8_0, repacked layout: 16 aligned quant words (block A words 0..7, block B
+// 8..15) plus one scale word (dA low half, dB high half).
+template <> struct Pair<kFmtQ8, kLayoutRepacked> {
+    static constexpr int kWords = 16;
+    uint32_t x[16];
+    float dxa, dxb;
+
+    __device__ __forceinline__ void set(const uint32_t (&v)[17]) {
+        uint32_t xa[8], xb[8];
+        x_aligned_words(v, xa, xb);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            x[k] = xa[k];
+            x[8 + k] = xb[k];
+        }
+        dxa = half_lo(v[0]);
+        dxb = half_hi(v[8]);
+    }
+    __device__ __forceinline__ void sums(const uint32_t *wq, int &sa, int &sb) const {
+        sa = 0;
+        sb = 0;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) sa = dp4a_ss(wq[k], x[k], sa);
+#pragma unroll
+        for (int k = 8; k < 16; ++k) sb = dp4a_ss(wq[k], x[k], sb);
+    }
+    // wq: 16 quant words (16-byte aligned); ws: the pair's scale word
+    __device__ __forceinline__ float fma_pair(const uint32_t *wq, uint32_t ws, float acc) const {
+        uint32_t r[16];
+        const uint4 *q4 = reinterpret_cast<const uint4 *>(wq);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const uint4 t = q4[k];
+            r[4 * k] = t.x;
+            r[4 * k + 1] = t.y;
+            r[4 * k + 2] = t.z;
+            r[4 * k + 3] = t.w;
+        }
+        int sa, sb;
+        sums(r, sa, sb);
+        acc = __fmaf_rn(static_cast<float>(sa), __fmul_rn(half_lo(ws), dxa), acc);
+        acc = __fmaf_rn(static_cast<float>(sb), __fmul_rn(half_hi(ws), dxb), acc);
+        return acc;
+    }
+};
+
+// Q4_0, repacked layout: 8 aligned quant words (block A qs words 0..3, block B
+// 4..7) plus one scale word.
+template <> struct Pair<kFmtQ4, kLayoutRepacked> {
+    static constexpr int kWords = 8;
+    uint32_t xlo[8], xhi[8];
+    int inita, initb;
+    float dxa, dxb;
+
+    __device__ __forceinline__ void set(const uint32_t (&v)[17]) {
+        uint32_t xa[8], xb[8];
+        x_aligned_words(v, xa, xb);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            xlo[k] = xa[k];
+            xhi[k] = xa[4 + k];
+            xlo[4 + k] = xb[k];
+            xhi[4 + k] = xb[4 + k];
+        }
+        inita = q4_offset_term(xa);
+        initb = q4_offset_term(xb);
+        dxa = half_lo(v[0]);
+        dxb = half_hi(v[8]);
+    }
+    __device__ __forceinline__ void sums(const uint32_t *wq, int &sa, int &sb) const {
+        int la = inita, ha = 0, lb = initb, hb = 0;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            la = dp4a_ss(wq[k] & kLoNib, xlo[k], la);
+            ha = dp4a_us(wq[k] & kHiNib, xhi[k], ha);
+            lb = dp4a_ss(wq[4 + k] & kLoNib, xlo[4 + k], lb);
+            hb = dp4a_us(wq[4 + k] & kHiNib, xhi[4 + k], hb);
+        }
+        sa = la + (ha >> 4);
+        sb = lb + (hb >> 4);
+    }
+    __device__ __forceinline__ float fma_pair(const uint32_t *wq, uint32_t ws, float acc) const {
+        uint32_t r[8];
+        const uint4 *q4 = reinterpret_cast<const uint4 *>(wq);
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            const uint4 t = q4[k];
+            r[4 * k] = t.x;
+            r[4 * k + 1] = t.y;
+            r[4 * k + 2] = t.z;
+            r[4 * k + 3] = t.w;
+        }
+        int sa, sb;
+        sums(r, sa, sb);
+        acc = __fmaf_rn(static_cast<float>(sa), __fmul_rn(half_lo(ws), dxa), acc);
+        acc = __fmaf_rn(static_cast<float>(sb), __fmul_rn(half_hi(ws), dxb), acc);
+        return acc;
+    }
+};
+
+// ------------------------------------------------- single-block (plain path)
+// Blocks at any 2-byte aligned address: 16-bit loads, aligned words assembled
+// in registers. Used by the plain kernel (shapes the pipelined kernel does not
+// take) and by its debug counterpart.
+__device__ __forceinline__ uint32_t ld_u16_pair(const uint16_t *p) {
+    return static_cast<uint32_t>(p[0]) | (static_cast<uint32_t>(p[1]) << 16);
+}
+
+// activation block at xb (34 bytes, 2-byte aligned): aligned code words + scale
+__device__ __forceinline__ void load_x_block(const uint8_t *xb, uint32_t (&xw)[8], float &dx) {
+    const uint16_t *h = reinterpret_cast<const uint16_t *>(xb);
+    dx = __half2float(__ushort_as_half(h[0]));
+#pragma unroll
+    for (int k = 0; k < 8; ++k) xw[k] = ld_u16_pair(h + 1 + 2 * k);
+}
+
+template <int FMT> struct Block;
+
+template <> struct Block<kFmtQ8> {
+    // quant words from a GGUF block (2-byte aligned) or an aligned repacked slot
+    __device__ __forceinline__ static void load_gguf(const uint8_t *blk, uint32_t (&q)[8], float &d) {
+        const uint16_t *h = reinterpret_cast<const uint16_t *>(blk);
+        d = __half2float(__ushort_as_half(h[0]));
+#pragma unroll
+        for (int k = 0; k < 8; ++k) q[k] = ld_u16_pair(h + 1 + 2 * k);
+    }
+    __device__ __forceinline__ static void load_repacked(const uint8_t *qs, const uint8_t *sc, uint32_t (&q)[8],
+                                                         float &d) {
+        const uint32_t *w = reinterpret_cast<const uint32_t *>(qs);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) q[k] = w[k];
+        d = __half2float(__ushort_as_half(*reinterpret_cast<const uint16_t *>(sc)));
+    }
+    __device__ __forceinline__ static int dot(const uint32_t (&q)[8], const uint32_t (&xw)[8]) {
+        int s = 0;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) s = dp4a_ss(q[k], xw[k], s);
+        return s;
+    }
+};
+
+template <> struct Block<kFmtQ4> {
+    __device__ __forceinline__ static void load_gguf(const uint8_t *blk, uint32_t (&q)[8], float &d) {
+        const uint16_t *h = reinterpret_cast<const uint16_t *>(blk);
+        d = __half2float(__ushort_as_half(h[0]));
+#pragma unroll
+        for (int k = 0; k < 4; ++k) q[k] = ld_u16_pair(h + 1 + 2 * k);
+#pragma unroll
+        for (int k = 4; k < 8; ++k) q[k] = 0;
+    }
+    __device__ __forceinline__ static void load_repacked(const uint8_t *qs, const uint8_t *sc, uint32_t (&q)[8],
+                                                         float &d) {
+        const uint32_t *w = reinterpret_cast<const uint32_t *>(qs);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) q[k] = w[k];
+#pragma unroll
+        for (int k = 4; k < 8; ++k) q[k] = 0;
+        d = __half2float(__ushort_as_half(*reinterpret_cast<const uint16_t *>(sc)));
+    }
+    // q[0..3]: the 16 qs bytes; element j = low nibble of qs_j, element j+16 = high nibble
+    __device__ __forceinline__ static int dot(const uint32_t (&q)[8], const uint32_t (&xw)[8]) {
+        int lo = q4_offset_term(xw), hi = 0;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            lo = dp4a_ss(q[k] & kLoNib, xw[k], lo);
+            hi = dp4a_ss((q[k] >> 4) & kLoNib, xw[4 + k], hi);
+        }
+        return lo + hi;
+    }
+};
+
+}  // namespace zdmmv

@@ -1,0 +1,61 @@
+// zdmmv_internal.h -- host-side declarations shared by the translation units of
+// libzdmmv.so (not part of the public C ABI; see include/zdmmv.h for that).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace zdmmv {
+
+// Arguments of the DMMV kernels (passed by value, like a push-constant block).
+// One "slot" per blockIdx.y: slot k reads matrix w (+ idx[k]*expert_stride when
+// idx is set), activation xq + k*xq_stride and writes y + k*y_stride.
+struct DmmvArgs {
+    const uint8_t *w;        // matrix base (GGUF blocks, or repacked quant stream + scales)
+    int64_t expert_stride;   // bytes between stacked matrices (gather)
+    const int32_t *idx;      // device expert index per slot, or nullptr
+    int32_t n_experts;       // valid index range [0, n_experts)
+    int32_t *status;         // nullable: 1 is stored here for a bad index
+    uint32_t *fault;         // device fault word (ZDMMV_FAULT_* bits)
+    const uint8_t *xq;       // Q8_0 activation blocks of slot 0
+    int64_t xq_stride;       // bytes between slots' activations (0 = shared)
+    float *y;                // output of slot 0
+    int64_t y_stride;        // floats between slots' outputs
+    int64_t rows;            // rows of the matrix
+    int32_t nb;              // blocks per row
+    int32_t batch;           // activation vectors per slot (plain kernel only)
+    int32_t tile_rows;       // rows per pipeline stage (pipelined kernel)
+    int32_t stage_bytes;     // shared-memory bytes per stage (pipelined kernel)
+    int32_t x_bytes_padded;  // shared-memory bytes of the staged activation
+};
+
+// Launch description chosen by the host for the pipelined kernel.
+struct TmaPlan {
+    int lpr;         // lanes that share one row
+    int ppl;         // block pairs per lane
+    int stages;      // pipeline depth
+    int tile_rows;   // rows per stage
+    int stage_bytes;
+    int x_bytes_padded;
+    int smem_bytes;  // dynamic shared memory per CTA
+};
+
+constexpr int kConsumerThreads = 256;  // 8 consumer warps
+constexpr int kProducerThreads = 32;   // 1 producer warp (one lane issues the copies)
+constexpr int kTmaThreads = kConsumerThreads + kProducerThreads;
+constexpr int kBarrierBytes = 256;     // shared-memory prefix holding the mbarriers
+
+// Whether the pipelined kernel takes this shape, and its plan.
+bool tma_shape_ok(int fmt, int64_t cols);
+TmaPlan tma_plan(int fmt, int layout, int64_t cols);
+
+// Launchers of the pipelined kernel (one translation unit per format).
+cudaError_t launch_tma_q8(const DmmvArgs &a, const TmaPlan &p, int layout, int ctas_per_slot, int slots,
+                          cudaStream_t st, bool pdl);
+cudaError_t launch_tma_q4(const DmmvArgs &a, const TmaPlan &p, int layout, int ctas_per_slot, int slots,
+                          cudaStream_t st, bool pdl);
+// CTAs of the pipelined kernel that fit on one SM for this plan.
+int tma_ctas_per_sm_q8(int layout, const TmaPlan &p);
+int tma_ctas_per_sm_q4(int layout, const TmaPlan &p);
+
+}  // namespace zdmmv

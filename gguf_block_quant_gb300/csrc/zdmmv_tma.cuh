@@ -1,0 +1,309 @@
+// zdmmv_tma.cuh -- the TMA-pipelined decode DMMV kernel for sm_103a.
+//
+// Design (one CTA = 8 consumer warps + 1 producer warp, several CTAs per SM):
+//  * Each CTA owns a contiguous range of rows. In GGUF layout consecutive rows
+//    are consecutive bytes, so a tile of T rows is ONE contiguous chunk and is
+//    fetched with a single bulk TMA copy (cp.async.bulk) into a shared-memory
+//    stage; the repacked layout takes one copy for the quants and one for the
+//    scales. The weight stream is read from HBM exactly once, with an
+//    evict-first L2 policy (it is never re-read).
+//  * The producer lane keeps STAGES tiles in flight (full/empty mbarrier pairs);
+//    the 8 consumer warps never wait on global memory, only on a stage.
+//  * The Q8_0 activation (at most a few KB) is staged once per CTA by one more
+//    bulk copy and then held in REGISTERS: lane l of a row group owns block
+//    pairs l, l+LPR, ... for every row, so the inner loop reads only weights
+//    from shared memory (the pages stage the input vector in LDS so that the
+//    weights own the cache: habr ZINC article, "Трюк с shared memory"; here the
+//    activation goes one level further, into registers).
+//  * LPR lanes share a row; their partial sums meet in an xor-shuffle tree
+//    (subgroupAdd -> __shfl reductions: "CUDA backend for ZINC", "4. Kernel port
+//    strategy"). The reduction order depends only on the row's contents, never
+//    on its position, so results are bitwise invariant under row permutation
+//    and identical for the same row in any call.
+//  * Every mbarrier wait is bounded (1 s); on a timeout the kernel sets the
+//    device fault word, drains its own copies (bounded) and returns.
+#pragma once
+
+#include "zdmmv_device.cuh"
+#include "zdmmv_internal.h"
+
+namespace zdmmv {
+
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <int FMT, int LAYOUT> struct RowGeom;
+template <int FMT> struct RowGeom<FMT, kLayoutGguf> {
+    static constexpr int kPairBytes = 2 * Fmt<FMT>::kBlockBytes;
+};
+template <int FMT> struct RowGeom<FMT, kLayoutRepacked> {
+    static constexpr int kPairQuantBytes = 2 * Fmt<FMT>::kQuantBytes;
+};
+
+// One lane's contribution to one row: pairs l, l+LPR, ... (fixed order).
+template <int FMT, int LAYOUT, int LPR, int PPL>
+__device__ __forceinline__ float row_partial(const Pair<FMT, LAYOUT> (&xr)[PPL], const uint8_t *stage, int i,
+                                             int tile_rows, int nb, int l) {
+    const int npairs = nb >> 1;
+    float acc = 0.0f;
+    if constexpr (LAYOUT == kLayoutGguf) {
+        const uint8_t *row = stage + static_cast<size_t>(i) * nb * Fmt<FMT>::kBlockBytes;
+#pragma unroll
+        for (int j = 0; j < PPL; ++j) {
+            const int p = l + j * LPR;
+            if (p < npairs)
+                acc = xr[j].fma_pair(reinterpret_cast<const uint32_t *>(row + p * RowGeom<FMT, LAYOUT>::kPairBytes),
+                                     acc);
+        }
+    } else {
+        const uint8_t *rq = stage + static_cast<size_t>(i) * nb * Fmt<FMT>::kQuantBytes;
+        const uint8_t *rs = stage + static_cast<size_t>(tile_rows) * nb * Fmt<FMT>::kQuantBytes +
+                            static_cast<size_t>(i) * nb * 2;
+#pragma unroll
+        for (int j = 0; j < PPL; ++j) {
+            const int p = l + j * LPR;
+            if (p < npairs) {
+                const uint32_t ws = *reinterpret_cast<const uint32_t *>(rs + 4 * p);
+                acc = xr[j].fma_pair(
+                    reinterpret_cast<const uint32_t *>(rq + p * RowGeom<FMT, LAYOUT>::kPairQuantBytes), ws, acc);
+            }
+        }
+    }
+    return acc;
+}
+
+template <int FMT, int LAYOUT, int LPR, int PPL, int STAGES, int MINB>
+__global__ void __launch_bounds__(kTmaThreads, MINB) dmmv_tma_kernel(const DmmvArgs a) {
+    using P = Pair<FMT, LAYOUT>;
+    constexpr int kRowsPar = kConsumerThreads / LPR;
+    constexpr int kBB = Fmt<FMT>::kBlockBytes;
+    constexpr int kQB = Fmt<FMT>::kQuantBytes;
+    static_assert(kConsumerThreads % LPR == 0 && LPR <= 32, "row groups must live inside a warp");
+
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem);
+    uint64_t *empty = full + STAGES;
+    uint64_t *xbar = empty + STAGES;
+    uint8_t *xs = smem + kBarrierBytes;
+    uint8_t *stage0 = xs + a.x_bytes_padded;
+
+    const int tid = threadIdx.x;
+    const int slot = blockIdx.y;
+    const int64_t rows = a.rows;
+    const int64_t r0 = rows * blockIdx.x / gridDim.x;
+    const int64_t r1 = rows * (blockIdx.x + 1) / gridDim.x;
+    const int nb = a.nb;
+
+    // everything below reads inputs a preceding kernel may have written
+    pdl_wait();
+    pdl_launch_dependents();
+
+    float *y = a.y + slot * a.y_stride;
+    const uint8_t *w = a.w;
+    if (a.idx != nullptr) {
+        const int e = a.idx[slot];
+        if (e < 0 || e >= a.n_experts) {
+            for (int64_t r = r0 + tid; r < r1; r += blockDim.x) y[r] = __int_as_float(0x7fc00000);
+            if (tid == 0 && a.status != nullptr) atomicExch(a.status, 1);
+            return;
+        }
+        w += static_cast<int64_t>(e) * a.expert_stride;
+    }
+    if (r1 <= r0) return;
+    const uint8_t *xq = a.xq + slot * a.xq_stride;
+    const int T = a.tile_rows;
+    const int ntiles = static_cast<int>((r1 - r0 + T - 1) / T);
+
+    if (tid == 0) {
+#pragma unroll
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kConsumerThreads / 32);
+        }
+        mbar_init(xbar, 1);
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    if (tid >= kConsumerThreads) {
+        // ------------------------------------------------------- producer
+        if (tid != kConsumerThreads) return;
+        const uint64_t wpol = l2_evict_first_policy();
+        const uint64_t xpol = l2_evict_last_policy();
+        const uint32_t xbytes = static_cast<uint32_t>(nb) * 34u;
+        mbar_arrive_expect_tx(xbar, xbytes);
+        bulk_copy_g2s(xs, xq, xbytes, xbar, xpol);
+        int issued = 0;
+        bool ok = true;
+        for (int t = 0; t < ntiles; ++t) {
+            const int s = t % STAGES;
+            if (t >= STAGES) {
+                if (!mbar_wait(&empty[s], static_cast<uint32_t>((t / STAGES) - 1) & 1u)) {
+                    ok = false;
+                    break;
+                }
+                fence_proxy_async_smem();
+            }
+            const int64_t tr0 = r0 + static_cast<int64_t>(t) * T;
+            const int nr = static_cast<int>(min(static_cast<int64_t>(T), r1 - tr0));
+            uint8_t *dst = stage0 + static_cast<size_t>(s) * a.stage_bytes;
+            if constexpr (LAYOUT == kLayoutGguf) {
+                const uint32_t bytes = static_cast<uint32_t>(nr) * static_cast<uint32_t>(nb) * kBB;
+                mbar_arrive_expect_tx(&full[s], bytes);
+                bulk_copy_g2s(dst, w + tr0 * nb * kBB, bytes, &full[s], wpol);
+            } else {
+                const uint32_t qbytes = static_cast<uint32_t>(nr) * static_cast<uint32_t>(nb) * kQB;
+                const uint32_t sbytes = static_cast<uint32_t>(nr) * static_cast<uint32_t>(nb) * 2u;
+                mbar_arrive_expect_tx(&full[s], qbytes + sbytes);
+                bulk_copy_g2s(dst, w + tr0 * nb * kQB, qbytes, &full[s], wpol);
+                bulk_copy_g2s(dst + static_cast<size_t>(T) * nb * kQB, w + rows * nb * kQB + tr0 * nb * 2, sbytes,
+                              &full[s], wpol);
+            }
+            issued = t + 1;
+        }
+        if (!ok) atomicOr(a.fault, 1u);
+        // Never leave while a copy into this CTA's shared memory is in flight:
+        // wait (bounded) for the last copy issued into every stage.
+        for (int s = 0; s < STAGES; ++s) {
+            const int t_last = (issued - 1 - s) >= 0 ? ((issued - 1 - s) / STAGES) * STAGES + s : -1;
+            if (t_last >= 0) (void)mbar_wait(&full[s], static_cast<uint32_t>(t_last / STAGES) & 1u);
+        }
+        (void)mbar_wait(xbar, 0);
+        return;
+    }
+
+    // ---------------------------------------------------------- consumers
+    const int lane = tid & 31;
+    const int g = tid / LPR;  // row group
+    const int l = tid % LPR;  // lane inside the row group
+    if (!mbar_wait(xbar, 0)) {
+        atomicOr(a.fault, 1u);
+        return;
+    }
+    P xr[PPL];
+#pragma unroll
+    for (int j = 0; j < PPL; ++j) {
+        const int p = l + j * LPR;
+        if (p < (nb >> 1)) {
+            uint32_t v[17];
+            load_x_pair_words(xs, p, v);
+            xr[j].set(v);
+        }
+    }
+
+    for (int t = 0; t < ntiles; ++t) {
+        const int s = t % STAGES;
+        if (!mbar_wait(&full[s], static_cast<uint32_t>(t / STAGES) & 1u)) {
+            atomicOr(a.fault, 1u);
+            return;
+        }
+        const uint8_t *st = stage0 + static_cast<size_t>(s) * a.stage_bytes;
+        const int64_t tr0 = r0 + static_cast<int64_t>(t) * T;
+        const int nr = static_cast<int>(min(static_cast<int64_t>(T), r1 - tr0));
+        for (int base = 0; base < nr; base += kRowsPar) {
+            const int i = base + g;
+            float acc = 0.0f;
+            if (i < nr) acc = row_partial<FMT, LAYOUT, LPR, PPL>(xr, st, i, T, nb, l);
+#pragma unroll
+            for (int o = LPR / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+            if (l == 0 && i < nr) y[tr0 + i] = acc;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+    }
+}
+
+// ------------------------------------------------------------------ host side
+template <int FMT, int LAYOUT, int LPR, int PPL, int STAGES>
+struct TmaInst {
+    static constexpr int kMinBlocks = PPL >= 4 ? 1 : 2;
+    static void *fn() { return reinterpret_cast<void *>(&dmmv_tma_kernel<FMT, LAYOUT, LPR, PPL, STAGES, kMinBlocks>); }
+
+    static cudaError_t prepare() {
+        // raise the dynamic shared-memory limit once per device
+        static bool done[64] = {};
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e != cudaSuccess) return e;
+        if (dev < 64 && done[dev]) return cudaSuccess;
+        int optin = 0;
+        e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+        if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(fn(), cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
+        if (e != cudaSuccess) return e;
+        if (dev < 64) done[dev] = true;
+        return cudaSuccess;
+    }
+
+    static cudaError_t launch(const DmmvArgs &a, const TmaPlan &p, int ctas_per_slot, int slots, cudaStream_t st,
+                              bool pdl) {
+        cudaError_t e = prepare();
+        if (e != cudaSuccess) return e;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned>(ctas_per_slot), static_cast<unsigned>(slots), 1);
+        cfg.blockDim = dim3(kTmaThreads, 1, 1);
+        cfg.dynamicSmemBytes = static_cast<size_t>(p.smem_bytes);
+        cfg.stream = st;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = pdl ? 1 : 0;
+        return cudaLaunchKernelEx(&cfg, dmmv_tma_kernel<FMT, LAYOUT, LPR, PPL, STAGES, kMinBlocks>, a);
+    }
+
+    static int ctas_per_sm(int smem_bytes) {
+        if (prepare() != cudaSuccess) return 1;
+        int occ = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, dmmv_tma_kernel<FMT, LAYOUT, LPR, PPL, STAGES, kMinBlocks>,
+                                                          kTmaThreads, static_cast<size_t>(smem_bytes)) != cudaSuccess)
+            return 1;
+        return occ > 0 ? occ : 1;
+    }
+};
+
+// Dispatch over the (lpr, ppl, stages) variants instantiated for one format.
+template <int FMT, int LAYOUT, typename F>
+cudaError_t with_variant(const TmaPlan &p, F &&f) {
+#define ZDMMV_VARIANT(LPR_, PPL_, ST_)                                        \
+    if (p.lpr == LPR_ && p.ppl == PPL_ && p.stages == ST_)                    \
+        return f(TmaInst<FMT, LAYOUT, LPR_, PPL_, ST_>{});
+    ZDMMV_VARIANT(8, 1, 4)
+    ZDMMV_VARIANT(16, 1, 4)
+    ZDMMV_VARIANT(32, 1, 4)
+    ZDMMV_VARIANT(32, 2, 4)
+    ZDMMV_VARIANT(32, 4, 4)
+    ZDMMV_VARIANT(8, 1, 3)
+    ZDMMV_VARIANT(16, 1, 3)
+    ZDMMV_VARIANT(32, 1, 3)
+    ZDMMV_VARIANT(32, 2, 3)
+    ZDMMV_VARIANT(32, 4, 3)
+#undef ZDMMV_VARIANT
+    return cudaErrorInvalidConfiguration;
+}
+
+template <int FMT>
+cudaError_t launch_tma_fmt(const DmmvArgs &a, const TmaPlan &p, int layout, int ctas_per_slot, int slots,
+                           cudaStream_t st, bool pdl) {
+    auto go = [&](auto inst) { return decltype(inst)::launch(a, p, ctas_per_slot, slots, st, pdl); };
+    if (layout == kLayoutGguf) return with_variant<FMT, kLayoutGguf>(p, go);
+    return with_variant<FMT, kLayoutRepacked>(p, go);
+}
+
+template <int FMT>
+int tma_ctas_per_sm_fmt(int layout, const TmaPlan &p) {
+    int occ = 1;
+    auto q = [&](auto inst) {
+        occ = decltype(inst)::ctas_per_sm(p.smem_bytes);
+        return cudaSuccess;
+    };
+    if (layout == kLayoutGguf)
+        (void)with_variant<FMT, kLayoutGguf>(p, q);
+    else
+        (void)with_variant<FMT, kLayoutRepacked>(p, q);
+    return occ;
+}
+
+}  // namespace zdmmv

@@ -55,12 +55,12 @@ def weight_blocks(fmt: int, rows: int, cols: int, seed: int, stream: int = S_WEI
         dt = np.dtype([("d", "<f2"), ("qs", "i1", (32,))])
         blk = np.empty(n, dtype=dt)
         blk["d"] = _scales_f16(g, n, scale_lo, scale_hi)
-        blk["qs"] = g.integers(-127, 128, size=(n, 32), dtype=np.int16).astype(np.int8)
+        blk["qs"] = g.integers(-127, 127, size=(n, 32), dtype=np.int8, endpoint=True)
     elif fmt == Q4_0:
         dt = np.dtype([("d", "<f2"), ("qs", "u1", (16,))])
         blk = np.empty(n, dtype=dt)
         blk["d"] = _scales_f16(g, n, scale_lo, scale_hi)
-        blk["qs"] = g.integers(0, 256, size=(n, 16), dtype=np.int16).astype(np.uint8)
+        blk["qs"] = g.integers(0, 255, size=(n, 16), dtype=np.uint8, endpoint=True)
     else:
         raise ValueError(f"unknown format {fmt}")
     assert dt.itemsize == BLOCK_BYTES[fmt]

@@ -1,0 +1,209 @@
+/*
+ * zdmmv.h -- C ABI of the GB300 (sm_103a) GGUF block-quantized decode DMMV
+ * library (libzdmmv.so).
+ *
+ * The operation. A decode DMMV ("dequantize matrix x vector") computes
+ * y = W.x for one decode token: it reads the quantized weights once,
+ * dequantizes them in registers, multiplies by the input vector and writes the
+ * result, with no intermediate dequantized buffer (habr article "Как мы
+ * запустили 35B LLM ... внутри ZINC inference engine", section "Что такое DMMV";
+ * decode is bound by memory bandwidth, section "Ядро: DMMV и борьба за
+ * пропускную способность памяти"). The arithmetic is a packed int8x4 integer
+ * dot product accumulated in int32 -- GL_EXT_integer_dot_product on Vulkan,
+ * __dp4a in CUDA ("Bringing ZINC to NVIDIA: a CUDA backend", section "The
+ * reassuring result: ZINC's matmuls are __dp4a, not tensor cores"; "CUDA
+ * backend for ZINC -- design & implementation plan", section "4. Kernel port
+ * strategy"). Per 32-element block b of row r:
+ *     s_b  = sum_{i<32} qw_i * qx_i                      (int32, exact)
+ *     y_r  = sum_b fp16(d_w[r,b]) * fp16(d_x[b]) * s_b    (fp32 accumulation)
+ * where qw_i is the Q8_0 int8 value, or the Q4_0 4-bit value minus 8 (the -8
+ * offset of the Q4 unpack in "Что такое DMMV"), and qx_i / d_x come from the
+ * activation quantized to Q8_0 blocks by zdmmv_quantize_act_q8_0.
+ *
+ * Block formats (GGML/GGUF layouts, bit-for-bit; "The reassuring result",
+ * "Bringing ZINC to NVIDIA"), little-endian:
+ *     Q8_0 (34 B): fp16 d, int8 q[32];                  value = d*q
+ *     Q4_0 (18 B): fp16 d, uint8 qs[16]; element j = qs[j] & 15,
+ *                  element j+16 = qs[j] >> 4 (j < 16);   value = d*(q-8)
+ * A [rows x cols] matrix in ZDMMV_LAYOUT_GGUF is rows*cols/32 blocks, row-major.
+ * ZDMMV_LAYOUT_REPACKED (produced by zdmmv_repack) keeps the same bytes as a
+ * quant stream (block (r,b) at (r*nb+b)*QB, QB = 32 or 16) followed by an fp16
+ * scale array (block (r,b) at rows*nb*QB + (r*nb+b)*2), nb = cols/32.
+ *
+ * Conventions for every entry point:
+ *  - Pointers named *_dev / w / xq / y are DEVICE pointers owned by the caller;
+ *    the library never allocates, frees or retains them.
+ *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
+ *    default stream). Argument errors are returned synchronously before any
+ *    launch; launch failures return ZDMMV_ERR_CUDA. No entry point
+ *    synchronizes the device except zdmmv_device_status.
+ *  - There is no CPU fallback: every result is computed by the CUDA kernels.
+ *  - Inputs must be finite (a NaN or infinite activation gives unspecified
+ *    codes).
+ */
+#ifndef ZDMMV_H
+#define ZDMMV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t (struct CUstream_st *); declared here so the
+ * header needs no CUDA include. */
+typedef struct CUstream_st *zdmmv_stream_t;
+
+typedef enum {
+    ZDMMV_OK = 0,
+    ZDMMV_ERR_NULL = 1,    /* a required pointer is NULL */
+    ZDMMV_ERR_SHAPE = 2,   /* cols <= 0, cols % 32 != 0, rows < 0, k % 32 != 0,
+                              batch outside 1..8, n < 0, bad strides */
+    ZDMMV_ERR_ALIGN = 3,   /* w, xq or a stride not 16-byte aligned; x, y not 4-byte aligned */
+    ZDMMV_ERR_LAYOUT = 4,  /* unknown layout */
+    ZDMMV_ERR_FORMAT = 5,  /* unknown block format */
+    ZDMMV_ERR_SIZE = 6,    /* destination or workspace too small */
+    ZDMMV_ERR_CUDA = 7,    /* a CUDA runtime call or a kernel launch failed */
+    ZDMMV_ERR_DEVICE = 8   /* a kernel reported a fault (see zdmmv_device_status) */
+} zdmmv_status;
+
+typedef enum { ZDMMV_Q4_0 = 2, ZDMMV_Q8_0 = 8 } zdmmv_fmt;     /* GGML type ids */
+typedef enum { ZDMMV_LAYOUT_GGUF = 0, ZDMMV_LAYOUT_REPACKED = 1 } zdmmv_layout;
+
+#define ZDMMV_QK 32         /* elements per block */
+#define ZDMMV_MAX_BATCH 8   /* activation vectors per batched call */
+
+/* Device fault bits reported by zdmmv_device_status. */
+#define ZDMMV_FAULT_WAIT_TIMEOUT 1u  /* a bounded wait on a copy or a pipeline stage gave up */
+
+/* Human-readable name of a status code (static string). */
+const char *zdmmv_status_str(zdmmv_status st);
+
+/* Library version string (static). */
+const char *zdmmv_version(void);
+
+/* Bytes of one block of `fmt` (34 or 18), 0 for an unknown format. */
+size_t zdmmv_block_bytes(zdmmv_fmt fmt);
+
+/* Quantize k fp32 activations to k/32 Q8_0 blocks (34 B each), per block:
+ *   amax = max|x_i|; d = amax/127 (fp32, IEEE division); id = d ? 1/d : 0;
+ *   q_i = round(x_i*id) (fp32 product, ties away from zero); store fp16(d)
+ *   (round to nearest even) then q[32].
+ * This is the activation quantizer that feeds the int8 dot (the "quantize"
+ * shaders in "Bringing ZINC to NVIDIA", section "Porting the kernels"; the
+ * rounding reading is the GGUF reference quantizer's, since the pages do not
+ * print it). A batch of vectors stored back to back is one call with k =
+ * batch*cols.
+ *   x   device, k floats, 4-byte aligned;   xq device, k/32*34 bytes.
+ *   k   multiple of 32; k == 0 is a no-op.
+ * Errors: ERR_NULL, ERR_SHAPE, ERR_ALIGN, ERR_CUDA. */
+zdmmv_status zdmmv_quantize_act_q8_0(const float *x, int64_t k, void *xq,
+                                     zdmmv_stream_t stream);
+
+/* y = W.x for one activation vector (Q8_0 or Q4_0 weights).
+ *   w      device, the matrix in `layout`, 16-byte aligned.
+ *   rows   >= 0 (0 is a no-op);  cols > 0, multiple of 32.
+ *   xq     device, cols/32 Q8_0 activation blocks, 16-byte aligned.
+ *   y      device, rows floats (fp32), 4-byte aligned.
+ * Matrices whose rows are 16-byte multiples (cols % 256 == 0) and cols <= 8192
+ * take the TMA-pipelined kernel; other shapes take a plain kernel with the
+ * same arithmetic. Errors: ERR_NULL, ERR_SHAPE, ERR_ALIGN, ERR_LAYOUT, ERR_CUDA. */
+zdmmv_status zdmmv_q8_0(const void *w, zdmmv_layout layout, int64_t rows, int64_t cols,
+                        const void *xq, float *y, zdmmv_stream_t stream);
+zdmmv_status zdmmv_q4_0(const void *w, zdmmv_layout layout, int64_t rows, int64_t cols,
+                        const void *xq, float *y, zdmmv_stream_t stream);
+
+/* The same weight matrix against `batch` (1..8) activation vectors in one call:
+ * xq is [batch][cols/32] Q8_0 blocks, y is [batch][rows] fp32. The weight
+ * stream is read from HBM once per call (concurrency headroom of decode slots:
+ * habr article, section "RDNA4: что мы узнали о железе"). batch == 1 is the
+ * same computation as zdmmv_q8_0 / zdmmv_q4_0, bit for bit.
+ * Errors: as zdmmv_q8_0, plus ERR_SHAPE for batch outside 1..8. */
+zdmmv_status zdmmv_q8_0_batched(const void *w, zdmmv_layout layout, int64_t rows,
+                                int64_t cols, const void *xq, int batch, float *y,
+                                zdmmv_stream_t stream);
+zdmmv_status zdmmv_q4_0_batched(const void *w, zdmmv_layout layout, int64_t rows,
+                                int64_t cols, const void *xq, int batch, float *y,
+                                zdmmv_stream_t stream);
+
+/* MoE expert gather: n matrices picked by index from a stack of n_experts
+ * equally shaped matrices, all in ONE launch (routed experts are selected per
+ * token by the router: "CUDA backend for ZINC", M1 list "dmmv_q4k_moe";
+ * batching the experts into one dispatch: habr article, sections "Gap
+ * analysis" and "Что дальше"; a GPU-side gather that drops the router
+ * round-trip: "RTX 5090: Batched Prefill & CUDA Graphs in ZINC", "What's next").
+ *   w_stack             device; expert e starts at w_stack + e*expert_stride_bytes
+ *                       (16-byte multiple), each a [rows x cols] matrix in `layout`.
+ *   idx                 DEVICE int32[n], read by the kernel (no host round-trip).
+ *   n                   number of selected experts (>= 0; 0 is a no-op).
+ *   n_experts           valid indices are 0 .. n_experts-1.
+ *   xq                  device Q8_0 blocks; slot k reads xq + k*xq_stride_bytes
+ *                       (xq_stride_bytes = 0: one activation shared by all slots;
+ *                       otherwise a 16-byte multiple >= cols/32*34).
+ *   y                   device fp32 [n][rows].
+ *   status_dev          nullable device int32; an index outside [0, n_experts)
+ *                       fills that slot's rows with NaN and stores 1 here. The
+ *                       kernel never reads out of range for a bad index.
+ * Slot k's result equals zdmmv_q{8,4}_0 on matrix idx[k], bit for bit.
+ * Errors: ERR_NULL, ERR_SHAPE, ERR_ALIGN, ERR_LAYOUT, ERR_FORMAT, ERR_CUDA. */
+zdmmv_status zdmmv_expert_gather(zdmmv_fmt fmt, const void *w_stack,
+                                 int64_t expert_stride_bytes, zdmmv_layout layout,
+                                 int64_t rows, int64_t cols, const int32_t *idx, int n,
+                                 int n_experts, const void *xq, int64_t xq_stride_bytes,
+                                 float *y, int32_t *status_dev, zdmmv_stream_t stream);
+
+/* Bytes of the repacked form of a [rows x cols] matrix (equal to the GGUF size);
+ * 0 for an unknown format or a bad shape. */
+size_t zdmmv_repacked_bytes(zdmmv_fmt fmt, int64_t rows, int64_t cols);
+
+/* One-time repack of a GGUF-layout matrix into ZDMMV_LAYOUT_REPACKED (a
+ * 16-byte aligned quant stream plus a separate fp16 scale array; the pages'
+ * shaders read 128-bit vec4/uvec4 words: "CUDA backend for ZINC", "4. Kernel
+ * port strategy"). Pure byte permutation, bit-exact.
+ *   src, dst   device, 16-byte aligned, must not overlap; dst_bytes >=
+ *              zdmmv_repacked_bytes(fmt, rows, cols).
+ * Errors: ERR_NULL, ERR_SHAPE, ERR_ALIGN, ERR_FORMAT, ERR_SIZE, ERR_CUDA. */
+zdmmv_status zdmmv_repack(zdmmv_fmt fmt, const void *src, int64_t rows, int64_t cols,
+                          void *dst, size_t dst_bytes, zdmmv_stream_t stream);
+
+/* One decode step with HOST activations and outputs: copies x_host
+ * ([batch][cols] fp32; pinned memory gives asynchronous copies) to the device,
+ * quantizes it, runs the DMMV on the resident weights and copies y back to
+ * y_host ([batch][rows] fp32), all ordered on `stream`. The caller synchronizes
+ * the stream before reading y_host.
+ *   workspace_dev  device, >= zdmmv_host_step_workspace_bytes(rows, cols, batch),
+ *                  16-byte aligned; holds x, its Q8_0 blocks and y.
+ * Errors: as zdmmv_q8_0_batched, plus ERR_SIZE. */
+size_t zdmmv_host_step_workspace_bytes(int64_t rows, int64_t cols, int batch);
+zdmmv_status zdmmv_host_step(zdmmv_fmt fmt, const void *w, zdmmv_layout layout,
+                             int64_t rows, int64_t cols, const float *x_host, int batch,
+                             float *y_host, void *workspace_dev, size_t workspace_bytes,
+                             zdmmv_stream_t stream);
+
+/* Debug / verification: the int32 per-block dot products s[r*nb+b] exactly as
+ * the DMMV kernel that zdmmv_q{8,4}_0 would run for this shape forms them (same
+ * device functions), for checking them bit for bit.
+ *   sums  device int32 [rows][cols/32].
+ * Errors: as zdmmv_q8_0, plus ERR_FORMAT. */
+zdmmv_status zdmmv_debug_block_sums(zdmmv_fmt fmt, const void *w, zdmmv_layout layout,
+                                    int64_t rows, int64_t cols, const void *xq,
+                                    int32_t *sums, zdmmv_stream_t stream);
+
+/* Self-test of the packed int8x4 dot on the device: out[i] = c[i] +
+ * sum_j a[i].byte_j * b[i].byte_j (signed bytes), the "dp4a ... = 70" smoke of
+ * "Bringing ZINC to NVIDIA", section "The reassuring result". All device
+ * pointers, n >= 0 elements. Errors: ERR_NULL, ERR_SHAPE, ERR_CUDA. */
+zdmmv_status zdmmv_selftest_dp4a(const int32_t *a, const int32_t *b, const int32_t *c,
+                                 int32_t *out, int n, zdmmv_stream_t stream);
+
+/* Read (and, if clear != 0, reset) the device fault bits of the current device
+ * (ZDMMV_FAULT_*). Synchronizes the device first. *bits_out = 0 means no kernel
+ * has reported a fault. Errors: ERR_NULL, ERR_CUDA. */
+zdmmv_status zdmmv_device_status(uint32_t *bits_out, int clear);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ZDMMV_H */

@@ -1,0 +1,84 @@
+"""CPU-side checks of the C-ABI library: it builds for sm_103a, loads, exports
+every function include/zdmmv.h declares, and rejects bad arguments on the host
+before any launch. No kernel runs here (no GPU on this machine)."""
+import ctypes
+
+import pytest
+
+from gguf_block_quant_gb300 import zdmmv
+
+
+@pytest.fixture(scope="module")
+def L():
+    return zdmmv.lib()
+
+
+def test_every_declared_function_is_exported(L):
+    names = zdmmv.header_functions()
+    assert len(names) >= 15
+    missing = [n for n in names if not hasattr(L, n)]
+    assert not missing, missing
+    assert set(names) == set(zdmmv._SIGS), "binding and header disagree"
+
+
+def test_status_strings_and_sizes(L):
+    assert L.zdmmv_status_str(0) == b"ok"
+    assert L.zdmmv_status_str(2) == b"bad shape"
+    assert b"sm_103a" in L.zdmmv_version()
+    assert L.zdmmv_block_bytes(zdmmv.Q8_0) == 34
+    assert L.zdmmv_block_bytes(zdmmv.Q4_0) == 18
+    assert L.zdmmv_block_bytes(3) == 0
+    assert L.zdmmv_repacked_bytes(zdmmv.Q4_0, 4096, 4096) == 4096 * 128 * 18
+    assert L.zdmmv_repacked_bytes(zdmmv.Q8_0, 3, 33) == 0
+    # x (batch*cols fp32) + Q8_0 blocks + y (batch*rows fp32), each rounded to 256 B
+    assert L.zdmmv_host_step_workspace_bytes(100, 64, 2) == 512 + 256 + 1024
+    assert L.zdmmv_host_step_workspace_bytes(100, 64, 9) == 0
+
+
+# Host-side argument checks return before any CUDA call, so they run without a GPU.
+FAKE = 1 << 20          # a 16-byte aligned non-null "device" address, never dereferenced
+ODD = FAKE + 2
+
+
+def test_dmmv_argument_checks(L):
+    for fn in (L.zdmmv_q8_0, L.zdmmv_q4_0):
+        assert fn(None, 0, 4, 64, FAKE, FAKE, None) == 1            # null weights
+        assert fn(FAKE, 0, 4, 48, FAKE, FAKE, None) == 2            # cols % 32
+        assert fn(FAKE, 0, 4, 0, FAKE, FAKE, None) == 2             # cols == 0
+        assert fn(FAKE, 0, -1, 64, FAKE, FAKE, None) == 2           # rows < 0
+        assert fn(FAKE, 7, 4, 64, FAKE, FAKE, None) == 4            # layout
+        assert fn(ODD, 0, 4, 64, FAKE, FAKE, None) == 3             # misaligned w
+        assert fn(FAKE, 0, 4, 64, ODD, FAKE, None) == 3             # misaligned xq
+        assert fn(FAKE, 0, 4, 64, FAKE, FAKE + 1, None) == 3        # misaligned y
+    assert L.zdmmv_q8_0_batched(FAKE, 0, 4, 64, FAKE, 0, FAKE, None) == 2
+    assert L.zdmmv_q8_0_batched(FAKE, 0, 4, 64, FAKE, 9, FAKE, None) == 2
+    assert L.zdmmv_q4_0_batched(FAKE, 0, 4, 64, FAKE, 9, FAKE, None) == 2
+
+
+def test_empty_inputs_are_no_ops(L):
+    # rows == 0 / k == 0 / n == 0 return OK without touching the device
+    assert L.zdmmv_q8_0(None, 0, 0, 64, None, None, None) == 0
+    assert L.zdmmv_quantize_act_q8_0(None, 0, None, None) == 0
+    assert L.zdmmv_expert_gather(2, FAKE, 1 << 16, 0, 4, 64, FAKE, 0, 8, FAKE, 0, FAKE, None, None) == 0
+    assert L.zdmmv_repack(8, None, 0, 64, None, 0, None) == 0
+    assert L.zdmmv_selftest_dp4a(None, None, None, None, 0, None) == 0
+
+
+def test_other_argument_checks(L):
+    assert L.zdmmv_quantize_act_q8_0(FAKE, 33, FAKE, None) == 2
+    assert L.zdmmv_quantize_act_q8_0(None, 64, FAKE, None) == 1
+    assert L.zdmmv_quantize_act_q8_0(FAKE + 2, 64, FAKE, None) == 3
+    g = L.zdmmv_expert_gather
+    assert g(3, FAKE, 1 << 16, 0, 4, 64, FAKE, 2, 8, FAKE, 0, FAKE, None, None) == 5      # format
+    assert g(2, FAKE, 1 << 16, 0, 4, 64, None, 2, 8, FAKE, 0, FAKE, None, None) == 1      # idx null
+    assert g(2, FAKE, 8, 0, 4, 64, FAKE, 2, 8, FAKE, 0, FAKE, None, None) == 2            # stride < matrix
+    assert g(2, FAKE, 1 << 16, 0, 4, 64, FAKE, 2, 8, FAKE, 40, FAKE, None, None) == 2     # xq stride < vector
+    assert g(2, FAKE, (1 << 16) + 8, 0, 4, 64, FAKE, 2, 8, FAKE, 0, FAKE, None, None) == 3  # stride % 16
+    assert g(2, FAKE, 1 << 16, 0, 4, 64, FAKE, -1, 8, FAKE, 0, FAKE, None, None) == 2     # n < 0
+    assert L.zdmmv_repack(8, FAKE, 4, 64, FAKE + 4096, 10, None) == 6                     # dst too small
+    assert L.zdmmv_repack(8, FAKE, 4, 64, FAKE + 16, 4096, None) == 2                     # overlap
+    assert L.zdmmv_repack(3, FAKE, 4, 64, FAKE + 4096, 4096, None) == 5
+    assert L.zdmmv_host_step(8, FAKE, 0, 4, 64, FAKE, 1, FAKE, FAKE, 10, None) == 6
+    assert L.zdmmv_host_step(8, FAKE, 0, 4, 64, FAKE, 0, FAKE, FAKE, 1 << 20, None) == 2
+    assert L.zdmmv_device_status(None, 0) == 1
+    assert L.zdmmv_debug_block_sums(8, FAKE, 0, 4, 40, FAKE, FAKE, None) == 2

@@ -1,0 +1,304 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle.
+
+Bar (fixed by the method's statement): per-block int32 dot products are bit for
+bit the oracle's; every fp32 output row satisfies
+    |y - y_ref| <= 1e-5 * sum_b |d_w d_x s_b| + 1e-6
+where y_ref and the error scale come from the oracle (fp64); the quantizer's
+bytes are bit for bit the oracle's. Every output buffer is pre-filled with a NaN
+sentinel so rows the kernel never wrote show up.
+
+Inputs come from gguf_block_quant_gb300.synth (seeded draws, no arithmetic of
+the method); expected values only from oracle/.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gguf_block_quant_gb300 import synth
+from gguf_block_quant_gb300 import zdmmv as Z
+
+pytestmark = pytest.mark.gpu
+
+Q4_0, Q8_0 = Z.Q4_0, Z.Q8_0
+REL, ABS = 1e-5, 1e-6
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    Z.lib()
+    Z.device_status(clear=True)
+    yield
+    assert Z.device_status() == 0, "a kernel reported a device fault"
+
+
+def dev(a: np.ndarray) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def nan_out(*shape) -> torch.Tensor:
+    return torch.full(shape, float("nan"), dtype=torch.float32, device="cuda")
+
+
+def check_y(y: torch.Tensor, y_ref, e_ref):
+    yh = y.double().cpu().numpy().reshape(np.shape(y_ref))
+    assert not np.isnan(yh).any(), "some rows were never written (NaN sentinel)"
+    ok, worst = oracle.within_tolerance(yh, y_ref, e_ref, REL, ABS)
+    assert ok, f"tolerance exceeded: worst |dy|/bound = {worst:.3g}"
+    return worst
+
+
+def run_dmmv(fmt, w_np, rows, cols, xq_np, layout=Z.GGUF, w_dev=None):
+    w = w_dev if w_dev is not None else dev(w_np)
+    if layout == Z.REPACKED and w_dev is None:
+        w = Z.repack(fmt, w, rows, cols)
+    y = nan_out(rows)
+    Z.dmmv(fmt, w, rows, cols, dev(xq_np), y=y, layout=layout)
+    torch.cuda.synchronize()
+    return y
+
+
+# ----------------------------------------------------------------- dp4a smoke
+def test_dp4a_selftest_pages_value_and_random():
+    pack = oracle.pack_int8x4
+    a = [pack([1, 2, 3, 4])]
+    b = [pack([5, 6, 7, 8])]
+    c = [0]
+    g = np.random.default_rng(3)
+    for _ in range(500):
+        a.append(int(g.integers(0, 1 << 32)))
+        b.append(int(g.integers(0, 1 << 32)))
+        c.append(int(g.integers(-(1 << 20), 1 << 20)))
+    to_i32 = lambda v: np.array(v, dtype=np.uint32).view(np.int32)
+    out = Z.selftest_dp4a(dev(to_i32(a)), dev(to_i32(b)), dev(np.array(c, dtype=np.int32)))
+    out = out.cpu().numpy()
+    assert out[0] == 70
+    ref = [oracle.dp4a(int(x), int(y), int(z)) for x, y, z in zip(a, b, c)]
+    assert list(out) == ref
+
+
+# ----------------------------------------------------------------- quantizer
+@pytest.mark.parametrize("k", [32, 2048, 4096, 32 * 1001, 4096 * 8])
+def test_quantize_bit_exact(k):
+    x = synth.activations(k, seed=k)
+    xq = Z.quantize_act_q8_0(dev(x))
+    torch.cuda.synchronize()
+    assert np.array_equal(xq.cpu().numpy(), oracle.quantize_q8_0(x))
+
+
+def test_quantize_bit_exact_special_blocks():
+    blocks = []
+    for case in [[127.0, 2.5, -2.5, 0.5, -0.5, 1.5, 63.5, -127.0], [-254.0, 3.0, -3.0, 1.0, 100.0],
+                 [], [1.0, -1.0], [1e-30, -3e-31], [60000.0, -1.0], [5e-8, 1e-8]]:
+        b = np.zeros(32, dtype=np.float32)
+        b[:len(case)] = case
+        blocks.append(b)
+    g = np.random.default_rng(9)
+    for s in (1e-6, 1e-2, 1.0, 1e3):
+        blocks.append((g.standard_normal(32) * s).astype(np.float32))
+    x = np.concatenate(blocks)
+    xq = Z.quantize_act_q8_0(dev(x))
+    torch.cuda.synchronize()
+    assert np.array_equal(xq.cpu().numpy(), oracle.quantize_q8_0(x))
+
+
+# -------------------------------------------------- dense DMMV vs the oracle
+SHAPES = [
+    # (fmt, rows, cols): pipelined-kernel shapes (cols % 256 == 0) with ragged
+    # row counts spanning several tiles, and plain-kernel shapes
+    (Q8_0, 64, 2048), (Q8_0, 1000, 512), (Q8_0, 777, 1024), (Q8_0, 1531, 4096), (Q8_0, 301, 8192),
+    (Q4_0, 4096, 4096), (Q4_0, 2999, 2048), (Q4_0, 513, 512), (Q4_0, 257, 8192),
+    (Q8_0, 1, 32), (Q8_0, 37, 96), (Q4_0, 53, 160), (Q4_0, 5, 224), (Q8_0, 19, 14336), (Q4_0, 33, 16384),
+]
+
+
+@pytest.mark.parametrize("layout", [Z.GGUF, Z.REPACKED])
+@pytest.mark.parametrize("fmt,rows,cols", SHAPES)
+def test_dmmv_matches_oracle(fmt, rows, cols, layout):
+    w = synth.weight_blocks(fmt, rows, cols, seed=rows + cols)
+    x = synth.activations(cols, seed=rows)
+    xq_ref = oracle.quantize_q8_0(x)
+    xq = Z.quantize_act_q8_0(dev(x))
+    y = nan_out(rows)
+    wd = dev(w)
+    if layout == Z.REPACKED:
+        wd = Z.repack(fmt, wd, rows, cols)
+    Z.dmmv(fmt, wd, rows, cols, xq, y=y, layout=layout)
+    torch.cuda.synchronize()
+    assert np.array_equal(xq.cpu().numpy(), xq_ref)
+    y_ref, e_ref = oracle.dmmv(fmt, w, rows, cols, xq_ref)
+    check_y(y, y_ref, e_ref)
+
+
+@pytest.mark.parametrize("layout", [Z.GGUF, Z.REPACKED])
+@pytest.mark.parametrize("fmt,rows,cols", [(Q8_0, 300, 2048), (Q4_0, 300, 4096), (Q8_0, 70, 512),
+                                           (Q4_0, 41, 96), (Q8_0, 9, 14336)])
+def test_block_sums_bit_exact(fmt, rows, cols, layout):
+    w = synth.weight_blocks(fmt, rows, cols, seed=5 * rows)
+    xq = synth.activation_blocks(cols // 32, seed=6 * rows)
+    wd = dev(w)
+    if layout == Z.REPACKED:
+        wd = Z.repack(fmt, wd, rows, cols)
+    s = Z.debug_block_sums(fmt, wd, rows, cols, dev(xq), layout=layout)
+    torch.cuda.synchronize()
+    assert np.array_equal(s.cpu().numpy(), oracle.block_sums(fmt, w, rows, cols, xq))
+
+
+@pytest.mark.parametrize("fmt,rows,cols", [(Q8_0, 500, 4096), (Q4_0, 700, 2048), (Q8_0, 90, 512),
+                                           (Q4_0, 3, 8192), (Q8_0, 10, 96)])
+def test_exact_integer_outputs_equal_oracle_bitwise(fmt, rows, cols):
+    """Unit scales and small codes keep every fp32 partial sum an exact integer,
+    so the kernel's y must equal the oracle's exactly: this pins the hot kernel's
+    integer block sums end to end."""
+    w = synth.weight_blocks_small(fmt, rows, cols, seed=rows, qmax=7)
+    xq = synth.activation_blocks(cols // 32, seed=cols, qmax=15, fixed_scale=1.0)
+    for layout in (Z.GGUF, Z.REPACKED):
+        y = run_dmmv(fmt, w, rows, cols, xq, layout=layout)
+        y_ref, _ = oracle.dmmv(fmt, w, rows, cols, xq)
+        assert np.array_equal(y.double().cpu().numpy(), y_ref)
+
+
+@pytest.mark.parametrize("fmt,cols", [(Q8_0, 2048), (Q4_0, 4096), (Q8_0, 160)])
+def test_row_permutation_equivariance_bitwise(fmt, cols):
+    rows = 611
+    w = synth.weight_blocks(fmt, rows, cols, seed=77)
+    xq = synth.activation_blocks(cols // 32, seed=78)
+    perm = np.random.default_rng(1).permutation(rows)
+    wp = w.reshape(rows, -1)[perm].reshape(-1)
+    y = run_dmmv(fmt, w, rows, cols, xq).cpu().numpy()
+    yp = run_dmmv(fmt, wp, rows, cols, xq).cpu().numpy()
+    assert np.array_equal(yp, y[perm])
+
+
+@pytest.mark.parametrize("fmt", [Q8_0, Q4_0])
+def test_power_of_two_input_scaling_exact(fmt):
+    rows, cols, k = 999, 2048, 3
+    w = synth.weight_blocks(fmt, rows, cols, seed=88)
+    x = synth.activations(cols, seed=89)
+    xs = (x * np.float32(2.0 ** k)).astype(np.float32)
+    wd = dev(w)
+    y1 = nan_out(rows)
+    y2 = nan_out(rows)
+    Z.dmmv(fmt, wd, rows, cols, Z.quantize_act_q8_0(dev(x)), y=y1)
+    Z.dmmv(fmt, wd, rows, cols, Z.quantize_act_q8_0(dev(xs)), y=y2)
+    torch.cuda.synchronize()
+    assert torch.equal(y2, y1 * 2.0 ** k)
+
+
+def test_layouts_agree_bitwise():
+    for fmt, rows, cols in [(Q8_0, 333, 4096), (Q4_0, 333, 2048), (Q4_0, 40, 96)]:
+        w = synth.weight_blocks(fmt, rows, cols, seed=3)
+        xq = synth.activation_blocks(cols // 32, seed=4)
+        a = run_dmmv(fmt, w, rows, cols, xq, layout=Z.GGUF)
+        b = run_dmmv(fmt, w, rows, cols, xq, layout=Z.REPACKED)
+        assert torch.equal(a, b)
+
+
+def test_zero_rows_is_a_no_op():
+    y = nan_out(4)
+    Z.q8_0(torch.empty(16, dtype=torch.uint8, device="cuda"), 0, 64,
+           torch.empty(80, dtype=torch.uint8, device="cuda"), y=y)
+    torch.cuda.synchronize()
+    assert torch.isnan(y).all()
+
+
+# ----------------------------------------------------------------- repack
+@pytest.mark.parametrize("fmt,rows,cols", [(Q8_0, 123, 4096), (Q4_0, 1000, 2048), (Q4_0, 7, 96)])
+def test_repack_bit_exact(fmt, rows, cols):
+    w = synth.weight_blocks(fmt, rows, cols, seed=rows)
+    r = Z.repack(fmt, dev(w), rows, cols)
+    torch.cuda.synchronize()
+    assert np.array_equal(r.cpu().numpy(), oracle.repack(fmt, w, rows, cols))
+
+
+# ----------------------------------------------------------------- batched
+@pytest.mark.parametrize("layout", [Z.GGUF, Z.REPACKED])
+@pytest.mark.parametrize("fmt,rows,cols", [(Q8_0, 1434, 4096), (Q4_0, 901, 2048), (Q8_0, 99, 160)])
+@pytest.mark.parametrize("batch", [1, 2, 4, 8])
+def test_batched_matches_oracle_and_single_calls(fmt, rows, cols, batch, layout):
+    w = synth.weight_blocks(fmt, rows, cols, seed=batch)
+    x = synth.activations(cols, seed=10 + batch, batch=batch)
+    xq = Z.quantize_act_q8_0(dev(x))
+    wd = dev(w)
+    if layout == Z.REPACKED:
+        wd = Z.repack(fmt, wd, rows, cols)
+    y = nan_out(batch, rows)
+    Z.dmmv_batched(fmt, wd, rows, cols, xq, batch, y=y, layout=layout)
+    torch.cuda.synchronize()
+    xq_ref = oracle.quantize_q8_0(x)
+    y_ref, e_ref = oracle.dmmv_batched(fmt, w, rows, cols, xq_ref, batch)
+    check_y(y, y_ref, e_ref)
+    nbx = cols // 32 * 34
+    for v in range(batch):
+        ys = nan_out(rows)
+        Z.dmmv(fmt, wd, rows, cols, xq[v * nbx:(v + 1) * nbx], y=ys, layout=layout)
+        torch.cuda.synchronize()
+        assert torch.equal(ys, y[v]), "batched result differs from the single-vector call"
+
+
+# ------------------------------------------------------------ expert gather
+def _moe_stack(fmt, rows, cols, n_slots, seed):
+    return synth.weight_blocks(fmt, n_slots * rows, cols, seed=seed)
+
+
+@pytest.mark.parametrize("layout", [Z.GGUF, Z.REPACKED])
+def test_expert_gather_small_stack(layout):
+    rows, cols, n_exp = 96, 512, 12
+    per = rows * cols // 32 * 18
+    stack = _moe_stack(Q4_0, rows, cols, n_exp, seed=5)
+    idx = np.array([11, 0, 7, 7, 3], dtype=np.int32)
+    x = synth.activations(cols, seed=6, batch=len(idx))
+    xq_ref = oracle.quantize_q8_0(x)
+    sd = dev(stack)
+    if layout == Z.REPACKED:
+        sd = torch.cat([Z.repack(Q4_0, sd[e * per:(e + 1) * per], rows, cols) for e in range(n_exp)])
+    y = nan_out(len(idx), rows)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    Z.expert_gather(Q4_0, sd, per, rows, cols, dev(idx), n_exp, dev(xq_ref), cols // 32 * 34, y=y,
+                    status=st, layout=layout)
+    torch.cuda.synchronize()
+    y_ref, e_ref, st_ref = oracle.expert_gather(Q4_0, stack, per, rows, cols, idx, n_exp, xq_ref,
+                                                cols // 32 * 34)
+    assert st.item() == 0 == st_ref
+    check_y(y, y_ref, e_ref)
+    for k, e in enumerate(idx):
+        ys = run_dmmv(Q4_0, None, rows, cols, xq_ref.reshape(len(idx), -1)[k], layout=layout,
+                      w_dev=sd[e * per:(e + 1) * per])
+        assert torch.equal(ys, y[k])
+
+
+@pytest.mark.parametrize("cols", [512, 96])
+def test_expert_gather_bad_index_gives_nan_and_status(cols):
+    rows, n_exp = 40, 4
+    per = rows * cols // 32 * 34
+    stack = _moe_stack(Q8_0, rows, cols, n_exp, seed=8)
+    xq = synth.activation_blocks(cols // 32, seed=9)
+    idx = np.array([2, 4, -1, 0], dtype=np.int32)
+    y = torch.zeros(len(idx), rows, dtype=torch.float32, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    Z.expert_gather(Q8_0, dev(stack), per, rows, cols, dev(idx), n_exp, dev(xq), 0, y=y, status=st)
+    torch.cuda.synchronize()
+    y_ref, e_ref, st_ref = oracle.expert_gather(Q8_0, stack, per, rows, cols, idx, n_exp, xq, 0)
+    assert st.item() == 1 == st_ref
+    yh = y.cpu().numpy()
+    assert np.isnan(yh[1]).all() and np.isnan(yh[2]).all()
+    good = [0, 3]
+    ok, _ = oracle.within_tolerance(yh[good], y_ref[good], e_ref[good])
+    assert ok
+
+
+# ------------------------------------------------------- end-to-end host step
+@pytest.mark.parametrize("fmt,rows,cols,batch", [(Q4_0, 4096, 4096, 1), (Q8_0, 1000, 4096, 4),
+                                                 (Q8_0, 33, 96, 2)])
+def test_host_step_matches_oracle(fmt, rows, cols, batch):
+    w = synth.weight_blocks(fmt, rows, cols, seed=21)
+    x = synth.activations(cols, seed=22, batch=batch)
+    xh = torch.from_numpy(np.ascontiguousarray(x)).pin_memory()
+    yh = torch.full((batch, rows), float("nan"), dtype=torch.float32).pin_memory()
+    ws = torch.empty(Z.host_step_workspace_bytes(rows, cols, batch), dtype=torch.uint8, device="cuda")
+    Z.host_step(fmt, dev(w), rows, cols, xh, yh, ws, batch=batch)
+    torch.cuda.synchronize()
+    xq_ref = oracle.quantize_q8_0(x)
+    y_ref, e_ref = oracle.dmmv_batched(fmt, w, rows, cols, xq_ref, batch)
+    check_y(yh, y_ref, e_ref)
