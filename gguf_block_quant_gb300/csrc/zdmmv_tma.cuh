@@ -178,8 +178,9 @@ __global__ void __launch_bounds__(kTmaThreads, MINB) dmmv_tma_kernel(const DmmvA
     const int lane = tid & 31;
     const int g = tid / LPR;  // row group
     const int l = tid % LPR;  // lane inside the row group
-    if (!mbar_wait(xbar, 0)) {
-        atomicOr(a.fault, 1u);
+    // waits are made warp-uniform so a timeout can never split a warp before its shuffles
+    if (!__all_sync(0xffffffffu, mbar_wait(xbar, 0))) {
+        if (lane == 0) atomicOr(a.fault, 1u);
         return;
     }
     P xr[PPL];
@@ -195,8 +196,8 @@ __global__ void __launch_bounds__(kTmaThreads, MINB) dmmv_tma_kernel(const DmmvA
 
     for (int t = 0; t < ntiles; ++t) {
         const int s = t % STAGES;
-        if (!mbar_wait(&full[s], static_cast<uint32_t>(t / STAGES) & 1u)) {
-            atomicOr(a.fault, 1u);
+        if (!__all_sync(0xffffffffu, mbar_wait(&full[s], static_cast<uint32_t>(t / STAGES) & 1u))) {
+            if (lane == 0) atomicOr(a.fault, 1u);
             return;
         }
         const uint8_t *st = stage0 + static_cast<size_t>(s) * a.stage_bytes;
