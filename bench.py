@@ -51,6 +51,8 @@ def parse():
     p.add_argument("--no-extra", action="store_true", help="skip the other four workloads")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--eager", action="store_true", help="launch eagerly instead of graph replay")
+    p.add_argument("--profile", default=None, metavar="WORKLOAD",
+                   help="no timing: a few launches of one workload (for ncu captures)")
     return p.parse_args()
 
 
@@ -244,10 +246,17 @@ class DensePool:
         self.xq = [torch.empty(nq, dtype=torch.uint8, device="cuda") for _ in range(layers)]
         self.y = [torch.empty(cfg.batch * cfg.rows, dtype=torch.float32, device="cuda") for _ in range(layers)]
         self.Z = Z
-        self.step()   # activations quantized once so the DMMV-only pass reads valid blocks
+        self.step_unfused()   # activations quantized once so the DMMV-only pass reads valid blocks
         torch.cuda.synchronize()
 
     def step(self):
+        """One decode token: per layer the fused quantize + DMMV (one launch)."""
+        Z, c = self.Z, self.cfg
+        for l in range(self.layers):
+            Z.dmmv_f32(c.fmt, self.w[l], c.rows, c.cols, self.x[l], batch=c.batch, y=self.y[l])
+
+    def step_unfused(self):
+        """The same token with the two-kernel chain: quantize, then DMMV."""
         Z, c = self.Z, self.cfg
         for l in range(self.layers):
             Z.quantize_act_q8_0(self.x[l], self.xq[l])
@@ -275,16 +284,20 @@ def measure_dense(cfg, layers, steps, warmup, world, device, eager):
     pool = DensePool(cfg, layers)
     run = graph_or_eager(pool.dmmv_only, eager)
     pool_step = graph_or_eager(pool.step, eager)
+    pool_step2 = graph_or_eager(pool.step_unfused, eager)
     ms_dmmv, _ = time_fn(run, steps, warmup, world, device)
     ms_step, _ = time_fn(pool_step, steps, warmup, world, device)
+    ms_step2, _ = time_fn(pool_step2, steps, warmup, world, device)
     per_launch_s = ms_dmmv / 1e3 / (steps * layers)
     per_step_s = ms_step / 1e3 / steps
     nbytes = cfg.algorithmic_bytes()
     del pool
     torch.cuda.empty_cache()
     return {"layers": layers, "dmmv_us": per_launch_s * 1e6, "dmmv_gbs": nbytes / per_launch_s / 1e9,
-            "step_gbs": layers * nbytes / per_step_s / 1e9, "rows_per_s": cfg.batch * cfg.rows / per_launch_s,
-            "algorithmic_bytes": nbytes}
+            "fused_step_gbs": layers * nbytes / per_step_s / 1e9,
+            "fused_us_per_layer": per_step_s / layers * 1e6,
+            "two_kernel_step_gbs": layers * nbytes / (ms_step2 / 1e3 / steps) / 1e9,
+            "rows_per_s": cfg.batch * cfg.rows / per_launch_s, "algorithmic_bytes": nbytes}
 
 
 def measure_moe(steps, warmup, world, device, eager, l2_bytes):
@@ -390,14 +403,19 @@ def gpu_arm(args):
     nbytes = cfg.algorithmic_bytes()
     achieved = nbytes / per_launch / 1e9
 
-    # the headline: whole steps (quantize + DMMV per layer), clocks sampled meanwhile
+    # the two-kernel chain (quantize kernel, then DMMV kernel, per layer)
+    run_unfused = graph_or_eager(pool.step_unfused, args.eager)
+    ms_unfused, _ = time_fn(run_unfused, args.steps, args.warmup, world, device)
+
+    # the headline: whole steps (fused quantize + DMMV per layer), clocks sampled meanwhile
     run_step = graph_or_eager(pool.step, args.eager)
     sampler = ClockSampler(local)
     ms, clocks = time_fn(run_step, args.steps, args.warmup, world, device, sampler)
     ms_per_step = ms / args.steps
     value = world * layers * nbytes / (ms_per_step / 1e3) / 1e9
     rows_per_s = world * layers * cfg.rows / (ms_per_step / 1e3)
-    del pool, run_dmmv, run_step
+    unfused_gbs = world * layers * nbytes / (ms_unfused / args.steps / 1e3) / 1e9
+    del pool, run_dmmv, run_step, run_unfused
     torch.cuda.empty_cache()
 
     e2e = e2e_dense(cfg, min(layers, 64), max(3, args.steps // 10), args.warmup, world, device)
@@ -422,7 +440,8 @@ def gpu_arm(args):
             "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "int8", "data": "synthetic",
             "config": {"workload": cfg.name, "rows": cfg.rows, "cols": cfg.cols, "format": "Q4_0", "batch": 1,
-                       "layers_per_step": layers, "step": "quantize_act_q8_0 + DMMV per layer",
+                       "layers_per_step": layers,
+                       "step": "per layer: fp32 activation -> Q8_0 quantization + DMMV (fused, one launch)",
                        "l2": f"inputs larger than L2: {layers} distinct weight matrices "
                              f"({layers * cfg.weight_bytes / 1e6:.0f} MB) per step, L2 {l2 / 1e6:.0f} MB",
                        "launch": "eager" if args.eager else "cuda_graph replay", "parallelism": f"replicas x{world}"},
@@ -435,7 +454,8 @@ def gpu_arm(args):
                          "peak_kind": f"{peak_kind} HBM copy bandwidth"},
             "cpu_baseline": cpu,
             "e2e": e2e,
-            "gpu_launches": 2 * layers * args.steps,
+            "two_kernel_chain_gbs": round(unfused_gbs, 2),
+            "gpu_launches": layers * args.steps,
             "clocks": clocks,
             "workloads": workloads,
         }
@@ -485,9 +505,30 @@ def reference_arm(args):
     }), flush=True)
 
 
+def profile_mode(name: str):
+    """A handful of untimed launches on a small pool (4 layers): the two-kernel
+    chain once to fill the activation blocks, then 3 x (fused step, two-kernel
+    step). Meant to run under ncu with a kernel filter and a launch count."""
+    import torch
+    from gguf_block_quant_gb300 import synth
+    from gguf_block_quant_gb300 import zdmmv as Z
+    Z.lib()
+    workloads = {c.name: c for c in (synth.SSM_ALPHA_BETA, synth.DENSE_Q4_0, synth.LM_HEAD_Q4_0,
+                                     *synth.BATCHED_Q8_0.values())}
+    cfg = workloads[name]
+    pool = DensePool(cfg, 4)
+    for _ in range(3):
+        pool.step()
+        pool.step_unfused()
+    torch.cuda.synchronize()
+    print(json.dumps({"profile": name, "layers": 4, "fault": Z.device_status()}))
+
+
 def main():
     args = parse()
-    if args.impl == "reference":
+    if args.profile:
+        profile_mode(args.profile)
+    elif args.impl == "reference":
         reference_arm(args)
     else:
         gpu_arm(args)

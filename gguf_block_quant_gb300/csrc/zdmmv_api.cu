@@ -120,19 +120,11 @@ __global__ void __launch_bounds__(256) quantize_q8_0_kernel(const float *__restr
     const int64_t blk = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
     if (blk >= nblocks) return;
     const float v = x[blk * kQK + lane];
-    // max of |x| over the block; for non-negative floats the bit patterns order like the values
-    const uint32_t amax_bits = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(v)));
-    const float amax = __uint_as_float(amax_bits);
-    const float d = amax / 127.0f;                 // IEEE division (no fast-math in this build)
-    const float id = d != 0.0f ? 1.0f / d : 0.0f;  // IEEE reciprocal
-    const float q = roundf(__fmul_rn(v, id));      // round half away from zero
+    unsigned short d_bits;
+    const int q = quantize_q8_0_lane(v, d_bits);
     uint8_t *out = xq + blk * 34;
-    out[2 + lane] = static_cast<uint8_t>(static_cast<int8_t>(static_cast<int>(q)));
-    if (lane == 0) {
-        const unsigned short hb = __half_as_ushort(__float2half_rn(d));
-        out[0] = static_cast<uint8_t>(hb & 0xffu);
-        out[1] = static_cast<uint8_t>(hb >> 8);
-    }
+    out[2 + lane] = static_cast<uint8_t>(static_cast<int8_t>(q));
+    if (lane == 0) *reinterpret_cast<unsigned short *>(out) = d_bits;  // one 2-byte store (blocks are 2-byte aligned)
 }
 
 // One thread per block: GGUF block -> quant stream slot + scale slot.
@@ -208,6 +200,56 @@ __global__ void __launch_bounds__(256) dmmv_plain_kernel(const DmmvArgs a) {
     }
 }
 
+// Plain DMMV with the fp32 activation quantized by each CTA into shared memory
+// first (same quantizer device function as everywhere else), then one warp per
+// row over a grid-stride row loop. Used by the fused entry point for shapes the
+// pipelined kernel does not take.
+template <int FMT, int LAYOUT>
+__global__ void __launch_bounds__(256) dmmv_plain_fx_kernel(const DmmvArgs a) {
+    extern __shared__ __align__(16) uint8_t xsm[];  // batch * nb Q8_0 blocks
+    pdl_wait_api();
+    pdl_trigger_api();
+    constexpr int kBB = Fmt<FMT>::kBlockBytes;
+    constexpr int kQB = Fmt<FMT>::kQuantBytes;
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int nwarps = blockDim.x >> 5;
+    const int nb = a.nb;
+    const int total = a.batch * nb;
+    for (int b = warp; b < total; b += nwarps) {
+        const int v = b / nb;
+        const int blk = b - v * nb;
+        const float xv = a.xf[static_cast<int64_t>(v) * a.xf_stride + static_cast<int64_t>(blk) * kQK + lane];
+        unsigned short d_bits;
+        const int q = quantize_q8_0_lane(xv, d_bits);
+        xsm[34 * b + 2 + lane] = static_cast<uint8_t>(static_cast<int8_t>(q));
+        if (lane == 0) *reinterpret_cast<unsigned short *>(xsm + 34 * b) = d_bits;
+    }
+    __syncthreads();
+    for (int64_t row = static_cast<int64_t>(blockIdx.x) * nwarps + warp; row < a.rows;
+         row += static_cast<int64_t>(gridDim.x) * nwarps) {
+        for (int v = 0; v < a.batch; ++v) {
+            const uint8_t *xq = xsm + static_cast<int64_t>(v) * nb * 34;
+            float acc = 0.0f;
+            for (int b = lane; b < nb; b += 32) {
+                uint32_t q[8], xw[8];
+                float dw, dx;
+                const int64_t blk = row * nb + b;
+                if constexpr (LAYOUT == kLayoutGguf)
+                    Block<FMT>::load_gguf(a.w + blk * kBB, q, dw);
+                else
+                    Block<FMT>::load_repacked(a.w + blk * kQB, a.w + a.rows * nb * kQB + blk * 2, q, dw);
+                load_x_block(xq + static_cast<int64_t>(b) * 34, xw, dx);
+                const int s = Block<FMT>::dot(q, xw);
+                acc = __fmaf_rn(static_cast<float>(s), __fmul_rn(dw, dx), acc);
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+            if (lane == 0) a.y[static_cast<int64_t>(v) * a.rows + row] = acc;
+        }
+    }
+}
+
 // Debug: the int32 block sums with the device functions of the kernel that the
 // DMMV entry points pick for this shape. PAIRS: one thread per (row, pair) via
 // Pair<>::sums (pipelined kernel); else one thread per (row, block) via Block<>.
@@ -278,8 +320,37 @@ cudaError_t launch_plain(int fmt, int layout, const DmmvArgs &a, int slots, cuda
                                  : cudaLaunchKernelEx(&cfg, dmmv_plain_kernel<kFmtQ4, kLayoutRepacked>, a);
 }
 
+constexpr int kPlainFxMaxSmem = 200 * 1024;
+
+cudaError_t launch_plain_fx(int fmt, int layout, const DmmvArgs &a, int sms, cudaStream_t st) {
+    const size_t smem = static_cast<size_t>(a.batch) * a.nb * 34;
+    int64_t ctas = (a.rows + 7) / 8;
+    if (ctas > static_cast<int64_t>(sms) * 4) ctas = static_cast<int64_t>(sms) * 4;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(ctas), 1, 1);
+    cfg.blockDim = dim3(256, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl_enabled() ? 1 : 0;
+    auto go = [&](auto kern) -> cudaError_t {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kPlainFxMaxSmem);
+        if (e != cudaSuccess) return e;
+        return cudaLaunchKernelEx(&cfg, kern, a);
+    };
+    if (fmt == kFmtQ8)
+        return layout == kLayoutGguf ? go(dmmv_plain_fx_kernel<kFmtQ8, kLayoutGguf>)
+                                     : go(dmmv_plain_fx_kernel<kFmtQ8, kLayoutRepacked>);
+    return layout == kLayoutGguf ? go(dmmv_plain_fx_kernel<kFmtQ4, kLayoutGguf>)
+                                 : go(dmmv_plain_fx_kernel<kFmtQ4, kLayoutRepacked>);
+}
+
 // Run the DMMV over `slots` slots (expert gather / batch through slots).
-zdmmv_status run_dmmv(int fmt, int layout, DmmvArgs a, int slots, cudaStream_t st) {
+// fused_x: the activation is fp32 (a.xf) and the kernel quantizes it itself.
+zdmmv_status run_dmmv(int fmt, int layout, DmmvArgs a, int slots, cudaStream_t st, bool fused_x = false) {
     const DeviceInfo *dev = nullptr;
     cudaError_t e = device_info(&dev);
     if (e != cudaSuccess) return ZDMMV_ERR_CUDA;
@@ -297,10 +368,12 @@ zdmmv_status run_dmmv(int fmt, int layout, DmmvArgs a, int slots, cudaStream_t s
         if (ctas < 1) ctas = 1;
         if (ctas > a.rows) ctas = a.rows;
         if (ctas > 65535) ctas = 65535;
-        e = fmt == kFmtQ8 ? launch_tma_q8(a, p, layout, static_cast<int>(ctas), slots, st, pdl_enabled())
-                          : launch_tma_q4(a, p, layout, static_cast<int>(ctas), slots, st, pdl_enabled());
+        e = fmt == kFmtQ8
+                ? launch_tma_q8(a, p, layout, fused_x, static_cast<int>(ctas), slots, st, pdl_enabled())
+                : launch_tma_q4(a, p, layout, fused_x, static_cast<int>(ctas), slots, st, pdl_enabled());
         return from_cuda(e);
     }
+    if (fused_x) return from_cuda(launch_plain_fx(fmt, layout, a, dev->sms, st));
     return from_cuda(launch_plain(fmt, layout, a, slots, st));
 }
 
@@ -340,6 +413,32 @@ zdmmv_status dmmv_entry(int fmt, const void *w, zdmmv_layout layout, int64_t row
     }
     a.batch = batch;
     return run_dmmv(fmt, layout, a, 1, st);
+}
+
+zdmmv_status dmmv_f32_entry(int fmt, const void *w, int layout, int64_t rows, int64_t cols, const float *x,
+                            int batch, float *y, cudaStream_t st) {
+    if (block_bytes(fmt) == 0) return ZDMMV_ERR_FORMAT;
+    if (layout != ZDMMV_LAYOUT_GGUF && layout != ZDMMV_LAYOUT_REPACKED) return ZDMMV_ERR_LAYOUT;
+    if (rows < 0 || cols <= 0 || cols % kQK || cols / kQK > 0x3fffffff) return ZDMMV_ERR_SHAPE;
+    if (batch < 1 || batch > ZDMMV_MAX_BATCH) return ZDMMV_ERR_SHAPE;
+    if (rows == 0) return ZDMMV_OK;
+    if (!w || !x || !y) return ZDMMV_ERR_NULL;
+    if (!aligned(w, 16) || !aligned(x, 4) || !aligned(y, 4)) return ZDMMV_ERR_ALIGN;
+    DmmvArgs a{};
+    a.w = static_cast<const uint8_t *>(w);
+    a.xf = x;
+    a.xf_stride = cols;
+    a.y = y;
+    a.y_stride = rows;
+    a.rows = rows;
+    a.nb = static_cast<int32_t>(cols / kQK);
+    if (tma_shape_ok(fmt, cols)) {
+        a.batch = 1;
+        return run_dmmv(fmt, layout, a, batch, st, true);
+    }
+    if (static_cast<int64_t>(batch) * a.nb * 34 > kPlainFxMaxSmem) return ZDMMV_ERR_SHAPE;
+    a.batch = batch;
+    return run_dmmv(fmt, layout, a, 1, st, true);
 }
 
 }  // namespace
@@ -439,6 +538,11 @@ zdmmv_status zdmmv_expert_gather(zdmmv_fmt fmt, const void *w_stack, int64_t exp
     a.nb = static_cast<int32_t>(nb);
     a.batch = 1;
     return run_dmmv(fmt, layout, a, n, reinterpret_cast<cudaStream_t>(stream));
+}
+
+zdmmv_status zdmmv_dmmv_f32(zdmmv_fmt fmt, const void *w, zdmmv_layout layout, int64_t rows, int64_t cols,
+                            const float *x, int batch, float *y, zdmmv_stream_t stream) {
+    return dmmv_f32_entry(fmt, w, layout, rows, cols, x, batch, y, reinterpret_cast<cudaStream_t>(stream));
 }
 
 size_t zdmmv_repacked_bytes(zdmmv_fmt fmt, int64_t rows, int64_t cols) {

@@ -141,6 +141,21 @@ constexpr uint32_t kLoNib = 0x0f0f0f0fu;
 constexpr uint32_t kHiNib = 0xf0f0f0f0u;
 constexpr uint32_t kOnes = 0x01010101u;
 
+// Q8_0 quantization of one 32-element block held one element per lane of a full
+// warp: amax = max|x_i|; d = amax/127 (IEEE division); id = d ? 1/d : 0 (IEEE
+// reciprocal); q_i = round(x_i*id) (fp32 product, ties away from zero); the scale
+// is stored as fp16(d), round to nearest even. Returns this lane's code and the
+// scale bits. The same function serves the stand-alone quantizer and the fused
+// DMMV prologue, so both produce identical bytes.
+__device__ __forceinline__ int quantize_q8_0_lane(float v, unsigned short &d_bits) {
+    // for non-negative floats the bit patterns order like the values
+    const float amax = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(v))));
+    const float d = amax / 127.0f;
+    const float id = d != 0.0f ? 1.0f / d : 0.0f;
+    d_bits = __half_as_ushort(__float2half_rn(d));
+    return static_cast<int>(roundf(__fmul_rn(v, id)));
+}
+
 // Sum of the 32 int8 codes of an activation block, times -8 (the Q4_0 offset
 // term), from its eight aligned code words.
 __device__ __forceinline__ int q4_offset_term(const uint32_t (&xw)[8]) {

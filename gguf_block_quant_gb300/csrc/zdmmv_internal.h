@@ -19,6 +19,8 @@ struct DmmvArgs {
     uint32_t *fault;         // device fault word (ZDMMV_FAULT_* bits)
     const uint8_t *xq;       // Q8_0 activation blocks of slot 0
     int64_t xq_stride;       // bytes between slots' activations (0 = shared)
+    const float *xf;         // fp32 activation of slot 0 (fused-quantization kernels)
+    int64_t xf_stride;       // floats between slots' fp32 activations
     float *y;                // output of slot 0
     int64_t y_stride;        // floats between slots' outputs
     int64_t rows;            // rows of the matrix
@@ -50,10 +52,11 @@ bool tma_shape_ok(int fmt, int64_t cols);
 TmaPlan tma_plan(int fmt, int layout, int64_t cols);
 
 // Launchers of the pipelined kernel (one translation unit per format).
-cudaError_t launch_tma_q8(const DmmvArgs &a, const TmaPlan &p, int layout, int ctas_per_slot, int slots,
-                          cudaStream_t st, bool pdl);
-cudaError_t launch_tma_q4(const DmmvArgs &a, const TmaPlan &p, int layout, int ctas_per_slot, int slots,
-                          cudaStream_t st, bool pdl);
+// fused_x: the kernel quantizes the fp32 activation a.xf itself (no a.xq).
+cudaError_t launch_tma_q8(const DmmvArgs &a, const TmaPlan &p, int layout, bool fused_x, int ctas_per_slot,
+                          int slots, cudaStream_t st, bool pdl);
+cudaError_t launch_tma_q4(const DmmvArgs &a, const TmaPlan &p, int layout, bool fused_x, int ctas_per_slot,
+                          int slots, cudaStream_t st, bool pdl);
 // CTAs of the pipelined kernel that fit on one SM for this plan.
 int tma_ctas_per_sm_q8(int layout, const TmaPlan &p);
 int tma_ctas_per_sm_q4(int layout, const TmaPlan &p);

@@ -74,12 +74,42 @@ __device__ __forceinline__ float row_partial(const Pair<FMT, LAYOUT> (&xr)[PPL],
     return acc;
 }
 
-template <int FMT, int LAYOUT, int LPR, int PPL, int STAGES, int MINB>
+// Issue the bulk copy (or copies) of tile t into stage s.
+template <int FMT, int LAYOUT>
+__device__ __forceinline__ void issue_tile(const DmmvArgs &a, const uint8_t *w, int64_t r0, int64_t r1, int t, int s,
+                                           uint8_t *stage0, uint64_t *full, uint64_t pol) {
+    constexpr int kBB = Fmt<FMT>::kBlockBytes;
+    constexpr int kQB = Fmt<FMT>::kQuantBytes;
+    const int T = a.tile_rows;
+    const int nb = a.nb;
+    const int64_t tr0 = r0 + static_cast<int64_t>(t) * T;
+    const int nr = static_cast<int>(min(static_cast<int64_t>(T), r1 - tr0));
+    uint8_t *dst = stage0 + static_cast<size_t>(s) * a.stage_bytes;
+    if constexpr (LAYOUT == kLayoutGguf) {
+        const uint32_t bytes = static_cast<uint32_t>(nr) * static_cast<uint32_t>(nb) * kBB;
+        mbar_arrive_expect_tx(&full[s], bytes);
+        bulk_copy_g2s(dst, w + tr0 * nb * kBB, bytes, &full[s], pol);
+    } else {
+        const uint32_t qbytes = static_cast<uint32_t>(nr) * static_cast<uint32_t>(nb) * kQB;
+        const uint32_t sbytes = static_cast<uint32_t>(nr) * static_cast<uint32_t>(nb) * 2u;
+        mbar_arrive_expect_tx(&full[s], qbytes + sbytes);
+        bulk_copy_g2s(dst, w + tr0 * nb * kQB, qbytes, &full[s], pol);
+        bulk_copy_g2s(dst + static_cast<size_t>(T) * nb * kQB, w + a.rows * nb * kQB + tr0 * nb * 2, sbytes,
+                      &full[s], pol);
+    }
+}
+
+__device__ __forceinline__ void consumer_barrier() {
+    asm volatile("bar.sync 1, %0;" ::"n"(kConsumerThreads) : "memory");
+}
+
+// FX = true: the kernel reads the fp32 activation (a.xf) and quantizes it to
+// Q8_0 blocks in shared memory itself (same device function as the stand-alone
+// quantizer, hence identical bytes), instead of staging a.xq.
+template <int FMT, int LAYOUT, int LPR, int PPL, int STAGES, int MINB, bool FX>
 __global__ void __launch_bounds__(kTmaThreads, MINB) dmmv_tma_kernel(const DmmvArgs a) {
     using P = Pair<FMT, LAYOUT>;
     constexpr int kRowsPar = kConsumerThreads / LPR;
-    constexpr int kBB = Fmt<FMT>::kBlockBytes;
-    constexpr int kQB = Fmt<FMT>::kQuantBytes;
     static_assert(kConsumerThreads % LPR == 0 && LPR <= 32, "row groups must live inside a warp");
 
     extern __shared__ __align__(128) uint8_t smem[];
@@ -96,13 +126,14 @@ __global__ void __launch_bounds__(kTmaThreads, MINB) dmmv_tma_kernel(const DmmvA
     const int64_t r1 = rows * (blockIdx.x + 1) / gridDim.x;
     const int nb = a.nb;
 
-    // everything below reads inputs a preceding kernel may have written
-    pdl_wait();
+    // Dependent launches may start as soon as every CTA of this grid is resident;
+    // what they do before their own dependency wait is stream weights only.
     pdl_launch_dependents();
 
     float *y = a.y + slot * a.y_stride;
     const uint8_t *w = a.w;
     if (a.idx != nullptr) {
+        pdl_wait();  // the index list may be written by the preceding kernel
         const int e = a.idx[slot];
         if (e < 0 || e >= a.n_experts) {
             for (int64_t r = r0 + tid; r < r1; r += blockDim.x) y[r] = __int_as_float(0x7fc00000);
@@ -112,7 +143,6 @@ __global__ void __launch_bounds__(kTmaThreads, MINB) dmmv_tma_kernel(const DmmvA
         w += static_cast<int64_t>(e) * a.expert_stride;
     }
     if (r1 <= r0) return;
-    const uint8_t *xq = a.xq + slot * a.xq_stride;
     const int T = a.tile_rows;
     const int ntiles = static_cast<int>((r1 - r0 + T - 1) / T);
 
@@ -131,36 +161,26 @@ __global__ void __launch_bounds__(kTmaThreads, MINB) dmmv_tma_kernel(const DmmvA
         // ------------------------------------------------------- producer
         if (tid != kConsumerThreads) return;
         const uint64_t wpol = l2_evict_first_policy();
-        const uint64_t xpol = l2_evict_last_policy();
-        const uint32_t xbytes = static_cast<uint32_t>(nb) * 34u;
-        mbar_arrive_expect_tx(xbar, xbytes);
-        bulk_copy_g2s(xs, xq, xbytes, xbar, xpol);
-        int issued = 0;
+        // Weights are read-only parameters: the first STAGES tiles are streamed
+        // before waiting for the preceding kernel, overlapping its tail.
+        const int npre = ntiles < STAGES ? ntiles : STAGES;
+        for (int t = 0; t < npre; ++t) issue_tile<FMT, LAYOUT>(a, w, r0, r1, t, t, stage0, full, wpol);
+        int issued = npre;
+        pdl_wait();
+        if constexpr (!FX) {
+            const uint32_t xbytes = static_cast<uint32_t>(nb) * 34u;
+            mbar_arrive_expect_tx(xbar, xbytes);
+            bulk_copy_g2s(xs, a.xq + slot * a.xq_stride, xbytes, xbar, l2_evict_last_policy());
+        }
         bool ok = true;
-        for (int t = 0; t < ntiles; ++t) {
+        for (int t = npre; t < ntiles; ++t) {
             const int s = t % STAGES;
-            if (t >= STAGES) {
-                if (!mbar_wait(&empty[s], static_cast<uint32_t>((t / STAGES) - 1) & 1u)) {
-                    ok = false;
-                    break;
-                }
-                fence_proxy_async_smem();
+            if (!mbar_wait(&empty[s], static_cast<uint32_t>((t / STAGES) - 1) & 1u)) {
+                ok = false;
+                break;
             }
-            const int64_t tr0 = r0 + static_cast<int64_t>(t) * T;
-            const int nr = static_cast<int>(min(static_cast<int64_t>(T), r1 - tr0));
-            uint8_t *dst = stage0 + static_cast<size_t>(s) * a.stage_bytes;
-            if constexpr (LAYOUT == kLayoutGguf) {
-                const uint32_t bytes = static_cast<uint32_t>(nr) * static_cast<uint32_t>(nb) * kBB;
-                mbar_arrive_expect_tx(&full[s], bytes);
-                bulk_copy_g2s(dst, w + tr0 * nb * kBB, bytes, &full[s], wpol);
-            } else {
-                const uint32_t qbytes = static_cast<uint32_t>(nr) * static_cast<uint32_t>(nb) * kQB;
-                const uint32_t sbytes = static_cast<uint32_t>(nr) * static_cast<uint32_t>(nb) * 2u;
-                mbar_arrive_expect_tx(&full[s], qbytes + sbytes);
-                bulk_copy_g2s(dst, w + tr0 * nb * kQB, qbytes, &full[s], wpol);
-                bulk_copy_g2s(dst + static_cast<size_t>(T) * nb * kQB, w + rows * nb * kQB + tr0 * nb * 2, sbytes,
-                              &full[s], wpol);
-            }
+            fence_proxy_async_smem();
+            issue_tile<FMT, LAYOUT>(a, w, r0, r1, t, s, stage0, full, wpol);
             issued = t + 1;
         }
         if (!ok) atomicOr(a.fault, 1u);
@@ -170,7 +190,7 @@ __global__ void __launch_bounds__(kTmaThreads, MINB) dmmv_tma_kernel(const DmmvA
             const int t_last = (issued - 1 - s) >= 0 ? ((issued - 1 - s) / STAGES) * STAGES + s : -1;
             if (t_last >= 0) (void)mbar_wait(&full[s], static_cast<uint32_t>(t_last / STAGES) & 1u);
         }
-        (void)mbar_wait(xbar, 0);
+        if constexpr (!FX) (void)mbar_wait(xbar, 0);
         return;
     }
 
@@ -178,10 +198,39 @@ __global__ void __launch_bounds__(kTmaThreads, MINB) dmmv_tma_kernel(const DmmvA
     const int lane = tid & 31;
     const int g = tid / LPR;  // row group
     const int l = tid % LPR;  // lane inside the row group
-    // waits are made warp-uniform so a timeout can never split a warp before its shuffles
-    if (!__all_sync(0xffffffffu, mbar_wait(xbar, 0))) {
-        if (lane == 0) atomicOr(a.fault, 1u);
-        return;
+    pdl_wait();               // outputs may still be read, and the activation written, by the preceding kernel
+    if constexpr (FX) {
+        // quantize the fp32 activation into Q8_0 blocks in shared memory: warp
+        // w takes blocks w, w+8, ...; up to 16 loads per lane in flight per round
+        const float *xf = a.xf + slot * a.xf_stride;
+        constexpr int kWarps = kConsumerThreads / 32;
+        constexpr int kRound = 16;
+        const int warp = tid >> 5;
+        for (int b0 = warp; b0 < nb; b0 += kWarps * kRound) {
+            float v[kRound];
+#pragma unroll
+            for (int u = 0; u < kRound; ++u) {
+                const int b = b0 + u * kWarps;
+                v[u] = b < nb ? xf[static_cast<int64_t>(b) * kQK + lane] : 0.0f;
+            }
+#pragma unroll
+            for (int u = 0; u < kRound; ++u) {
+                const int b = b0 + u * kWarps;
+                if (b < nb) {  // warp-uniform
+                    unsigned short d_bits;
+                    const int q = quantize_q8_0_lane(v[u], d_bits);
+                    xs[34 * b + 2 + lane] = static_cast<uint8_t>(static_cast<int8_t>(q));
+                    if (lane == 0) *reinterpret_cast<unsigned short *>(xs + 34 * b) = d_bits;
+                }
+            }
+        }
+        consumer_barrier();
+    } else {
+        // waits are made warp-uniform so a timeout can never split a warp before its shuffles
+        if (!__all_sync(0xffffffffu, mbar_wait(xbar, 0))) {
+            if (lane == 0) atomicOr(a.fault, 1u);
+            return;
+        }
     }
     P xr[PPL];
 #pragma unroll
@@ -217,10 +266,11 @@ __global__ void __launch_bounds__(kTmaThreads, MINB) dmmv_tma_kernel(const DmmvA
 }
 
 // ------------------------------------------------------------------ host side
-template <int FMT, int LAYOUT, int LPR, int PPL, int STAGES>
+template <int FMT, int LAYOUT, int LPR, int PPL, int STAGES, bool FX>
 struct TmaInst {
     static constexpr int kMinBlocks = PPL >= 4 ? 1 : 2;
-    static void *fn() { return reinterpret_cast<void *>(&dmmv_tma_kernel<FMT, LAYOUT, LPR, PPL, STAGES, kMinBlocks>); }
+    static constexpr auto kKernel = &dmmv_tma_kernel<FMT, LAYOUT, LPR, PPL, STAGES, kMinBlocks, FX>;
+    static void *fn() { return reinterpret_cast<void *>(kKernel); }
 
     static cudaError_t prepare() {
         // raise the dynamic shared-memory limit once per device
@@ -252,25 +302,25 @@ struct TmaInst {
         attr[0].val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = attr;
         cfg.numAttrs = pdl ? 1 : 0;
-        return cudaLaunchKernelEx(&cfg, dmmv_tma_kernel<FMT, LAYOUT, LPR, PPL, STAGES, kMinBlocks>, a);
+        return cudaLaunchKernelEx(&cfg, kKernel, a);
     }
 
     static int ctas_per_sm(int smem_bytes) {
         if (prepare() != cudaSuccess) return 1;
         int occ = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, dmmv_tma_kernel<FMT, LAYOUT, LPR, PPL, STAGES, kMinBlocks>,
-                                                          kTmaThreads, static_cast<size_t>(smem_bytes)) != cudaSuccess)
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kKernel, kTmaThreads,
+                                                          static_cast<size_t>(smem_bytes)) != cudaSuccess)
             return 1;
         return occ > 0 ? occ : 1;
     }
 };
 
 // Dispatch over the (lpr, ppl, stages) variants instantiated for one format.
-template <int FMT, int LAYOUT, typename F>
+template <int FMT, int LAYOUT, bool FX, typename F>
 cudaError_t with_variant(const TmaPlan &p, F &&f) {
 #define ZDMMV_VARIANT(LPR_, PPL_, ST_)                                        \
     if (p.lpr == LPR_ && p.ppl == PPL_ && p.stages == ST_)                    \
-        return f(TmaInst<FMT, LAYOUT, LPR_, PPL_, ST_>{});
+        return f(TmaInst<FMT, LAYOUT, LPR_, PPL_, ST_, FX>{});
     ZDMMV_VARIANT(8, 1, 4)
     ZDMMV_VARIANT(16, 1, 4)
     ZDMMV_VARIANT(32, 1, 4)
@@ -286,11 +336,15 @@ cudaError_t with_variant(const TmaPlan &p, F &&f) {
 }
 
 template <int FMT>
-cudaError_t launch_tma_fmt(const DmmvArgs &a, const TmaPlan &p, int layout, int ctas_per_slot, int slots,
-                           cudaStream_t st, bool pdl) {
+cudaError_t launch_tma_fmt(const DmmvArgs &a, const TmaPlan &p, int layout, bool fused_x, int ctas_per_slot,
+                           int slots, cudaStream_t st, bool pdl) {
     auto go = [&](auto inst) { return decltype(inst)::launch(a, p, ctas_per_slot, slots, st, pdl); };
-    if (layout == kLayoutGguf) return with_variant<FMT, kLayoutGguf>(p, go);
-    return with_variant<FMT, kLayoutRepacked>(p, go);
+    if (fused_x) {
+        if (layout == kLayoutGguf) return with_variant<FMT, kLayoutGguf, true>(p, go);
+        return with_variant<FMT, kLayoutRepacked, true>(p, go);
+    }
+    if (layout == kLayoutGguf) return with_variant<FMT, kLayoutGguf, false>(p, go);
+    return with_variant<FMT, kLayoutRepacked, false>(p, go);
 }
 
 template <int FMT>
@@ -301,9 +355,9 @@ int tma_ctas_per_sm_fmt(int layout, const TmaPlan &p) {
         return cudaSuccess;
     };
     if (layout == kLayoutGguf)
-        (void)with_variant<FMT, kLayoutGguf>(p, q);
+        (void)with_variant<FMT, kLayoutGguf, false>(p, q);
     else
-        (void)with_variant<FMT, kLayoutRepacked>(p, q);
+        (void)with_variant<FMT, kLayoutRepacked, false>(p, q);
     return occ;
 }
 

@@ -3,9 +3,9 @@
 
 namespace zdmmv {
 
-cudaError_t launch_tma_q4(const DmmvArgs &a, const TmaPlan &p, int layout, int ctas_per_slot, int slots,
-                          cudaStream_t st, bool pdl) {
-    return launch_tma_fmt<kFmtQ4>(a, p, layout, ctas_per_slot, slots, st, pdl);
+cudaError_t launch_tma_q4(const DmmvArgs &a, const TmaPlan &p, int layout, bool fused_x, int ctas_per_slot,
+                          int slots, cudaStream_t st, bool pdl) {
+    return launch_tma_fmt<kFmtQ4>(a, p, layout, fused_x, ctas_per_slot, slots, st, pdl);
 }
 
 int tma_ctas_per_sm_q4(int layout, const TmaPlan &p) { return tma_ctas_per_sm_fmt<kFmtQ4>(layout, p); }

@@ -53,6 +53,7 @@ _SIGS = {
     "zdmmv_q4_0": ([_vp, _int, _i64, _i64, _vp, _vp, _vp], _int),
     "zdmmv_q8_0_batched": ([_vp, _int, _i64, _i64, _vp, _int, _vp, _vp], _int),
     "zdmmv_q4_0_batched": ([_vp, _int, _i64, _i64, _vp, _int, _vp, _vp], _int),
+    "zdmmv_dmmv_f32": ([_int, _vp, _int, _i64, _i64, _vp, _int, _vp, _vp], _int),
     "zdmmv_expert_gather": ([_int, _vp, _i64, _int, _i64, _i64, _vp, _int, _int, _vp, _i64, _vp, _vp, _vp],
                             _int),
     "zdmmv_repacked_bytes": ([_int, _i64, _i64], ctypes.c_size_t),
@@ -172,6 +173,17 @@ def dmmv(fmt: int, w, rows: int, cols: int, xq, y=None, layout: int = GGUF, stre
 def dmmv_batched(fmt: int, w, rows: int, cols: int, xq, batch: int, y=None, layout: int = GGUF, stream=None):
     f = q8_0_batched if fmt == Q8_0 else q4_0_batched
     return f(w, rows, cols, xq, batch, y=y, layout=layout, stream=stream)
+
+
+def dmmv_f32(fmt: int, w, rows: int, cols: int, x, batch: int = 1, y=None, layout: int = GGUF,
+             stream=None):
+    """Fused decode step: quantize the fp32 activation x ([batch][cols]) and run
+    the DMMV in one launch; identical to quantize_act_q8_0 followed by dmmv."""
+    if x.dtype != torch.float32 or x.numel() != batch * cols:
+        raise ValueError("dmmv_f32: x must be float32 [batch][cols]")
+    y = _out(y, (batch, rows) if batch > 1 else (rows,), w.device)
+    _call("zdmmv_dmmv_f32", fmt, _ptr(w), layout, rows, cols, _ptr(x), batch, _ptr(y), _stream(stream))
+    return y
 
 
 def expert_gather(fmt: int, w_stack, expert_stride: int, rows: int, cols: int, idx, n_experts: int, xq,

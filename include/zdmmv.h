@@ -37,6 +37,15 @@
  *    default stream). Argument errors are returned synchronously before any
  *    launch; launch failures return ZDMMV_ERR_CUDA. No entry point
  *    synchronizes the device except zdmmv_device_status.
+ *  - Weight matrices are treated as read-only model parameters: with
+ *    programmatic dependent launch the DMMV kernels start streaming weight
+ *    tiles before the preceding kernel in the stream has finished (activations,
+ *    expert indices and outputs are touched only after it has). A weight buffer
+ *    must therefore be complete before the DMMV that reads it is enqueued
+ *    behind a kernel still writing it; enqueue an event or synchronize in
+ *    between if weights are produced on the device (zdmmv_repack's output may
+ *    be used directly: its kernel never releases dependents early). Set the
+ *    environment variable ZDMMV_PDL=0 to disable programmatic dependent launch.
  *  - There is no CPU fallback: every result is computed by the CUDA kernels.
  *  - Inputs must be finite (a NaN or infinite activation gives unspecified
  *    codes).
@@ -126,6 +135,22 @@ zdmmv_status zdmmv_q8_0_batched(const void *w, zdmmv_layout layout, int64_t rows
 zdmmv_status zdmmv_q4_0_batched(const void *w, zdmmv_layout layout, int64_t rows,
                                 int64_t cols, const void *xq, int batch, float *y,
                                 zdmmv_stream_t stream);
+
+/* Fused decode step: the same result as zdmmv_quantize_act_q8_0 followed by
+ * zdmmv_q{8,4}_0(_batched), bit for bit, in ONE launch. Each CTA quantizes the
+ * fp32 activation to Q8_0 blocks in shared memory itself, so a chain of decode
+ * layers pays one kernel per layer instead of two (per-token launch chains:
+ * "RTX 5090: Batched Prefill & CUDA Graphs in ZINC", "CUDA graphs -- the
+ * structural answer to launch latency").
+ *   fmt    ZDMMV_Q8_0 or ZDMMV_Q4_0 weights; w, layout, rows, cols as zdmmv_q8_0.
+ *   x      device fp32 [batch][cols], 4-byte aligned; batch 1..8.
+ *   y      device fp32 [batch][rows].
+ * Shapes off the pipelined path (cols % 256 != 0 or cols > 8192) need
+ * batch*cols/32*34 <= 200 KiB of shared memory, else ERR_SHAPE.
+ * Errors: as zdmmv_q8_0_batched, plus ERR_FORMAT. */
+zdmmv_status zdmmv_dmmv_f32(zdmmv_fmt fmt, const void *w, zdmmv_layout layout, int64_t rows,
+                            int64_t cols, const float *x, int batch, float *y,
+                            zdmmv_stream_t stream);
 
 /* MoE expert gather: n matrices picked by index from a stack of n_experts
  * equally shaped matrices, all in ONE launch (routed experts are selected per

@@ -232,7 +232,8 @@ def test_batched_matches_oracle_and_single_calls(fmt, rows, cols, batch, layout)
     nbx = cols // 32 * 34
     for v in range(batch):
         ys = nan_out(rows)
-        Z.dmmv(fmt, wd, rows, cols, xq[v * nbx:(v + 1) * nbx], y=ys, layout=layout)
+        # a separate (16-byte aligned) copy of vector v's blocks
+        Z.dmmv(fmt, wd, rows, cols, xq[v * nbx:(v + 1) * nbx].clone(), y=ys, layout=layout)
         torch.cuda.synchronize()
         assert torch.equal(ys, y[v]), "batched result differs from the single-vector call"
 
@@ -302,3 +303,57 @@ def test_host_step_matches_oracle(fmt, rows, cols, batch):
     xq_ref = oracle.quantize_q8_0(x)
     y_ref, e_ref = oracle.dmmv_batched(fmt, w, rows, cols, xq_ref, batch)
     check_y(yh, y_ref, e_ref)
+
+
+# ------------------------------------------------------- fused fp32 activation
+@pytest.mark.parametrize("layout", [Z.GGUF, Z.REPACKED])
+@pytest.mark.parametrize("fmt,rows,cols,batch", [(Q4_0, 4096, 4096, 1), (Q8_0, 1531, 2048, 1),
+                                                 (Q8_0, 700, 512, 3), (Q4_0, 99, 8192, 8),
+                                                 (Q8_0, 37, 96, 1), (Q4_0, 77, 160, 5), (Q8_0, 5, 14336, 2)])
+def test_fused_f32_equals_quantize_then_dmmv_bitwise(fmt, rows, cols, batch, layout):
+    w = synth.weight_blocks(fmt, rows, cols, seed=cols + batch)
+    x = synth.activations(cols, seed=rows, batch=batch)
+    wd = dev(w)
+    if layout == Z.REPACKED:
+        wd = Z.repack(fmt, wd, rows, cols)
+    xd = dev(x)
+    yf = nan_out(batch, rows)
+    Z.dmmv_f32(fmt, wd, rows, cols, xd, batch=batch, y=yf, layout=layout)
+    xq = Z.quantize_act_q8_0(xd)
+    yu = nan_out(batch, rows)
+    Z.dmmv_batched(fmt, wd, rows, cols, xq, batch, y=yu, layout=layout)
+    torch.cuda.synchronize()
+    assert torch.equal(yf, yu), "fused and two-kernel results differ"
+    y_ref, e_ref = oracle.dmmv_batched(fmt, w, rows, cols, oracle.quantize_q8_0(x), batch)
+    check_y(yf, y_ref, e_ref)
+
+
+def test_fused_f32_chain_with_reused_buffers():
+    """A decode chain whose layers reuse ping-pong activation/output buffers:
+    each layer's input is the previous layer's output (dependent launches)."""
+    rows = cols = 2048
+    fmt = Q4_0
+    ws = [synth.weight_blocks(fmt, rows, cols, seed=300 + i) for i in range(6)]
+    x = synth.activations(cols, seed=301)
+    bufs = [dev(x), nan_out(rows)]
+    wds = [dev(w) for w in ws]
+    for i, wd in enumerate(wds):
+        Z.dmmv_f32(fmt, wd, rows, cols, bufs[i % 2], y=bufs[(i + 1) % 2])
+    torch.cuda.synchronize()
+    got = bufs[len(wds) % 2].cpu().numpy()
+    # the same chain through the oracle (each layer's fp32 output rounded to fp32 as the kernel stores it)
+    cur = x
+    for i, w in enumerate(ws):
+        y_ref, e_ref = oracle.dmmv(fmt, w, rows, cols, oracle.quantize_q8_0(cur))
+        if i == len(ws) - 1:
+            ok, worst = oracle.within_tolerance(got, y_ref, e_ref)
+            assert ok, worst
+        else:
+            # the next layer consumes the kernel's own output (fp32); take it from a second run
+            yk = nan_out(rows)
+            Z.dmmv_f32(fmt, wds[i], rows, cols, dev(cur), y=yk)
+            torch.cuda.synchronize()
+            yk = yk.cpu().numpy()
+            ok, worst = oracle.within_tolerance(yk, y_ref, e_ref)
+            assert ok, worst
+            cur = yk
