@@ -60,6 +60,19 @@ bool pdl_enabled() {
     return on;
 }
 
+// CTAs of one pipelined launch per SM: kCtasPerSmSmall below kLargeLaunchBytes
+// of weights, kCtasPerSmLarge above (environment ZDMMV_CTAS_PER_SM, 1..8,
+// overrides both).
+int ctas_per_sm_per_launch(int64_t weight_bytes) {
+    static const int forced = [] {
+        const char *e = std::getenv("ZDMMV_CTAS_PER_SM");
+        const int n = e ? std::atoi(e) : 0;
+        return (n >= 1 && n <= 8) ? n : 0;
+    }();
+    if (forced) return forced;
+    return weight_bytes >= kLargeLaunchBytes ? kCtasPerSmLarge : kCtasPerSmSmall;
+}
+
 inline bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 inline int block_bytes(int fmt) { return fmt == kFmtQ8 ? 34 : (fmt == kFmtQ4 ? 18 : 0); }
 inline int64_t round_up(int64_t v, int64_t m) { return (v + m - 1) / m * m; }
@@ -69,6 +82,18 @@ zdmmv_status from_cuda(cudaError_t e) { return e == cudaSuccess ? ZDMMV_OK : ZDM
 }  // namespace
 
 // ------------------------------------------------------------ planning
+namespace {
+// Target bytes of one pipeline stage (environment ZDMMV_STAGE_KB, 4..64).
+int stage_target_bytes() {
+    static const int v = [] {
+        const char *e = std::getenv("ZDMMV_STAGE_KB");
+        const int n = e ? std::atoi(e) : 0;
+        return (n >= 4 && n <= 64 ? n : 20) * 1024;
+    }();
+    return v;
+}
+}  // namespace
+
 bool tma_shape_ok(int fmt, int64_t cols) {
     if (block_bytes(fmt) == 0 || cols <= 0 || cols % kQK) return false;
     const int64_t nb = cols / kQK;
@@ -95,14 +120,19 @@ TmaPlan tma_plan(int fmt, int layout, int64_t cols) {
     }
     const int rows_par = kConsumerThreads / p.lpr;
     const int row_bytes = nb * block_bytes(fmt);
-    const int unit = rows_par * row_bytes;        // bytes of one pass of the row groups
-    constexpr int kStageTarget = 24 * 1024;
-    const int m = unit >= kStageTarget ? 1 : kStageTarget / unit;
-    p.tile_rows = rows_par * m;
+    const int stage_target = stage_target_bytes();
+    // a tile is a whole number of passes of the row groups (kTmaRowsIlp rows each
+    // when that fits the stage target)
+    int unit_rows = rows_par * kTmaRowsIlp;
+    if (unit_rows * row_bytes > stage_target) unit_rows = rows_par;
+    const int unit = unit_rows * row_bytes;
+    const int m = unit >= stage_target ? 1 : stage_target / unit;
+    p.tile_rows = unit_rows * m;
     p.stage_bytes = static_cast<int>(round_up(static_cast<int64_t>(p.tile_rows) * row_bytes, 128));
     p.x_bytes_padded = static_cast<int>(round_up(static_cast<int64_t>(nb) * 34, 128));
     p.stages = 4;
-    if (kBarrierBytes + p.x_bytes_padded + 4 * p.stage_bytes > 112 * 1024) p.stages = 3;
+    while (p.stages > 2 && kBarrierBytes + p.x_bytes_padded + p.stages * p.stage_bytes > kSmemPerCtaTarget)
+        --p.stages;
     p.smem_bytes = kBarrierBytes + p.x_bytes_padded + p.stages * p.stage_bytes;
     return p;
 }
@@ -362,7 +392,10 @@ zdmmv_status run_dmmv(int fmt, int layout, DmmvArgs a, int slots, cudaStream_t s
         a.tile_rows = p.tile_rows;
         a.stage_bytes = p.stage_bytes;
         a.x_bytes_padded = p.x_bytes_padded;
-        const int per_sm = fmt == kFmtQ8 ? tma_ctas_per_sm_q8(layout, p) : tma_ctas_per_sm_q4(layout, p);
+        int per_sm = fmt == kFmtQ8 ? tma_ctas_per_sm_q8(layout, p) : tma_ctas_per_sm_q4(layout, p);
+        const int64_t launch_bytes = a.rows * a.nb * static_cast<int64_t>(block_bytes(fmt)) * slots;
+        const int want = ctas_per_sm_per_launch(launch_bytes);
+        if (per_sm > want) per_sm = want;
         const int64_t total = static_cast<int64_t>(dev->sms) * per_sm;
         int64_t ctas = total / slots;
         if (ctas < 1) ctas = 1;
@@ -423,7 +456,7 @@ zdmmv_status dmmv_f32_entry(int fmt, const void *w, int layout, int64_t rows, in
     if (batch < 1 || batch > ZDMMV_MAX_BATCH) return ZDMMV_ERR_SHAPE;
     if (rows == 0) return ZDMMV_OK;
     if (!w || !x || !y) return ZDMMV_ERR_NULL;
-    if (!aligned(w, 16) || !aligned(x, 4) || !aligned(y, 4)) return ZDMMV_ERR_ALIGN;
+    if (!aligned(w, 16) || !aligned(x, 16) || !aligned(y, 4)) return ZDMMV_ERR_ALIGN;
     DmmvArgs a{};
     a.w = static_cast<const uint8_t *>(w);
     a.xf = x;

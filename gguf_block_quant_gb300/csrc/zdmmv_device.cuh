@@ -156,6 +156,26 @@ __device__ __forceinline__ int quantize_q8_0_lane(float v, unsigned short &d_bit
     return static_cast<int>(roundf(__fmul_rn(v, id)));
 }
 
+// The same quantizer with four blocks per warp: lanes 8k..8k+7 hold block k's
+// elements (4 per lane, lane 8k+j has elements 4j..4j+3). The block maximum is an
+// exact max, reduced over the 8 lanes, and d, id and the codes use exactly the
+// operations of quantize_q8_0_lane, so the bytes are identical. Returns the four
+// codes packed little-endian.
+__device__ __forceinline__ uint32_t quantize_q8_0_quad(float4 v, unsigned short &d_bits) {
+    float m = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
+    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+    const float d = m / 127.0f;
+    const float id = d != 0.0f ? 1.0f / d : 0.0f;
+    d_bits = __half_as_ushort(__float2half_rn(d));
+    const uint32_t q0 = static_cast<uint8_t>(static_cast<int8_t>(static_cast<int>(roundf(__fmul_rn(v.x, id)))));
+    const uint32_t q1 = static_cast<uint8_t>(static_cast<int8_t>(static_cast<int>(roundf(__fmul_rn(v.y, id)))));
+    const uint32_t q2 = static_cast<uint8_t>(static_cast<int8_t>(static_cast<int>(roundf(__fmul_rn(v.z, id)))));
+    const uint32_t q3 = static_cast<uint8_t>(static_cast<int8_t>(static_cast<int>(roundf(__fmul_rn(v.w, id)))));
+    return q0 | (q1 << 8) | (q2 << 16) | (q3 << 24);
+}
+
 // Sum of the 32 int8 codes of an activation block, times -8 (the Q4_0 offset
 // term), from its eight aligned code words.
 __device__ __forceinline__ int q4_offset_term(const uint32_t (&xw)[8]) {

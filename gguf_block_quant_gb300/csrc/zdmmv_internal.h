@@ -42,10 +42,19 @@ struct TmaPlan {
     int smem_bytes;  // dynamic shared memory per CTA
 };
 
-constexpr int kConsumerThreads = 256;  // 8 consumer warps
+constexpr int kConsumerThreads = 128;  // 4 consumer warps
 constexpr int kProducerThreads = 32;   // 1 producer warp (one lane issues the copies)
 constexpr int kTmaThreads = kConsumerThreads + kProducerThreads;
 constexpr int kBarrierBytes = 256;     // shared-memory prefix holding the mbarriers
+// CTAs of one pipelined launch per SM. A small launch takes fewer than fit (4 by
+// registers and shared memory) on purpose: the free slots let the next decode
+// kernel in the stream become resident and stream its weights while this one
+// finishes (programmatic dependent launch). A large launch takes them all.
+constexpr int kCtasPerSmSmall = 2;
+constexpr int kCtasPerSmLarge = 4;
+constexpr int64_t kLargeLaunchBytes = 32ll << 20;  // weight bytes per launch
+constexpr int kSmemPerCtaTarget = 54 * 1024;         // keeps 4 CTAs per SM possible
+constexpr int kTmaRowsIlp = 2;                       // rows per row group in flight
 
 // Whether the pipelined kernel takes this shape, and its plan.
 bool tma_shape_ok(int fmt, int64_t cols);

@@ -24,6 +24,8 @@
 //    device fault word, drains its own copies (bounded) and returns.
 #pragma once
 
+#include <atomic>
+
 #include "zdmmv_device.cuh"
 #include "zdmmv_internal.h"
 
@@ -110,6 +112,7 @@ template <int FMT, int LAYOUT, int LPR, int PPL, int STAGES, int MINB, bool FX>
 __global__ void __launch_bounds__(kTmaThreads, MINB) dmmv_tma_kernel(const DmmvArgs a) {
     using P = Pair<FMT, LAYOUT>;
     constexpr int kRowsPar = kConsumerThreads / LPR;
+    constexpr int kRowsIlp = kTmaRowsIlp;
     static_assert(kConsumerThreads % LPR == 0 && LPR <= 32, "row groups must live inside a warp");
 
     extern __shared__ __align__(128) uint8_t smem[];
@@ -200,27 +203,34 @@ __global__ void __launch_bounds__(kTmaThreads, MINB) dmmv_tma_kernel(const DmmvA
     const int l = tid % LPR;  // lane inside the row group
     pdl_wait();               // outputs may still be read, and the activation written, by the preceding kernel
     if constexpr (FX) {
-        // quantize the fp32 activation into Q8_0 blocks in shared memory: warp
-        // w takes blocks w, w+8, ...; up to 16 loads per lane in flight per round
+        // quantize the fp32 activation into Q8_0 blocks in shared memory: each
+        // warp takes four blocks per iteration (16-byte loads, 8 lanes per block)
         const float *xf = a.xf + slot * a.xf_stride;
         constexpr int kWarps = kConsumerThreads / 32;
-        constexpr int kRound = 16;
+        constexpr int kRound = 8;
         const int warp = tid >> 5;
-        for (int b0 = warp; b0 < nb; b0 += kWarps * kRound) {
-            float v[kRound];
+        const int sub = lane >> 3;  // block within the quad
+        const int j = lane & 7;     // 4-element group within the block
+        const int nquads = nb >> 2; // nb is a multiple of 8 on this path
+        for (int q0 = warp; q0 < nquads; q0 += kWarps * kRound) {
+            float4 v[kRound];
 #pragma unroll
             for (int u = 0; u < kRound; ++u) {
-                const int b = b0 + u * kWarps;
-                v[u] = b < nb ? xf[static_cast<int64_t>(b) * kQK + lane] : 0.0f;
+                const int qd = q0 + u * kWarps;
+                v[u] = qd < nquads ? *reinterpret_cast<const float4 *>(xf + static_cast<int64_t>(4 * qd + sub) * kQK + 4 * j)
+                                   : make_float4(0.f, 0.f, 0.f, 0.f);
             }
 #pragma unroll
             for (int u = 0; u < kRound; ++u) {
-                const int b = b0 + u * kWarps;
-                if (b < nb) {  // warp-uniform
+                const int qd = q0 + u * kWarps;
+                if (qd < nquads) {  // warp-uniform
                     unsigned short d_bits;
-                    const int q = quantize_q8_0_lane(v[u], d_bits);
-                    xs[34 * b + 2 + lane] = static_cast<uint8_t>(static_cast<int8_t>(q));
-                    if (lane == 0) *reinterpret_cast<unsigned short *>(xs + 34 * b) = d_bits;
+                    const uint32_t codes = quantize_q8_0_quad(v[u], d_bits);
+                    uint8_t *blk = xs + 34 * (4 * qd + sub);
+                    uint16_t *dst = reinterpret_cast<uint16_t *>(blk + 2 + 4 * j);  // 2-byte aligned
+                    dst[0] = static_cast<uint16_t>(codes & 0xffffu);
+                    dst[1] = static_cast<uint16_t>(codes >> 16);
+                    if (j == 0) *reinterpret_cast<unsigned short *>(blk) = d_bits;
                 }
             }
         }
@@ -252,13 +262,25 @@ __global__ void __launch_bounds__(kTmaThreads, MINB) dmmv_tma_kernel(const DmmvA
         const uint8_t *st = stage0 + static_cast<size_t>(s) * a.stage_bytes;
         const int64_t tr0 = r0 + static_cast<int64_t>(t) * T;
         const int nr = static_cast<int>(min(static_cast<int64_t>(T), r1 - tr0));
-        for (int base = 0; base < nr; base += kRowsPar) {
-            const int i = base + g;
-            float acc = 0.0f;
-            if (i < nr) acc = row_partial<FMT, LAYOUT, LPR, PPL>(xr, st, i, T, nb, l);
+        // kRowsIlp rows per row group at a time: independent loads, dot chains and
+        // shuffle trees interleave; every row still gets the same reduction tree
+        for (int base = 0; base < nr; base += kRowsPar * kRowsIlp) {
+            float acc[kRowsIlp];
 #pragma unroll
-            for (int o = LPR / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-            if (l == 0 && i < nr) y[tr0 + i] = acc;
+            for (int r = 0; r < kRowsIlp; ++r) {
+                const int i = base + r * kRowsPar + g;
+                acc[r] = i < nr ? row_partial<FMT, LAYOUT, LPR, PPL>(xr, st, i, T, nb, l) : 0.0f;
+            }
+#pragma unroll
+            for (int o = LPR / 2; o > 0; o >>= 1) {
+#pragma unroll
+                for (int r = 0; r < kRowsIlp; ++r) acc[r] += __shfl_xor_sync(0xffffffffu, acc[r], o);
+            }
+#pragma unroll
+            for (int r = 0; r < kRowsIlp; ++r) {
+                const int i = base + r * kRowsPar + g;
+                if (l == 0 && i < nr) y[tr0 + i] = acc[r];
+            }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);
@@ -268,7 +290,7 @@ __global__ void __launch_bounds__(kTmaThreads, MINB) dmmv_tma_kernel(const DmmvA
 // ------------------------------------------------------------------ host side
 template <int FMT, int LAYOUT, int LPR, int PPL, int STAGES, bool FX>
 struct TmaInst {
-    static constexpr int kMinBlocks = PPL >= 4 ? 1 : 2;
+    static constexpr int kMinBlocks = PPL >= 4 ? 2 : 4;
     static constexpr auto kKernel = &dmmv_tma_kernel<FMT, LAYOUT, LPR, PPL, STAGES, kMinBlocks, FX>;
     static void *fn() { return reinterpret_cast<void *>(kKernel); }
 
@@ -305,13 +327,27 @@ struct TmaInst {
         return cudaLaunchKernelEx(&cfg, kKernel, a);
     }
 
+    // CTAs per SM for this shared-memory size; the occupancy query is cached per
+    // device (one entry: a decode stream calls the same shapes over and over)
     static int ctas_per_sm(int smem_bytes) {
+        static std::atomic<uint64_t> cache[64];  // (smem_bytes << 32) | occupancy, per device
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+        const bool cacheable = dev >= 0 && dev < 64;
+        if (cacheable) {
+            const uint64_t c = cache[dev].load(std::memory_order_relaxed);
+            if (c != 0 && static_cast<int>(c >> 32) == smem_bytes) return static_cast<int>(c & 0xffffffffu);
+        }
         if (prepare() != cudaSuccess) return 1;
         int occ = 0;
         if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kKernel, kTmaThreads,
                                                           static_cast<size_t>(smem_bytes)) != cudaSuccess)
             return 1;
-        return occ > 0 ? occ : 1;
+        occ = occ > 0 ? occ : 1;
+        if (cacheable)
+            cache[dev].store((static_cast<uint64_t>(smem_bytes) << 32) | static_cast<uint32_t>(occ),
+                             std::memory_order_relaxed);
+        return occ;
     }
 };
 
@@ -331,6 +367,11 @@ cudaError_t with_variant(const TmaPlan &p, F &&f) {
     ZDMMV_VARIANT(32, 1, 3)
     ZDMMV_VARIANT(32, 2, 3)
     ZDMMV_VARIANT(32, 4, 3)
+    ZDMMV_VARIANT(8, 1, 2)
+    ZDMMV_VARIANT(16, 1, 2)
+    ZDMMV_VARIANT(32, 1, 2)
+    ZDMMV_VARIANT(32, 2, 2)
+    ZDMMV_VARIANT(32, 4, 2)
 #undef ZDMMV_VARIANT
     return cudaErrorInvalidConfiguration;
 }

@@ -143,7 +143,7 @@ zdmmv_status zdmmv_q4_0_batched(const void *w, zdmmv_layout layout, int64_t rows
  * "RTX 5090: Batched Prefill & CUDA Graphs in ZINC", "CUDA graphs -- the
  * structural answer to launch latency").
  *   fmt    ZDMMV_Q8_0 or ZDMMV_Q4_0 weights; w, layout, rows, cols as zdmmv_q8_0.
- *   x      device fp32 [batch][cols], 4-byte aligned; batch 1..8.
+ *   x      device fp32 [batch][cols], 16-byte aligned; batch 1..8.
  *   y      device fp32 [batch][rows].
  * Shapes off the pipelined path (cols % 256 != 0 or cols > 8192) need
  * batch*cols/32*34 <= 200 KiB of shared memory, else ERR_SHAPE.

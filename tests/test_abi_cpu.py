@@ -87,6 +87,6 @@ def test_other_argument_checks(L):
     assert f(3, FAKE, 0, 4, 64, FAKE, 1, FAKE, None) == 5
     assert f(8, FAKE, 2, 4, 64, FAKE, 1, FAKE, None) == 4
     assert f(8, FAKE, 0, 4, 64, FAKE, 9, FAKE, None) == 2
-    assert f(8, FAKE, 0, 4, 64, FAKE + 2, 1, FAKE, None) == 3
+    assert f(8, FAKE, 0, 4, 64, FAKE + 4, 1, FAKE, None) == 3
     assert f(8, FAKE + 8, 0, 4, 64, FAKE, 1, FAKE, None) == 3
     assert L.zdmmv_debug_block_sums(8, FAKE, 0, 4, 40, FAKE, FAKE, None) == 2
