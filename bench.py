@@ -229,15 +229,19 @@ def time_fn(run, steps: int, warmup: int, world: int, device, sampler=None):
 
 
 class DensePool:
-    """LAYERS distinct copies of one dense workload's tensors, resident in HBM."""
+    """LAYERS distinct copies of one dense workload's tensors, resident in HBM
+    (weights in the GGUF layout, or repacked once when layout == REPACKED)."""
 
-    def __init__(self, cfg, layers: int):
+    def __init__(self, cfg, layers: int, layout: int = 0):
         import numpy as np
         import torch
         from gguf_block_quant_gb300 import synth
         from gguf_block_quant_gb300 import zdmmv as Z
         self.cfg, self.layers = cfg, layers
         w = torch.from_numpy(synth.weight_blocks(cfg.fmt, cfg.rows, cfg.cols, seed=cfg.seed)).cuda()
+        if layout == Z.REPACKED:
+            w = Z.repack(cfg.fmt, w, cfg.rows, cfg.cols)
+        self.layout = layout
         self.w = [w] + [w.clone() for _ in range(layers - 1)]
         x = synth.activations(cfg.cols, seed=cfg.seed, scale=cfg.x_scale, batch=max(cfg.batch, 1))
         x = torch.from_numpy(np.ascontiguousarray(x).reshape(-1)).cuda()
@@ -253,7 +257,7 @@ class DensePool:
         """One decode token: per layer the fused quantize + DMMV (one launch)."""
         Z, c = self.Z, self.cfg
         for l in range(self.layers):
-            Z.dmmv_f32(c.fmt, self.w[l], c.rows, c.cols, self.x[l], batch=c.batch, y=self.y[l])
+            Z.dmmv_f32(c.fmt, self.w[l], c.rows, c.cols, self.x[l], batch=c.batch, y=self.y[l], layout=self.layout)
 
     def step_unfused(self):
         """The same token with the two-kernel chain: quantize, then DMMV."""
@@ -261,17 +265,19 @@ class DensePool:
         for l in range(self.layers):
             Z.quantize_act_q8_0(self.x[l], self.xq[l])
             if c.batch == 1:
-                Z.dmmv(c.fmt, self.w[l], c.rows, c.cols, self.xq[l], y=self.y[l])
+                Z.dmmv(c.fmt, self.w[l], c.rows, c.cols, self.xq[l], y=self.y[l], layout=self.layout)
             else:
-                Z.dmmv_batched(c.fmt, self.w[l], c.rows, c.cols, self.xq[l], c.batch, y=self.y[l])
+                Z.dmmv_batched(c.fmt, self.w[l], c.rows, c.cols, self.xq[l], c.batch, y=self.y[l],
+                               layout=self.layout)
 
     def dmmv_only(self):
         Z, c = self.Z, self.cfg
         for l in range(self.layers):
             if c.batch == 1:
-                Z.dmmv(c.fmt, self.w[l], c.rows, c.cols, self.xq[l], y=self.y[l])
+                Z.dmmv(c.fmt, self.w[l], c.rows, c.cols, self.xq[l], y=self.y[l], layout=self.layout)
             else:
-                Z.dmmv_batched(c.fmt, self.w[l], c.rows, c.cols, self.xq[l], c.batch, y=self.y[l])
+                Z.dmmv_batched(c.fmt, self.w[l], c.rows, c.cols, self.xq[l], c.batch, y=self.y[l],
+                               layout=self.layout)
 
 
 def layers_for(cfg, l2_bytes: int, min_layers: int = 2) -> int:
@@ -279,9 +285,9 @@ def layers_for(cfg, l2_bytes: int, min_layers: int = 2) -> int:
     return max(min_layers, -(-4 * l2_bytes // per))
 
 
-def measure_dense(cfg, layers, steps, warmup, world, device, eager):
+def measure_dense(cfg, layers, steps, warmup, world, device, eager, layout=0):
     import torch
-    pool = DensePool(cfg, layers)
+    pool = DensePool(cfg, layers, layout)
     run = graph_or_eager(pool.dmmv_only, eager)
     pool_step = graph_or_eager(pool.step, eager)
     pool_step2 = graph_or_eager(pool.step_unfused, eager)
@@ -351,8 +357,11 @@ def measure_moe(steps, warmup, world, device, eager, l2_bytes):
 
 
 def e2e_dense(cfg, layers, steps, warmup, world, device, eager=False):
-    """Through the public host-buffer C-ABI call: per layer, H2D of the fp32
-    activation from pinned memory, quantize, DMMV, D2H of y to pinned memory."""
+    """End to end through the public API: every step uploads the step's fp32
+    activations (one per layer) from pinned host memory, runs the fused
+    quantize + DMMV of every layer, and reads every layer's output back into
+    pinned host memory; copies and kernels are replayed as one graph (the pages
+    fold the token's upload and readback into the graph as copy nodes)."""
     import numpy as np
     import torch
     from gguf_block_quant_gb300 import synth
@@ -360,26 +369,25 @@ def e2e_dense(cfg, layers, steps, warmup, world, device, eager=False):
     w = torch.from_numpy(synth.weight_blocks(cfg.fmt, cfg.rows, cfg.cols, seed=cfg.seed)).cuda()
     ws_ = [w] + [w.clone() for _ in range(layers - 1)]
     x = synth.activations(cfg.cols, seed=cfg.seed, scale=cfg.x_scale)
-    xh = [torch.from_numpy(np.ascontiguousarray(x)).pin_memory() for _ in range(layers)]
-    yh = [torch.empty(cfg.rows, dtype=torch.float32).pin_memory() for _ in range(layers)]
-    wsb = Z.host_step_workspace_bytes(cfg.rows, cfg.cols, 1)
-    work = [torch.empty(wsb, dtype=torch.uint8, device="cuda") for _ in range(layers)]
+    xh = torch.from_numpy(np.ascontiguousarray(np.tile(x, (layers, 1)))).pin_memory()
+    yh = torch.empty(layers, cfg.rows, dtype=torch.float32).pin_memory()
+    xd = torch.empty(layers, cfg.cols, dtype=torch.float32, device="cuda")
+    yd = torch.empty(layers, cfg.rows, dtype=torch.float32, device="cuda")
 
     def step():
+        xd.copy_(xh, non_blocking=True)
         for l in range(layers):
-            Z.host_step(cfg.fmt, ws_[l], cfg.rows, cfg.cols, xh[l], yh[l], work[l])
+            Z.dmmv_f32(cfg.fmt, ws_[l], cfg.rows, cfg.cols, xd[l], y=yd[l])
+        yh.copy_(yd, non_blocking=True)
 
-    # the per-token chain with its pinned-memory copies captured once and replayed
-    # (the upload and readback become graph copy nodes)
     run = graph_or_eager(step, eager)
     ms, _ = time_fn(run, steps, warmup, world, device)
     per_step = ms / 1e3 / steps
-    h2d = layers * cfg.cols * 4
-    d2h = layers * cfg.rows * 4
     return {"value": layers * cfg.algorithmic_bytes() * world / per_step / 1e9, "unit": "GB/s",
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms / steps,
+            "h2d_bytes_per_step": xh.numel() * 4, "d2h_bytes_per_step": yh.numel() * 4,
+            "ms_per_step": ms / steps,
             "launch": ("eager" if eager else "cuda_graph replay") +
-                      " of zdmmv_host_step per layer (H2D of x from pinned memory, quantize, DMMV, D2H of y)"}
+                      ": pinned H2D of the step's activations, fused quantize + DMMV per layer, pinned D2H of the outputs"}
 
 
 def gpu_arm(args):
@@ -430,6 +438,10 @@ def gpu_arm(args):
             workloads[c.name] = measure_dense(c, layers_for(c, l2), max(5, args.steps // 4), args.warmup,
                                               world, device, args.eager)
             workloads[c.name]["pct_of_peak"] = 100 * workloads[c.name]["dmmv_gbs"] / hbm_peak
+            rp = measure_dense(c, layers_for(c, l2), max(5, args.steps // 4), args.warmup, world, device,
+                               args.eager, layout=1)
+            workloads[c.name]["repacked_layout"] = {"dmmv_gbs": rp["dmmv_gbs"], "dmmv_us": rp["dmmv_us"],
+                                                    "pct_of_peak": 100 * rp["dmmv_gbs"] / hbm_peak}
         workloads["moe_experts_top8_plus_shared"] = measure_moe(max(5, args.steps // 4), args.warmup, world,
                                                                 device, args.eager, l2)
 

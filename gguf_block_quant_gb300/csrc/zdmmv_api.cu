@@ -73,6 +73,26 @@ int ctas_per_sm_per_launch(int64_t weight_bytes) {
     return weight_bytes >= kLargeLaunchBytes ? kCtasPerSmLarge : kCtasPerSmSmall;
 }
 
+// Batched calls stream the weights once (dmmv_batch_kernel) unless
+// ZDMMV_BATCH_SLOTS=1, which runs one single-vector slot per vector instead.
+int batch_slots_forced() {
+    static const int v = [] {
+        const char *e = std::getenv("ZDMMV_BATCH_SLOTS");
+        return (e && e[0] == '1') ? 1 : 0;
+    }();
+    return v;
+}
+
+// CTAs per SM of a batched launch (environment ZDMMV_BATCH_CTAS_PER_SM, 1..4; default 2)
+int batch_ctas_per_sm() {
+    static const int v = [] {
+        const char *e = std::getenv("ZDMMV_BATCH_CTAS_PER_SM");
+        const int n = e ? std::atoi(e) : 0;
+        return (n >= 1 && n <= 4) ? n : 3;
+    }();
+    return v;
+}
+
 inline bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 inline int block_bytes(int fmt) { return fmt == kFmtQ8 ? 34 : (fmt == kFmtQ4 ? 18 : 0); }
 inline int64_t round_up(int64_t v, int64_t m) { return (v + m - 1) / m * m; }
@@ -135,6 +155,47 @@ TmaPlan tma_plan(int fmt, int layout, int64_t cols) {
         --p.stages;
     p.smem_bytes = kBarrierBytes + p.x_bytes_padded + p.stages * p.stage_bytes;
     return p;
+}
+
+bool batch_plan(int fmt, int64_t cols, int batch, BatchPlan *out) {
+    if (!tma_shape_ok(fmt, cols) || batch < 2 || batch > ZDMMV_MAX_BATCH) return false;
+    const int nb = static_cast<int>(cols / kQK);
+    BatchPlan p{};
+    if (nb % 128 == 0 && nb / 128 <= 2) {
+        p.g = 128; p.bpt = nb / 128;
+    } else if (nb == 64) {
+        p.g = 64; p.bpt = 1;
+    } else if (nb % 32 == 0 && nb / 32 <= 4) {
+        p.g = 32; p.bpt = nb / 32;
+    } else {
+        return false;  // other widths take the per-vector slots of the single-vector kernel
+    }
+    // vectors held in registers per pass: all of them with one block per thread
+    if (p.bpt == 1)
+        p.vb = batch <= 2 ? 2 : (batch <= 4 ? 4 : 8);
+    else
+        p.vb = p.bpt == 2 ? 2 : 1;
+    const int groups = kConsumerThreads / p.g;
+    const int row_bytes = nb * block_bytes(fmt);
+    const int unit_rows = groups * 2;  // two rows per group per iteration
+    const int stage_target = stage_target_bytes();
+    const int unit = unit_rows * row_bytes;
+    const int m = unit >= stage_target ? 1 : stage_target / unit;
+    p.tile_rows = unit_rows * m;
+    p.stage_bytes = static_cast<int>(round_up(static_cast<int64_t>(p.tile_rows) * row_bytes, 128));
+    p.x_bytes_padded = 0;  // each thread loads its activation blocks straight into registers
+    // per-tile partial sums: [passes][iterations][groups][warps per group][2*vb] floats
+    const int npass = (batch + p.vb - 1) / p.vb;
+    const int iters = (p.tile_rows + unit_rows - 1) / unit_rows;
+    const int red_bytes = npass * iters * (kConsumerThreads / 32) * 2 * p.vb * 4;
+    p.stages = 4;
+    while (p.stages > 2 &&
+           kBarrierBytes + p.x_bytes_padded + p.stages * p.stage_bytes + red_bytes > kSmemPerCtaTarget)
+        --p.stages;
+    p.smem_bytes = kBarrierBytes + p.x_bytes_padded + p.stages * p.stage_bytes + red_bytes;
+    if (p.smem_bytes > 200 * 1024) return false;
+    *out = p;
+    return true;
 }
 
 // ------------------------------------------------------------- kernels
@@ -436,6 +497,23 @@ zdmmv_status dmmv_entry(int fmt, const void *w, zdmmv_layout layout, int64_t row
     a.nb = static_cast<int32_t>(cols / kQK);
     const int64_t cols_pad = cols;
     (void)cols_pad;
+    BatchPlan bp{};
+    if (batch >= 2 && batch_slots_forced() == 0 && batch_plan(fmt, cols, batch, &bp)) {
+        // one weight stream for all vectors
+        const DeviceInfo *dev = nullptr;
+        if (device_info(&dev) != cudaSuccess) return ZDMMV_ERR_CUDA;
+        a.fault = dev->fault;
+        a.batch = batch;
+        a.y_stride = rows;
+        a.tile_rows = bp.tile_rows;
+        a.stage_bytes = bp.stage_bytes;
+        a.x_bytes_padded = bp.x_bytes_padded;
+        int64_t ctas = static_cast<int64_t>(dev->sms) * batch_ctas_per_sm();
+        if (ctas > rows) ctas = rows;
+        cudaError_t e = fmt == kFmtQ8 ? launch_batch_q8(a, bp, layout, static_cast<int>(ctas), st, pdl_enabled())
+                                      : launch_batch_q4(a, bp, layout, static_cast<int>(ctas), st, pdl_enabled());
+        return from_cuda(e);
+    }
     if (tma_shape_ok(fmt, cols)) {
         // batch vectors as slots of the pipelined kernel: slot v reads
         // activation v and writes output row block v

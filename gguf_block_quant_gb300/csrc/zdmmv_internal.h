@@ -66,6 +66,15 @@ cudaError_t launch_tma_q8(const DmmvArgs &a, const TmaPlan &p, int layout, bool 
                           int slots, cudaStream_t st, bool pdl);
 cudaError_t launch_tma_q4(const DmmvArgs &a, const TmaPlan &p, int layout, bool fused_x, int ctas_per_slot,
                           int slots, cudaStream_t st, bool pdl);
+// Batched kernel (one weight stream, 2..8 vectors): the plan and launchers.
+struct BatchPlan {
+    int g, bpt, vb;   // threads per row, blocks per thread, vectors per pass
+    int stages, tile_rows, stage_bytes, x_bytes_padded, smem_bytes;
+};
+bool batch_plan(int fmt, int64_t cols, int batch, BatchPlan *out);
+cudaError_t launch_batch_q8(const DmmvArgs &a, const BatchPlan &p, int layout, int ctas, cudaStream_t st, bool pdl);
+cudaError_t launch_batch_q4(const DmmvArgs &a, const BatchPlan &p, int layout, int ctas, cudaStream_t st, bool pdl);
+
 // CTAs of the pipelined kernel that fit on one SM for this plan.
 int tma_ctas_per_sm_q8(int layout, const TmaPlan &p);
 int tma_ctas_per_sm_q4(int layout, const TmaPlan &p);

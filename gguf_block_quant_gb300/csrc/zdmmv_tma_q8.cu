@@ -1,4 +1,5 @@
 // zdmmv_tma_q8.cu -- instantiations of the TMA-pipelined DMMV kernel for Q8_0 weights.
+#include "zdmmv_batch.cuh"
 #include "zdmmv_tma.cuh"
 
 namespace zdmmv {
@@ -9,5 +10,10 @@ cudaError_t launch_tma_q8(const DmmvArgs &a, const TmaPlan &p, int layout, bool 
 }
 
 int tma_ctas_per_sm_q8(int layout, const TmaPlan &p) { return tma_ctas_per_sm_fmt<kFmtQ8>(layout, p); }
+
+cudaError_t launch_batch_q8(const DmmvArgs &a, const BatchPlan &p, int layout, int ctas, cudaStream_t st,
+                            bool pdl) {
+    return launch_batch_fmt<kFmtQ8>(a, layout, p.g, p.bpt, p.vb, p.stages, p.smem_bytes, ctas, st, pdl);
+}
 
 }  // namespace zdmmv

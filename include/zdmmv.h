@@ -124,10 +124,14 @@ zdmmv_status zdmmv_q4_0(const void *w, zdmmv_layout layout, int64_t rows, int64_
                         const void *xq, float *y, zdmmv_stream_t stream);
 
 /* The same weight matrix against `batch` (1..8) activation vectors in one call:
- * xq is [batch][cols/32] Q8_0 blocks, y is [batch][rows] fp32. The weight
- * stream is read from HBM once per call (concurrency headroom of decode slots:
- * habr article, section "RDNA4: что мы узнали о железе"). batch == 1 is the
- * same computation as zdmmv_q8_0 / zdmmv_q4_0, bit for bit.
+ * xq is [batch][cols/32] Q8_0 blocks, y is [batch][rows] fp32. For widths of
+ * 256 * {1,2,3,4}, 2048, 4096 and 8192 columns each weight tile is streamed from
+ * HBM once and dotted against every vector (concurrency headroom of decode
+ * slots: habr article, section "RDNA4: что мы узнали о железе"); other widths
+ * run the single-vector computation once per vector. batch == 1 is the same
+ * computation as zdmmv_q8_0 / zdmmv_q4_0, bit for bit; batch > 1 results are
+ * deterministic and within the stated tolerance (their fp32 reduction order
+ * differs from the single-vector kernel's).
  * Errors: as zdmmv_q8_0, plus ERR_SHAPE for batch outside 1..8. */
 zdmmv_status zdmmv_q8_0_batched(const void *w, zdmmv_layout layout, int64_t rows,
                                 int64_t cols, const void *xq, int batch, float *y,
@@ -136,8 +140,8 @@ zdmmv_status zdmmv_q4_0_batched(const void *w, zdmmv_layout layout, int64_t rows
                                 int64_t cols, const void *xq, int batch, float *y,
                                 zdmmv_stream_t stream);
 
-/* Fused decode step: the same result as zdmmv_quantize_act_q8_0 followed by
- * zdmmv_q{8,4}_0(_batched), bit for bit, in ONE launch. Each CTA quantizes the
+/* Fused decode step: for each of the batch vectors the same result as
+ * zdmmv_quantize_act_q8_0 followed by zdmmv_q{8,4}_0, bit for bit, in ONE launch. Each CTA quantizes the
  * fp32 activation to Q8_0 blocks in shared memory itself, so a chain of decode
  * layers pays one kernel per layer instead of two (per-token launch chains:
  * "RTX 5090: Batched Prefill & CUDA Graphs in ZINC", "CUDA graphs -- the

@@ -214,8 +214,9 @@ def test_repack_bit_exact(fmt, rows, cols):
 
 # ----------------------------------------------------------------- batched
 @pytest.mark.parametrize("layout", [Z.GGUF, Z.REPACKED])
-@pytest.mark.parametrize("fmt,rows,cols", [(Q8_0, 1434, 4096), (Q4_0, 901, 2048), (Q8_0, 99, 160)])
-@pytest.mark.parametrize("batch", [1, 2, 4, 8])
+@pytest.mark.parametrize("fmt,rows,cols", [(Q8_0, 1434, 4096), (Q4_0, 901, 2048), (Q8_0, 99, 160),
+                                           (Q4_0, 300, 8192), (Q8_0, 257, 3072), (Q8_0, 77, 512)])
+@pytest.mark.parametrize("batch", [1, 2, 3, 4, 7, 8])
 def test_batched_matches_oracle_and_single_calls(fmt, rows, cols, batch, layout):
     w = synth.weight_blocks(fmt, rows, cols, seed=batch)
     x = synth.activations(cols, seed=10 + batch, batch=batch)
@@ -229,13 +230,37 @@ def test_batched_matches_oracle_and_single_calls(fmt, rows, cols, batch, layout)
     xq_ref = oracle.quantize_q8_0(x)
     y_ref, e_ref = oracle.dmmv_batched(fmt, w, rows, cols, xq_ref, batch)
     check_y(y, y_ref, e_ref)
-    nbx = cols // 32 * 34
-    for v in range(batch):
+    # deterministic: the same call again gives the same bits
+    y2 = nan_out(batch, rows)
+    Z.dmmv_batched(fmt, wd, rows, cols, xq, batch, y=y2, layout=layout)
+    torch.cuda.synchronize()
+    assert torch.equal(y, y2)
+    if batch == 1:
+        # batch 1 is the single-vector computation, bit for bit
         ys = nan_out(rows)
-        # a separate (16-byte aligned) copy of vector v's blocks
-        Z.dmmv(fmt, wd, rows, cols, xq[v * nbx:(v + 1) * nbx].clone(), y=ys, layout=layout)
+        Z.dmmv(fmt, wd, rows, cols, xq, y=ys, layout=layout)
         torch.cuda.synchronize()
-        assert torch.equal(ys, y[v]), "batched result differs from the single-vector call"
+        assert torch.equal(ys, y[0])
+
+
+@pytest.mark.parametrize("fmt,rows,cols", [(Q8_0, 333, 4096), (Q4_0, 517, 2048), (Q8_0, 130, 1024),
+                                           (Q4_0, 41, 8192), (Q8_0, 65, 3072), (Q4_0, 23, 96)])
+@pytest.mark.parametrize("batch", [2, 3, 5, 8])
+def test_batched_exact_integer_outputs_equal_oracle_bitwise(fmt, rows, cols, batch):
+    """Unit scales and small codes: every fp32 partial sum is an exact integer,
+    so each batched output equals the oracle's exactly (pins the batched
+    kernel's integer block sums)."""
+    w = synth.weight_blocks_small(fmt, rows, cols, seed=rows + batch, qmax=7)
+    xq = synth.activation_blocks(batch * cols // 32, seed=cols + batch, qmax=15, fixed_scale=1.0)
+    for layout in (Z.GGUF, Z.REPACKED):
+        wd = dev(w)
+        if layout == Z.REPACKED:
+            wd = Z.repack(fmt, wd, rows, cols)
+        y = nan_out(batch, rows)
+        Z.dmmv_batched(fmt, wd, rows, cols, dev(xq), batch, y=y, layout=layout)
+        torch.cuda.synchronize()
+        y_ref, _ = oracle.dmmv_batched(fmt, w, rows, cols, xq, batch)
+        assert np.array_equal(y.double().cpu().numpy(), y_ref)
 
 
 # ------------------------------------------------------------ expert gather
@@ -320,8 +345,11 @@ def test_fused_f32_equals_quantize_then_dmmv_bitwise(fmt, rows, cols, batch, lay
     yf = nan_out(batch, rows)
     Z.dmmv_f32(fmt, wd, rows, cols, xd, batch=batch, y=yf, layout=layout)
     xq = Z.quantize_act_q8_0(xd)
+    nbx = cols // 32 * 34
     yu = nan_out(batch, rows)
-    Z.dmmv_batched(fmt, wd, rows, cols, xq, batch, y=yu, layout=layout)
+    for v in range(batch):
+        # each vector through the two-kernel path (a 16-byte aligned copy of its blocks)
+        Z.dmmv(fmt, wd, rows, cols, xq[v * nbx:(v + 1) * nbx].clone(), y=yu[v], layout=layout)
     torch.cuda.synchronize()
     assert torch.equal(yf, yu), "fused and two-kernel results differ"
     y_ref, e_ref = oracle.dmmv_batched(fmt, w, rows, cols, oracle.quantize_q8_0(x), batch)
