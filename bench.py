@@ -337,7 +337,7 @@ def measure_moe(steps, warmup, world, device, eager, l2_bytes):
     gu, dn = m.gate_up_bytes(), m.down_bytes()
     layers = 16
 
-    def step():
+    def step3():
         for l in range(layers):
             g, u, d = stacks[l % n_sets]
             idx = idxs[l % len(idxs)]
@@ -346,14 +346,25 @@ def measure_moe(steps, warmup, world, device, eager, l2_bytes):
             Z.expert_gather(Z.Q8_0, d, dn, m.hidden, m.ffn, idx, m.n_slots, xqd, (m.ffn // 32) * 34, y=yd,
                             status=st)
 
-    run = graph_or_eager(step, eager)
-    ms, _ = time_fn(run, steps, warmup, world, device)
-    per_layer = ms / 1e3 / (steps * layers)
+    def step2():
+        for l in range(layers):
+            g, u, d = stacks[l % n_sets]
+            idx = idxs[l % len(idxs)]
+            Z.expert_gather2(Z.Q4_0, g, u, gu, m.ffn, m.hidden, idx, m.n_slots, xq, 0, y_a=yg, y_b=yu, status=st)
+            Z.expert_gather(Z.Q8_0, d, dn, m.hidden, m.ffn, idx, m.n_slots, xqd, (m.ffn // 32) * 34, y=yd,
+                            status=st)
+
     nbytes = m.algorithmic_bytes()
-    return {"layers": layers, "us_per_token_layer": per_layer * 1e6, "gbs": nbytes / per_layer / 1e9,
-            "rows_per_s": m.n_sel * (2 * m.ffn + m.hidden) / per_layer, "algorithmic_bytes": nbytes,
-            "launches_per_layer": 3,
-            "note": "touched experts differ per layer; stack copies alternate (some L2 reuse possible)"}
+    out = {"layers": layers, "algorithmic_bytes": nbytes,
+           "note": "touched experts differ per layer; stack copies alternate (some L2 reuse possible)"}
+    for name, fn, launches in (("three_launch", step3, 3), ("gate_up_fused", step2, 2)):
+        run = graph_or_eager(fn, eager)
+        ms, _ = time_fn(run, steps, warmup, world, device)
+        per_layer = ms / 1e3 / (steps * layers)
+        out[name] = {"us_per_token_layer": per_layer * 1e6, "gbs": nbytes / per_layer / 1e9,
+                     "rows_per_s": m.n_sel * (2 * m.ffn + m.hidden) / per_layer, "launches_per_layer": launches}
+    out["gbs"] = max(out["three_launch"]["gbs"], out["gate_up_fused"]["gbs"])
+    return out
 
 
 def e2e_dense(cfg, layers, steps, warmup, world, device, eager=False):

@@ -255,10 +255,12 @@ __global__ void __launch_bounds__(256) dmmv_plain_kernel(const DmmvArgs a) {
     const int64_t row = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
     const int slot = blockIdx.y;
     if (row >= a.rows) return;
-    float *y = a.y + slot * a.y_stride;
-    const uint8_t *w = a.w;
+    const bool second = a.w_b != nullptr && slot >= a.slots_a;
+    const int sel = second ? slot - a.slots_a : slot;
+    float *y = (second ? a.y_b : a.y) + sel * a.y_stride;
+    const uint8_t *w = second ? a.w_b : a.w;
     if (a.idx != nullptr) {
-        const int e = a.idx[slot];
+        const int e = a.idx[sel];
         if (e < 0 || e >= a.n_experts) {
             if (lane == 0) {
                 y[row] = __int_as_float(0x7fc00000);
@@ -269,7 +271,7 @@ __global__ void __launch_bounds__(256) dmmv_plain_kernel(const DmmvArgs a) {
         w += static_cast<int64_t>(e) * a.expert_stride;
     }
     const int nb = a.nb;
-    const uint8_t *xq0 = a.xq + slot * a.xq_stride;
+    const uint8_t *xq0 = a.xq + sel * a.xq_stride;
     for (int v = 0; v < a.batch; ++v) {
         const uint8_t *xq = xq0 + static_cast<int64_t>(v) * nb * 34;
         float acc = 0.0f;
@@ -526,6 +528,42 @@ zdmmv_status dmmv_entry(int fmt, const void *w, zdmmv_layout layout, int64_t row
     return run_dmmv(fmt, layout, a, 1, st);
 }
 
+zdmmv_status gather_entry(int fmt, const void *w_stack, const void *w_stack_b, int64_t expert_stride_bytes,
+                          int layout, int64_t rows, int64_t cols, const int32_t *idx, int n, int n_experts,
+                          const void *xq, int64_t xq_stride_bytes, float *y, float *y_b, int32_t *status_dev,
+                          cudaStream_t st) {
+    zdmmv_status s = check_matrix(fmt, w_stack, layout, rows, cols, xq, y);
+    if (s != ZDMMV_OK) return s;
+    if (n < 0 || n > 32767 || n_experts < 0) return ZDMMV_ERR_SHAPE;
+    if (n == 0 || rows == 0) return ZDMMV_OK;
+    if (!idx) return ZDMMV_ERR_NULL;
+    if (!aligned(idx, 4) || (status_dev && !aligned(status_dev, 4))) return ZDMMV_ERR_ALIGN;
+    if (w_stack_b && (!aligned(w_stack_b, 16) || !aligned(y_b, 4))) return ZDMMV_ERR_ALIGN;
+    const int64_t nb = cols / kQK;
+    const int64_t mat_bytes = rows * nb * block_bytes(fmt);
+    if (expert_stride_bytes < 0 || xq_stride_bytes < 0) return ZDMMV_ERR_SHAPE;
+    if (n_experts > 1 && expert_stride_bytes < mat_bytes) return ZDMMV_ERR_SHAPE;
+    if (xq_stride_bytes != 0 && xq_stride_bytes < nb * 34) return ZDMMV_ERR_SHAPE;
+    if (expert_stride_bytes % 16 || xq_stride_bytes % 16) return ZDMMV_ERR_ALIGN;
+    DmmvArgs a{};
+    a.w = static_cast<const uint8_t *>(w_stack);
+    a.w_b = static_cast<const uint8_t *>(w_stack_b);
+    a.y_b = y_b;
+    a.slots_a = n;
+    a.expert_stride = expert_stride_bytes;
+    a.idx = idx;
+    a.n_experts = n_experts;
+    a.status = status_dev;
+    a.xq = static_cast<const uint8_t *>(xq);
+    a.xq_stride = xq_stride_bytes;
+    a.y = y;
+    a.y_stride = rows;
+    a.rows = rows;
+    a.nb = static_cast<int32_t>(nb);
+    a.batch = 1;
+    return run_dmmv(fmt, layout, a, w_stack_b ? 2 * n : n, st);
+}
+
 zdmmv_status dmmv_f32_entry(int fmt, const void *w, int layout, int64_t rows, int64_t cols, const float *x,
                             int batch, float *y, cudaStream_t st) {
     if (block_bytes(fmt) == 0) return ZDMMV_ERR_FORMAT;
@@ -623,32 +661,18 @@ zdmmv_status zdmmv_expert_gather(zdmmv_fmt fmt, const void *w_stack, int64_t exp
                                  zdmmv_layout layout, int64_t rows, int64_t cols, const int32_t *idx, int n,
                                  int n_experts, const void *xq, int64_t xq_stride_bytes, float *y,
                                  int32_t *status_dev, zdmmv_stream_t stream) {
-    zdmmv_status s = check_matrix(fmt, w_stack, layout, rows, cols, xq, y);
-    if (s != ZDMMV_OK) return s;
-    if (n < 0 || n > 65535 || n_experts < 0) return ZDMMV_ERR_SHAPE;
-    if (n == 0 || rows == 0) return ZDMMV_OK;
-    if (!idx) return ZDMMV_ERR_NULL;
-    if (!aligned(idx, 4) || (status_dev && !aligned(status_dev, 4))) return ZDMMV_ERR_ALIGN;
-    const int64_t nb = cols / kQK;
-    const int64_t mat_bytes = rows * nb * block_bytes(fmt);
-    if (expert_stride_bytes < 0 || xq_stride_bytes < 0) return ZDMMV_ERR_SHAPE;
-    if (n_experts > 1 && expert_stride_bytes < mat_bytes) return ZDMMV_ERR_SHAPE;
-    if (xq_stride_bytes != 0 && xq_stride_bytes < nb * 34) return ZDMMV_ERR_SHAPE;
-    if (expert_stride_bytes % 16 || xq_stride_bytes % 16) return ZDMMV_ERR_ALIGN;
-    DmmvArgs a{};
-    a.w = static_cast<const uint8_t *>(w_stack);
-    a.expert_stride = expert_stride_bytes;
-    a.idx = idx;
-    a.n_experts = n_experts;
-    a.status = status_dev;
-    a.xq = static_cast<const uint8_t *>(xq);
-    a.xq_stride = xq_stride_bytes;
-    a.y = y;
-    a.y_stride = rows;
-    a.rows = rows;
-    a.nb = static_cast<int32_t>(nb);
-    a.batch = 1;
-    return run_dmmv(fmt, layout, a, n, reinterpret_cast<cudaStream_t>(stream));
+    return gather_entry(fmt, w_stack, nullptr, expert_stride_bytes, layout, rows, cols, idx, n, n_experts, xq,
+                        xq_stride_bytes, y, nullptr, status_dev, reinterpret_cast<cudaStream_t>(stream));
+}
+
+zdmmv_status zdmmv_expert_gather2(zdmmv_fmt fmt, const void *w_stack_a, const void *w_stack_b,
+                                  int64_t expert_stride_bytes, zdmmv_layout layout, int64_t rows, int64_t cols,
+                                  const int32_t *idx, int n, int n_experts, const void *xq,
+                                  int64_t xq_stride_bytes, float *y_a, float *y_b, int32_t *status_dev,
+                                  zdmmv_stream_t stream) {
+    if (!w_stack_b || !y_b) return n == 0 || rows == 0 ? ZDMMV_OK : ZDMMV_ERR_NULL;
+    return gather_entry(fmt, w_stack_a, w_stack_b, expert_stride_bytes, layout, rows, cols, idx, n, n_experts, xq,
+                        xq_stride_bytes, y_a, y_b, status_dev, reinterpret_cast<cudaStream_t>(stream));
 }
 
 zdmmv_status zdmmv_dmmv_f32(zdmmv_fmt fmt, const void *w, zdmmv_layout layout, int64_t rows, int64_t cols,

@@ -12,6 +12,9 @@ namespace zdmmv {
 // idx is set), activation xq + k*xq_stride and writes y + k*y_stride.
 struct DmmvArgs {
     const uint8_t *w;        // matrix base (GGUF blocks, or repacked quant stream + scales)
+    const uint8_t *w_b;      // second stack (slots >= slots_a use it, with y_b), or nullptr
+    float *y_b;              // output of the second stack's slot slots_a
+    int32_t slots_a;         // slots of the first stack (when w_b is set)
     int64_t expert_stride;   // bytes between stacked matrices (gather)
     const int32_t *idx;      // device expert index per slot, or nullptr
     int32_t n_experts;       // valid index range [0, n_experts)

@@ -133,11 +133,15 @@ __global__ void __launch_bounds__(kTmaThreads, MINB) dmmv_tma_kernel(const DmmvA
     // what they do before their own dependency wait is stream weights only.
     pdl_launch_dependents();
 
-    float *y = a.y + slot * a.y_stride;
-    const uint8_t *w = a.w;
+    // a second stack (e.g. the up projections next to the gates) takes the slots
+    // from slots_a on, with the same selected experts and activations
+    const bool second = a.w_b != nullptr && slot >= a.slots_a;
+    const int sel = second ? slot - a.slots_a : slot;
+    float *y = (second ? a.y_b : a.y) + sel * a.y_stride;
+    const uint8_t *w = second ? a.w_b : a.w;
     if (a.idx != nullptr) {
         pdl_wait();  // the index list may be written by the preceding kernel
-        const int e = a.idx[slot];
+        const int e = a.idx[sel];
         if (e < 0 || e >= a.n_experts) {
             for (int64_t r = r0 + tid; r < r1; r += blockDim.x) y[r] = __int_as_float(0x7fc00000);
             if (tid == 0 && a.status != nullptr) atomicExch(a.status, 1);
@@ -173,7 +177,7 @@ __global__ void __launch_bounds__(kTmaThreads, MINB) dmmv_tma_kernel(const DmmvA
         if constexpr (!FX) {
             const uint32_t xbytes = static_cast<uint32_t>(nb) * 34u;
             mbar_arrive_expect_tx(xbar, xbytes);
-            bulk_copy_g2s(xs, a.xq + slot * a.xq_stride, xbytes, xbar, l2_evict_last_policy());
+            bulk_copy_g2s(xs, a.xq + sel * a.xq_stride, xbytes, xbar, l2_evict_last_policy());
         }
         bool ok = true;
         for (int t = npre; t < ntiles; ++t) {
@@ -205,7 +209,7 @@ __global__ void __launch_bounds__(kTmaThreads, MINB) dmmv_tma_kernel(const DmmvA
     if constexpr (FX) {
         // quantize the fp32 activation into Q8_0 blocks in shared memory: each
         // warp takes four blocks per iteration (16-byte loads, 8 lanes per block)
-        const float *xf = a.xf + slot * a.xf_stride;
+        const float *xf = a.xf + sel * a.xf_stride;
         constexpr int kWarps = kConsumerThreads / 32;
         constexpr int kRound = 8;
         const int warp = tid >> 5;

@@ -56,6 +56,8 @@ _SIGS = {
     "zdmmv_dmmv_f32": ([_int, _vp, _int, _i64, _i64, _vp, _int, _vp, _vp], _int),
     "zdmmv_expert_gather": ([_int, _vp, _i64, _int, _i64, _i64, _vp, _int, _int, _vp, _i64, _vp, _vp, _vp],
                             _int),
+    "zdmmv_expert_gather2": ([_int, _vp, _vp, _i64, _int, _i64, _i64, _vp, _int, _int, _vp, _i64, _vp, _vp,
+                              _vp, _vp], _int),
     "zdmmv_repacked_bytes": ([_int, _i64, _i64], ctypes.c_size_t),
     "zdmmv_repack": ([_int, _vp, _i64, _i64, _vp, ctypes.c_size_t, _vp], _int),
     "zdmmv_host_step_workspace_bytes": ([_i64, _i64, _int], ctypes.c_size_t),
@@ -195,6 +197,20 @@ def expert_gather(fmt: int, w_stack, expert_stride: int, rows: int, cols: int, i
     _call("zdmmv_expert_gather", fmt, _ptr(w_stack), expert_stride, layout, rows, cols, _ptr(idx), n,
           n_experts, _ptr(xq), xq_stride, _ptr(y), _ptr(status), _stream(stream))
     return y
+
+
+def expert_gather2(fmt: int, w_stack_a, w_stack_b, expert_stride: int, rows: int, cols: int, idx,
+                   n_experts: int, xq, xq_stride: int, y_a=None, y_b=None, status=None, layout: int = GGUF,
+                   stream=None):
+    """Two same-shaped expert stacks (e.g. gate and up) in one launch."""
+    n = idx.numel()
+    if idx.dtype != torch.int32:
+        raise ValueError("expert_gather2: idx must be int32")
+    y_a = _out(y_a, (n, rows), w_stack_a.device)
+    y_b = _out(y_b, (n, rows), w_stack_a.device)
+    _call("zdmmv_expert_gather2", fmt, _ptr(w_stack_a), _ptr(w_stack_b), expert_stride, layout, rows, cols,
+          _ptr(idx), n, n_experts, _ptr(xq), xq_stride, _ptr(y_a), _ptr(y_b), _ptr(status), _stream(stream))
+    return y_a, y_b
 
 
 def repacked_bytes(fmt: int, rows: int, cols: int) -> int:

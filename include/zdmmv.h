@@ -165,7 +165,7 @@ zdmmv_status zdmmv_dmmv_f32(zdmmv_fmt fmt, const void *w, zdmmv_layout layout, i
  *   w_stack             device; expert e starts at w_stack + e*expert_stride_bytes
  *                       (16-byte multiple), each a [rows x cols] matrix in `layout`.
  *   idx                 DEVICE int32[n], read by the kernel (no host round-trip).
- *   n                   number of selected experts (>= 0; 0 is a no-op).
+ *   n                   number of selected experts (0..32767; 0 is a no-op).
  *   n_experts           valid indices are 0 .. n_experts-1.
  *   xq                  device Q8_0 blocks; slot k reads xq + k*xq_stride_bytes
  *                       (xq_stride_bytes = 0: one activation shared by all slots;
@@ -181,6 +181,21 @@ zdmmv_status zdmmv_expert_gather(zdmmv_fmt fmt, const void *w_stack,
                                  int64_t rows, int64_t cols, const int32_t *idx, int n,
                                  int n_experts, const void *xq, int64_t xq_stride_bytes,
                                  float *y, int32_t *status_dev, zdmmv_stream_t stream);
+
+/* Two expert stacks of the same shape and format against the same selected
+ * experts and activations, in ONE launch: y_a[k] = A_{idx[k]} . x_k and
+ * y_b[k] = B_{idx[k]} . x_k (the gate and up projections of the routed experts,
+ * which the pages plan as one fused launch: "CUDA backend for ZINC", M3
+ * "dmmv_*_fused_gate_up*"; same-input matvec pairs fused: "RTX 5090: Batched
+ * Prefill & CUDA Graphs in ZINC", "Gemma fusion"). Arguments as
+ * zdmmv_expert_gather, with the two stacks sharing expert_stride_bytes; y_a and
+ * y_b are [n][rows]. Each output equals zdmmv_expert_gather on its own stack,
+ * bit for bit. Errors: as zdmmv_expert_gather. */
+zdmmv_status zdmmv_expert_gather2(zdmmv_fmt fmt, const void *w_stack_a, const void *w_stack_b,
+                                  int64_t expert_stride_bytes, zdmmv_layout layout, int64_t rows,
+                                  int64_t cols, const int32_t *idx, int n, int n_experts,
+                                  const void *xq, int64_t xq_stride_bytes, float *y_a, float *y_b,
+                                  int32_t *status_dev, zdmmv_stream_t stream);
 
 /* Bytes of the repacked form of a [rows x cols] matrix (equal to the GGUF size);
  * 0 for an unknown format or a bad shape. */

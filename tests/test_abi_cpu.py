@@ -90,3 +90,8 @@ def test_other_argument_checks(L):
     assert f(8, FAKE, 0, 4, 64, FAKE + 4, 1, FAKE, None) == 3
     assert f(8, FAKE + 8, 0, 4, 64, FAKE, 1, FAKE, None) == 3
     assert L.zdmmv_debug_block_sums(8, FAKE, 0, 4, 40, FAKE, FAKE, None) == 2
+    g2 = L.zdmmv_expert_gather2
+    assert g2(2, FAKE, None, 1 << 16, 0, 4, 64, FAKE, 2, 8, FAKE, 0, FAKE, FAKE, None, None) == 1
+    assert g2(2, FAKE, FAKE, 1 << 16, 0, 4, 64, FAKE, 2, 8, FAKE, 0, FAKE, None, None, None) == 1
+    assert g2(2, FAKE, FAKE + 8, 1 << 16, 0, 4, 64, FAKE, 2, 8, FAKE, 0, FAKE, FAKE, None, None) == 3
+    assert g2(2, FAKE, FAKE, 1 << 16, 0, 4, 64, FAKE, 0, 8, FAKE, 0, FAKE, FAKE, None, None) == 0

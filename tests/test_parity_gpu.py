@@ -385,3 +385,33 @@ def test_fused_f32_chain_with_reused_buffers():
             ok, worst = oracle.within_tolerance(yk, y_ref, e_ref)
             assert ok, worst
             cur = yk
+
+
+@pytest.mark.parametrize("layout", [Z.GGUF, Z.REPACKED])
+@pytest.mark.parametrize("fmt,rows,cols", [(Q4_0, 512, 2048), (Q8_0, 300, 512), (Q4_0, 40, 96)])
+def test_expert_gather2_equals_two_gathers_bitwise(fmt, rows, cols, layout):
+    n_exp = 6
+    bb = 18 if fmt == Q4_0 else 34
+    per = rows * cols // 32 * bb
+    sa = synth.weight_blocks(fmt, n_exp * rows, cols, seed=41)
+    sb = synth.weight_blocks(fmt, n_exp * rows, cols, seed=42, stream=synth.S_WEIGHT2)
+    idx = np.array([5, 1, 3, 3, 0, 7], dtype=np.int32)   # 7 is out of range
+    xq = synth.activation_blocks(cols // 32, seed=43)
+    da, db = dev(sa), dev(sb)
+    if layout == Z.REPACKED:
+        da = torch.cat([Z.repack(fmt, da[e * per:(e + 1) * per], rows, cols) for e in range(n_exp)])
+        db = torch.cat([Z.repack(fmt, db[e * per:(e + 1) * per], rows, cols) for e in range(n_exp)])
+    ia = dev(idx)
+    st2 = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ya, yb = Z.expert_gather2(fmt, da, db, per, rows, cols, ia, n_exp, dev(xq), 0, status=st2, layout=layout)
+    ref_a = nan_out(len(idx), rows)
+    ref_b = nan_out(len(idx), rows)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    Z.expert_gather(fmt, da, per, rows, cols, ia, n_exp, dev(xq), 0, y=ref_a, status=st, layout=layout)
+    Z.expert_gather(fmt, db, per, rows, cols, ia, n_exp, dev(xq), 0, y=ref_b, status=st, layout=layout)
+    torch.cuda.synchronize()
+    assert st2.item() == 1 and st.item() == 1
+    assert torch.equal(ya[:5], ref_a[:5]) and torch.equal(yb[:5], ref_b[:5])
+    assert torch.isnan(ya[5]).all() and torch.isnan(yb[5]).all()
+    y_ref, e_ref, _ = oracle.expert_gather(fmt, sb, per, rows, cols, idx, n_exp, xq, 0)
+    check_y(yb[:5], y_ref[:5], e_ref[:5])
