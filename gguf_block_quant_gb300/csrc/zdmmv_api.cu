@@ -236,6 +236,23 @@ __global__ void __launch_bounds__(256) repack_kernel(const uint8_t *__restrict__
     reinterpret_cast<uint16_t *>(dst + nblocks * kQB)[i] = h[0];
 }
 
+// Failure-path self-test: one warp waits on an mbarrier that nothing ever
+// completes. The bounded wait gives up, the fault bit is recorded and
+// result[0] = 1; the kernel then returns normally.
+__global__ void selftest_wait_timeout_kernel(uint32_t *fault, int32_t *result) {
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);  // expects one arrival that never comes
+        fence_barrier_init();
+    }
+    __syncwarp();
+    const bool done = __all_sync(0xffffffffu, mbar_wait(&bar, 0));
+    if (threadIdx.x == 0) {
+        if (!done) atomicOr(fault, ZDMMV_FAULT_WAIT_TIMEOUT);
+        result[0] = done ? 0 : 1;
+    }
+}
+
 __global__ void selftest_dp4a_kernel(const int32_t *a, const int32_t *b, const int32_t *c, int32_t *out, int n) {
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
     if (i < n) out[i] = dp4a_ss(static_cast<uint32_t>(a[i]), static_cast<uint32_t>(b[i]), c[i]);
@@ -782,6 +799,14 @@ zdmmv_status zdmmv_selftest_dp4a(const int32_t *a, const int32_t *b, const int32
     if (n == 0) return ZDMMV_OK;
     if (!a || !b || !c || !out) return ZDMMV_ERR_NULL;
     selftest_dp4a_kernel<<<(n + 255) / 256, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(a, b, c, out, n);
+    return from_cuda(cudaGetLastError());
+}
+
+zdmmv_status zdmmv_selftest_wait_timeout(int32_t *result, zdmmv_stream_t stream) {
+    if (!result) return ZDMMV_ERR_NULL;
+    const DeviceInfo *dev = nullptr;
+    if (device_info(&dev) != cudaSuccess) return ZDMMV_ERR_CUDA;
+    selftest_wait_timeout_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(dev->fault, result);
     return from_cuda(cudaGetLastError());
 }
 

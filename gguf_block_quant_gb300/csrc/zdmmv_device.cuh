@@ -90,15 +90,17 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
     return t;
 }
 
-// Every wait in this library is bounded: after this long the waiter gives up,
-// the kernel records ZDMMV_FAULT_WAIT_TIMEOUT and returns instead of hanging.
+// Every wait in this library is bounded: after this long (or this many polls,
+// whichever comes first) the waiter gives up, the kernel records
+// ZDMMV_FAULT_WAIT_TIMEOUT and returns instead of hanging.
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s
+constexpr uint32_t kWaitMaxPolls = 1u << 26;
 
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
-    while (!mbar_try_wait(bar, parity)) {
-        if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+    for (uint32_t polls = 0; !mbar_try_wait(bar, parity); ++polls) {
+        if (polls >= kWaitMaxPolls || global_timer_ns() - t0 > kWaitLimitNs) return false;
     }
     return true;
 }

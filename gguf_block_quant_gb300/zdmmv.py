@@ -64,6 +64,7 @@ _SIGS = {
     "zdmmv_host_step": ([_int, _vp, _int, _i64, _i64, _vp, _int, _vp, _vp, ctypes.c_size_t, _vp], _int),
     "zdmmv_debug_block_sums": ([_int, _vp, _int, _i64, _i64, _vp, _vp, _vp], _int),
     "zdmmv_selftest_dp4a": ([_vp, _vp, _vp, _vp, _int, _vp], _int),
+    "zdmmv_selftest_wait_timeout": ([_vp, _vp], _int),
     "zdmmv_device_status": ([ctypes.POINTER(ctypes.c_uint32), _int], _int),
 }
 
@@ -252,6 +253,14 @@ def selftest_dp4a(a, b, c, out=None, stream=None):
         out = torch.empty_like(a)
     _call("zdmmv_selftest_dp4a", _ptr(a), _ptr(b), _ptr(c), _ptr(out), a.numel(), _stream(stream))
     return out
+
+
+def selftest_wait_timeout(result=None, stream=None):
+    """Run the failure-path self-test (a wait that can never complete, bounded)."""
+    if result is None:
+        result = torch.zeros(1, dtype=torch.int32, device="cuda")
+    _call("zdmmv_selftest_wait_timeout", _ptr(result), _stream(stream))
+    return result
 
 
 def device_status(clear: bool = False) -> int:

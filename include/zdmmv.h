@@ -241,6 +241,13 @@ zdmmv_status zdmmv_debug_block_sums(zdmmv_fmt fmt, const void *w, zdmmv_layout l
 zdmmv_status zdmmv_selftest_dp4a(const int32_t *a, const int32_t *b, const int32_t *c,
                                  int32_t *out, int n, zdmmv_stream_t stream);
 
+/* Self-test of the failure path: a kernel waits on a barrier that nothing ever
+ * completes; the wait gives up after its bound (about 1 s), the kernel records
+ * ZDMMV_FAULT_WAIT_TIMEOUT in the device fault word and stores 1 in result[0]
+ * (0 would mean the wait completed), and returns normally -- no trap, no hang,
+ * the context stays usable. result: device int32. Errors: ERR_NULL, ERR_CUDA. */
+zdmmv_status zdmmv_selftest_wait_timeout(int32_t *result, zdmmv_stream_t stream);
+
 /* Read (and, if clear != 0, reset) the device fault bits of the current device
  * (ZDMMV_FAULT_*). Synchronizes the device first. *bits_out = 0 means no kernel
  * has reported a fault. Errors: ERR_NULL, ERR_CUDA. */

@@ -81,6 +81,7 @@ def test_other_argument_checks(L):
     assert L.zdmmv_host_step(8, FAKE, 0, 4, 64, FAKE, 1, FAKE, FAKE, 10, None) == 6
     assert L.zdmmv_host_step(8, FAKE, 0, 4, 64, FAKE, 0, FAKE, FAKE, 1 << 20, None) == 2
     assert L.zdmmv_device_status(None, 0) == 1
+    assert L.zdmmv_selftest_wait_timeout(None, None) == 1
     f = L.zdmmv_dmmv_f32
     assert f(8, FAKE, 0, 0, 64, None, 1, None, None) == 0                                # rows == 0
     assert f(8, None, 0, 4, 64, FAKE, 1, FAKE, None) == 1
