@@ -306,6 +306,28 @@ def measure_dense(cfg, layers, steps, warmup, world, device, eager, layout=0):
             "rows_per_s": cfg.batch * cfg.rows / per_launch_s, "algorithmic_bytes": nbytes}
 
 
+def measure_argmax(cfg, layers, steps, warmup, world, device, eager):
+    """The LM head with the fused argmax epilogue (no logits written), back to back."""
+    import torch
+    pool = DensePool(cfg, layers)
+    Z = pool.Z
+    ws = [torch.empty(Z.ARGMAX_WORKSPACE_BYTES, dtype=torch.uint8, device="cuda") for _ in range(layers)]
+    out = [torch.empty(1, dtype=torch.int32, device="cuda") for _ in range(layers)]
+
+    def run_all():
+        for l in range(layers):
+            Z.dmmv_argmax(cfg.fmt, pool.w[l], cfg.rows, cfg.cols, pool.xq[l], workspace=ws[l], out=out[l])
+
+    run = graph_or_eager(run_all, eager)
+    ms, _ = time_fn(run, steps, warmup, world, device)
+    per = ms / 1e3 / (steps * layers)
+    nbytes = cfg.weight_bytes + cfg.nb * 34 + 4
+    del pool
+    torch.cuda.empty_cache()
+    return {"us": per * 1e6, "gbs": nbytes / per / 1e9, "algorithmic_bytes": nbytes,
+            "launches": 2, "note": "DMMV with per-CTA (max, row) partials + one-CTA reduce; logits never written"}
+
+
 def measure_moe(steps, warmup, world, device, eager, l2_bytes):
     """Config: 9 selected experts (8 routed + shared) of a 129-slot stack; one
     step = gate, up (Q4_0 512x2048) and down (Q8_0 2048x512) gathers, each ONE
@@ -453,6 +475,9 @@ def gpu_arm(args):
                                args.eager, layout=1)
             workloads[c.name]["repacked_layout"] = {"dmmv_gbs": rp["dmmv_gbs"], "dmmv_us": rp["dmmv_us"],
                                                     "pct_of_peak": 100 * rp["dmmv_gbs"] / hbm_peak}
+        workloads["lm_head_q4_0_248320x2048"]["argmax_epilogue"] = measure_argmax(
+            synth.LM_HEAD_Q4_0, layers_for(synth.LM_HEAD_Q4_0, l2), max(5, args.steps // 4), args.warmup, world,
+            device, args.eager)
         workloads["moe_experts_top8_plus_shared"] = measure_moe(max(5, args.steps // 4), args.warmup, world,
                                                                 device, args.eager, l2)
 

@@ -99,6 +99,17 @@ inline int64_t round_up(int64_t v, int64_t m) { return (v + m - 1) / m * m; }
 
 zdmmv_status from_cuda(cudaError_t e) { return e == cudaSuccess ? ZDMMV_OK : ZDMMV_ERR_CUDA; }
 
+// Launch without attributes; the launch's own error is returned (never an
+// earlier one left behind by an unrelated call).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_plain_cfg(void (*kern)(KArgs...), unsigned grid, unsigned block, cudaStream_t st, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid, 1, 1);
+    cfg.blockDim = dim3(block, 1, 1);
+    cfg.stream = st;
+    return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 }  // namespace
 
 // ------------------------------------------------------------ planning
@@ -234,6 +245,51 @@ __global__ void __launch_bounds__(256) repack_kernel(const uint8_t *__restrict__
 #pragma unroll
     for (int k = 0; k < kQB / 16; ++k) dq[k] = make_uint4(q[4 * k], q[4 * k + 1], q[4 * k + 2], q[4 * k + 3]);
     reinterpret_cast<uint16_t *>(dst + nblocks * kQB)[i] = h[0];
+}
+
+// Final pass of the argmax epilogue: one CTA reduces the per-CTA partials with
+// the same ordering (larger value, then smaller row).
+__global__ void __launch_bounds__(256) argmax_reduce_kernel(const uint2 *__restrict__ parts, int n,
+                                                            int32_t *__restrict__ out_row, float *__restrict__ out_max) {
+    pdl_wait_api();
+    pdl_trigger_api();
+    __shared__ float sv[8];
+    __shared__ int sr[8];
+    float bv = 0.0f;
+    int br = -1;
+    for (int i = threadIdx.x; i < n; i += blockDim.x) {
+        const uint2 p = parts[i];
+        const float v = __uint_as_float(p.x);
+        const int r = static_cast<int>(p.y);
+        if (r >= 0 && (br < 0 || v > bv || (v == bv && r < br))) {
+            bv = v;
+            br = r;
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float v = __shfl_xor_sync(0xffffffffu, bv, o);
+        const int r = __shfl_xor_sync(0xffffffffu, br, o);
+        if (r >= 0 && (br < 0 || v > bv || (v == bv && r < br))) {
+            bv = v;
+            br = r;
+        }
+    }
+    const int warp = threadIdx.x >> 5;
+    if ((threadIdx.x & 31) == 0) {
+        sv[warp] = bv;
+        sr[warp] = br;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        for (int q = 1; q < static_cast<int>(blockDim.x >> 5); ++q)
+            if (sr[q] >= 0 && (br < 0 || sv[q] > bv || (sv[q] == bv && sr[q] < br))) {
+                bv = sv[q];
+                br = sr[q];
+            }
+        out_row[0] = br;
+        if (out_max) out_max[0] = bv;
+    }
 }
 
 // Failure-path self-test: one warp waits on an mbarrier that nothing ever
@@ -447,7 +503,10 @@ cudaError_t launch_plain_fx(int fmt, int layout, const DmmvArgs &a, int sms, cud
     cfg.attrs = attr;
     cfg.numAttrs = pdl_enabled() ? 1 : 0;
     auto go = [&](auto kern) -> cudaError_t {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kPlainFxMaxSmem);
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e != cudaSuccess) return e;
+        e = raise_dynamic_smem_limit(reinterpret_cast<const void *>(kern), dev);
         if (e != cudaSuccess) return e;
         return cudaLaunchKernelEx(&cfg, kern, a);
     };
@@ -581,6 +640,53 @@ zdmmv_status gather_entry(int fmt, const void *w_stack, const void *w_stack_b, i
     return run_dmmv(fmt, layout, a, w_stack_b ? 2 * n : n, st);
 }
 
+zdmmv_status argmax_entry(int fmt, const void *w, int layout, int64_t rows, int64_t cols, const void *xq,
+                          int32_t *argmax_out, float *max_out, void *workspace, size_t workspace_bytes,
+                          cudaStream_t st) {
+    if (block_bytes(fmt) == 0) return ZDMMV_ERR_FORMAT;
+    if (layout != ZDMMV_LAYOUT_GGUF && layout != ZDMMV_LAYOUT_REPACKED) return ZDMMV_ERR_LAYOUT;
+    if (rows <= 0 || rows > 0x7fffffff || !tma_shape_ok(fmt, cols)) return ZDMMV_ERR_SHAPE;
+    if (!w || !xq || !argmax_out || !workspace) return ZDMMV_ERR_NULL;
+    if (!aligned(w, 16) || !aligned(xq, 16) || !aligned(workspace, 16) || !aligned(argmax_out, 4) ||
+        (max_out && !aligned(max_out, 4)))
+        return ZDMMV_ERR_ALIGN;
+    if (workspace_bytes < ZDMMV_ARGMAX_WORKSPACE_BYTES) return ZDMMV_ERR_SIZE;
+    const DeviceInfo *dev = nullptr;
+    if (device_info(&dev) != cudaSuccess) return ZDMMV_ERR_CUDA;
+    DmmvArgs a{};
+    a.w = static_cast<const uint8_t *>(w);
+    a.xq = static_cast<const uint8_t *>(xq);
+    a.rows = rows;
+    a.nb = static_cast<int32_t>(cols / kQK);
+    a.batch = 1;
+    a.fault = dev->fault;
+    a.argmax_parts = static_cast<uint2 *>(workspace);
+    const TmaPlan p = tma_plan(fmt, layout, cols);
+    a.tile_rows = p.tile_rows;
+    a.stage_bytes = p.stage_bytes;
+    a.x_bytes_padded = p.x_bytes_padded;
+    int per_sm = fmt == kFmtQ8 ? tma_ctas_per_sm_q8(layout, p) : tma_ctas_per_sm_q4(layout, p);
+    const int want = ctas_per_sm_per_launch(rows * a.nb * static_cast<int64_t>(block_bytes(fmt)));
+    if (per_sm > want) per_sm = want;
+    int64_t ctas = static_cast<int64_t>(dev->sms) * per_sm;
+    if (ctas > rows) ctas = rows;
+    if (ctas > kArgmaxMaxCtas) ctas = kArgmaxMaxCtas;
+    cudaError_t e = fmt == kFmtQ8 ? launch_argmax_q8(a, p, layout, static_cast<int>(ctas), st, pdl_enabled())
+                                  : launch_argmax_q4(a, p, layout, static_cast<int>(ctas), st, pdl_enabled());
+    if (e != cudaSuccess) return ZDMMV_ERR_CUDA;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(1, 1, 1);
+    cfg.blockDim = dim3(256, 1, 1);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl_enabled() ? 1 : 0;
+    return from_cuda(cudaLaunchKernelEx(&cfg, argmax_reduce_kernel, static_cast<const uint2 *>(a.argmax_parts),
+                                        static_cast<int>(ctas), argmax_out, max_out));
+}
+
 zdmmv_status dmmv_f32_entry(int fmt, const void *w, int layout, int64_t rows, int64_t cols, const float *x,
                             int batch, float *y, cudaStream_t st) {
     if (block_bytes(fmt) == 0) return ZDMMV_ERR_FORMAT;
@@ -697,6 +803,13 @@ zdmmv_status zdmmv_dmmv_f32(zdmmv_fmt fmt, const void *w, zdmmv_layout layout, i
     return dmmv_f32_entry(fmt, w, layout, rows, cols, x, batch, y, reinterpret_cast<cudaStream_t>(stream));
 }
 
+zdmmv_status zdmmv_dmmv_argmax(zdmmv_fmt fmt, const void *w, zdmmv_layout layout, int64_t rows, int64_t cols,
+                               const void *xq, int32_t *argmax_out, float *max_out, void *workspace,
+                               size_t workspace_bytes, zdmmv_stream_t stream) {
+    return argmax_entry(fmt, w, layout, rows, cols, xq, argmax_out, max_out, workspace, workspace_bytes,
+                        reinterpret_cast<cudaStream_t>(stream));
+}
+
 size_t zdmmv_repacked_bytes(zdmmv_fmt fmt, int64_t rows, int64_t cols) {
     if (block_bytes(fmt) == 0 || rows < 0 || cols <= 0 || cols % kQK) return 0;
     return static_cast<size_t>(rows * (cols / kQK) * block_bytes(fmt));
@@ -718,11 +831,10 @@ zdmmv_status zdmmv_repack(zdmmv_fmt fmt, const void *src, int64_t rows, int64_t 
     const int64_t ctas = (nblocks + 255) / 256;
     if (ctas > 0x7fffffff) return ZDMMV_ERR_SHAPE;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    if (fmt == ZDMMV_Q8_0)
-        repack_kernel<kFmtQ8><<<static_cast<unsigned>(ctas), 256, 0, st>>>(s8, nblocks, d8);
-    else
-        repack_kernel<kFmtQ4><<<static_cast<unsigned>(ctas), 256, 0, st>>>(s8, nblocks, d8);
-    return from_cuda(cudaGetLastError());
+    return from_cuda(fmt == ZDMMV_Q8_0 ? launch_plain_cfg(repack_kernel<kFmtQ8>, static_cast<unsigned>(ctas), 256, st,
+                                                          s8, nblocks, d8)
+                                       : launch_plain_cfg(repack_kernel<kFmtQ4>, static_cast<unsigned>(ctas), 256, st,
+                                                          s8, nblocks, d8));
 }
 
 size_t zdmmv_host_step_workspace_bytes(int64_t rows, int64_t cols, int batch) {
@@ -775,7 +887,8 @@ zdmmv_status zdmmv_debug_block_sums(zdmmv_fmt fmt, const void *w, zdmmv_layout l
     const uint8_t *w8 = static_cast<const uint8_t *>(w);
     const uint8_t *x8 = static_cast<const uint8_t *>(xq);
     const unsigned g = static_cast<unsigned>(ctas);
-#define ZDMMV_SUMS(F, L, PR) block_sums_kernel<F, L, PR><<<g, 256, 0, st>>>(w8, rows, nb, x8, sums)
+    cudaError_t e = cudaSuccess;
+#define ZDMMV_SUMS(F, L, PR) e = launch_plain_cfg(block_sums_kernel<F, L, PR>, g, 256, st, w8, rows, nb, x8, sums)
     if (fmt == ZDMMV_Q8_0) {
         if (layout == ZDMMV_LAYOUT_GGUF) {
             if (pairs) ZDMMV_SUMS(kFmtQ8, kLayoutGguf, true); else ZDMMV_SUMS(kFmtQ8, kLayoutGguf, false);
@@ -790,7 +903,7 @@ zdmmv_status zdmmv_debug_block_sums(zdmmv_fmt fmt, const void *w, zdmmv_layout l
         }
     }
 #undef ZDMMV_SUMS
-    return from_cuda(cudaGetLastError());
+    return from_cuda(e);
 }
 
 zdmmv_status zdmmv_selftest_dp4a(const int32_t *a, const int32_t *b, const int32_t *c, int32_t *out, int n,
@@ -798,16 +911,16 @@ zdmmv_status zdmmv_selftest_dp4a(const int32_t *a, const int32_t *b, const int32
     if (n < 0) return ZDMMV_ERR_SHAPE;
     if (n == 0) return ZDMMV_OK;
     if (!a || !b || !c || !out) return ZDMMV_ERR_NULL;
-    selftest_dp4a_kernel<<<(n + 255) / 256, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(a, b, c, out, n);
-    return from_cuda(cudaGetLastError());
+    return from_cuda(launch_plain_cfg(selftest_dp4a_kernel, static_cast<unsigned>((n + 255) / 256), 256,
+                                      reinterpret_cast<cudaStream_t>(stream), a, b, c, out, n));
 }
 
 zdmmv_status zdmmv_selftest_wait_timeout(int32_t *result, zdmmv_stream_t stream) {
     if (!result) return ZDMMV_ERR_NULL;
     const DeviceInfo *dev = nullptr;
     if (device_info(&dev) != cudaSuccess) return ZDMMV_ERR_CUDA;
-    selftest_wait_timeout_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(dev->fault, result);
-    return from_cuda(cudaGetLastError());
+    return from_cuda(launch_plain_cfg(selftest_wait_timeout_kernel, 1, 32, reinterpret_cast<cudaStream_t>(stream),
+                                      dev->fault, result));
 }
 
 zdmmv_status zdmmv_device_status(uint32_t *bits_out, int clear) {

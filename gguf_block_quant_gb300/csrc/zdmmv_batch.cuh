@@ -371,11 +371,7 @@ struct BatchInst {
         cudaError_t e = cudaGetDevice(&dev);
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < 64 && !done[dev]) {
-            int optin = 0;
-            e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-            if (e != cudaSuccess) return e;
-            e = cudaFuncSetAttribute(reinterpret_cast<const void *>(kKernel),
-                                     cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
+            e = raise_dynamic_smem_limit(reinterpret_cast<const void *>(kKernel), dev);
             if (e != cudaSuccess) return e;
             done[dev] = true;
         }

@@ -32,7 +32,11 @@ struct DmmvArgs {
     int32_t tile_rows;       // rows per pipeline stage (pipelined kernel)
     int32_t stage_bytes;     // shared-memory bytes per stage (pipelined kernel)
     int32_t x_bytes_padded;  // shared-memory bytes of the staged activation
+    uint2 *argmax_parts;     // argmax epilogue: per-CTA (max bits, row), or nullptr
 };
+
+// Most CTAs an argmax launch uses (its workspace holds one 8-byte partial each).
+constexpr int kArgmaxMaxCtas = 2048;
 
 // Launch description chosen by the host for the pipelined kernel.
 struct TmaPlan {
@@ -59,6 +63,18 @@ constexpr int64_t kLargeLaunchBytes = 32ll << 20;  // weight bytes per launch
 constexpr int kSmemPerCtaTarget = 54 * 1024;         // keeps 4 CTAs per SM possible
 constexpr int kTmaRowsIlp = 2;                       // rows per row group in flight
 
+// Allow a kernel the device's opt-in shared memory minus its static shared memory.
+inline cudaError_t raise_dynamic_smem_limit(const void *fn, int dev) {
+    int optin = 0;
+    cudaError_t e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (e != cudaSuccess) return e;
+    cudaFuncAttributes fa{};
+    e = cudaFuncGetAttributes(&fa, fn);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                optin - static_cast<int>(fa.sharedSizeBytes));
+}
+
 // Whether the pipelined kernel takes this shape, and its plan.
 bool tma_shape_ok(int fmt, int64_t cols);
 TmaPlan tma_plan(int fmt, int layout, int64_t cols);
@@ -77,6 +93,10 @@ struct BatchPlan {
 bool batch_plan(int fmt, int64_t cols, int batch, BatchPlan *out);
 cudaError_t launch_batch_q8(const DmmvArgs &a, const BatchPlan &p, int layout, int ctas, cudaStream_t st, bool pdl);
 cudaError_t launch_batch_q4(const DmmvArgs &a, const BatchPlan &p, int layout, int ctas, cudaStream_t st, bool pdl);
+
+// The pipelined kernel with the argmax epilogue (no y written; per-CTA partials).
+cudaError_t launch_argmax_q8(const DmmvArgs &a, const TmaPlan &p, int layout, int ctas, cudaStream_t st, bool pdl);
+cudaError_t launch_argmax_q4(const DmmvArgs &a, const TmaPlan &p, int layout, int ctas, cudaStream_t st, bool pdl);
 
 // CTAs of the pipelined kernel that fit on one SM for this plan.
 int tma_ctas_per_sm_q8(int layout, const TmaPlan &p);

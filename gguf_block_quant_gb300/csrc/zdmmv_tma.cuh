@@ -108,7 +108,15 @@ __device__ __forceinline__ void consumer_barrier() {
 // FX = true: the kernel reads the fp32 activation (a.xf) and quantizes it to
 // Q8_0 blocks in shared memory itself (same device function as the stand-alone
 // quantizer, hence identical bytes), instead of staging a.xq.
-template <int FMT, int LAYOUT, int LPR, int PPL, int STAGES, int MINB, bool FX>
+// Argmax epilogue ordering: a larger value wins, equal values keep the smaller row.
+__device__ __forceinline__ bool argmax_better(float v, int row, float bv, int brow) {
+    return row >= 0 && (brow < 0 || v > bv || (v == bv && row < brow));
+}
+
+// EPI = 0: store y. EPI = 1 (argmax epilogue): keep each row group's running
+// (max, first row) in registers, reduce over the CTA and store one 8-byte partial
+// per CTA in a.argmax_parts; no y is written.
+template <int FMT, int LAYOUT, int LPR, int PPL, int STAGES, int MINB, bool FX, int EPI = 0>
 __global__ void __launch_bounds__(kTmaThreads, MINB) dmmv_tma_kernel(const DmmvArgs a) {
     using P = Pair<FMT, LAYOUT>;
     constexpr int kRowsPar = kConsumerThreads / LPR;
@@ -149,7 +157,12 @@ __global__ void __launch_bounds__(kTmaThreads, MINB) dmmv_tma_kernel(const DmmvA
         }
         w += static_cast<int64_t>(e) * a.expert_stride;
     }
-    if (r1 <= r0) return;
+    if (r1 <= r0) {
+        if constexpr (EPI == 1) {
+            if (tid == 0) a.argmax_parts[blockIdx.x] = make_uint2(0u, 0xffffffffu);  // no candidate
+        }
+        return;
+    }
     const int T = a.tile_rows;
     const int ntiles = static_cast<int>((r1 - r0 + T - 1) / T);
 
@@ -257,6 +270,8 @@ __global__ void __launch_bounds__(kTmaThreads, MINB) dmmv_tma_kernel(const DmmvA
         }
     }
 
+    float best = 0.0f;  // argmax epilogue: this row group's running maximum and its row
+    int best_row = -1;
     for (int t = 0; t < ntiles; ++t) {
         const int s = t % STAGES;
         if (!__all_sync(0xffffffffu, mbar_wait(&full[s], static_cast<uint32_t>(t / STAGES) & 1u))) {
@@ -283,19 +298,47 @@ __global__ void __launch_bounds__(kTmaThreads, MINB) dmmv_tma_kernel(const DmmvA
 #pragma unroll
             for (int r = 0; r < kRowsIlp; ++r) {
                 const int i = base + r * kRowsPar + g;
-                if (l == 0 && i < nr) y[tr0 + i] = acc[r];
+                if constexpr (EPI == 0) {
+                    if (l == 0 && i < nr) y[tr0 + i] = acc[r];
+                } else {
+                    // rows reach a row group in increasing order: a strictly larger value replaces
+                    if (i < nr && (best_row < 0 || acc[r] > best)) {
+                        best = acc[r];
+                        best_row = static_cast<int>(tr0 + i);
+                    }
+                }
             }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);
     }
+    if constexpr (EPI == 1) {
+        // reduce the row groups' candidates (kept on every lane of a group) in group order
+        __shared__ float cand_v[kRowsPar];
+        __shared__ int cand_r[kRowsPar];
+        if (l == 0) {
+            cand_v[g] = best;
+            cand_r[g] = best_row;
+        }
+        consumer_barrier();
+        if (tid == 0) {
+            float bv = 0.0f;
+            int br = -1;
+            for (int q = 0; q < kRowsPar; ++q)
+                if (argmax_better(cand_v[q], cand_r[q], bv, br)) {
+                    bv = cand_v[q];
+                    br = cand_r[q];
+                }
+            a.argmax_parts[blockIdx.x] = make_uint2(__float_as_uint(bv), static_cast<uint32_t>(br));
+        }
+    }
 }
 
 // ------------------------------------------------------------------ host side
-template <int FMT, int LAYOUT, int LPR, int PPL, int STAGES, bool FX>
+template <int FMT, int LAYOUT, int LPR, int PPL, int STAGES, bool FX, int EPI = 0>
 struct TmaInst {
     static constexpr int kMinBlocks = PPL >= 4 ? 2 : 4;
-    static constexpr auto kKernel = &dmmv_tma_kernel<FMT, LAYOUT, LPR, PPL, STAGES, kMinBlocks, FX>;
+    static constexpr auto kKernel = &dmmv_tma_kernel<FMT, LAYOUT, LPR, PPL, STAGES, kMinBlocks, FX, EPI>;
     static void *fn() { return reinterpret_cast<void *>(kKernel); }
 
     static cudaError_t prepare() {
@@ -305,10 +348,7 @@ struct TmaInst {
         cudaError_t e = cudaGetDevice(&dev);
         if (e != cudaSuccess) return e;
         if (dev < 64 && done[dev]) return cudaSuccess;
-        int optin = 0;
-        e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-        if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(fn(), cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
+        e = raise_dynamic_smem_limit(fn(), dev);
         if (e != cudaSuccess) return e;
         if (dev < 64) done[dev] = true;
         return cudaSuccess;
@@ -356,11 +396,11 @@ struct TmaInst {
 };
 
 // Dispatch over the (lpr, ppl, stages) variants instantiated for one format.
-template <int FMT, int LAYOUT, bool FX, typename F>
+template <int FMT, int LAYOUT, bool FX, int EPI = 0, typename F>
 cudaError_t with_variant(const TmaPlan &p, F &&f) {
 #define ZDMMV_VARIANT(LPR_, PPL_, ST_)                                        \
     if (p.lpr == LPR_ && p.ppl == PPL_ && p.stages == ST_)                    \
-        return f(TmaInst<FMT, LAYOUT, LPR_, PPL_, ST_, FX>{});
+        return f(TmaInst<FMT, LAYOUT, LPR_, PPL_, ST_, FX, EPI>{});
     ZDMMV_VARIANT(8, 1, 4)
     ZDMMV_VARIANT(16, 1, 4)
     ZDMMV_VARIANT(32, 1, 4)
@@ -390,6 +430,13 @@ cudaError_t launch_tma_fmt(const DmmvArgs &a, const TmaPlan &p, int layout, bool
     }
     if (layout == kLayoutGguf) return with_variant<FMT, kLayoutGguf, false>(p, go);
     return with_variant<FMT, kLayoutRepacked, false>(p, go);
+}
+
+template <int FMT>
+cudaError_t launch_argmax_fmt(const DmmvArgs &a, const TmaPlan &p, int layout, int ctas, cudaStream_t st, bool pdl) {
+    auto go = [&](auto inst) { return decltype(inst)::launch(a, p, ctas, 1, st, pdl); };
+    if (layout == kLayoutGguf) return with_variant<FMT, kLayoutGguf, false, 1>(p, go);
+    return with_variant<FMT, kLayoutRepacked, false, 1>(p, go);
 }
 
 template <int FMT>

@@ -26,6 +26,7 @@ QK = 32
 MAX_BATCH = 8
 BLOCK_BYTES = {Q4_0: 18, Q8_0: 34}
 FAULT_WAIT_TIMEOUT = 1
+ARGMAX_WORKSPACE_BYTES = 16384
 
 STATUS = {0: "ok", 1: "null pointer", 2: "bad shape", 3: "misaligned pointer or stride",
           4: "unknown layout", 5: "unknown block format", 6: "buffer too small",
@@ -54,6 +55,7 @@ _SIGS = {
     "zdmmv_q8_0_batched": ([_vp, _int, _i64, _i64, _vp, _int, _vp, _vp], _int),
     "zdmmv_q4_0_batched": ([_vp, _int, _i64, _i64, _vp, _int, _vp, _vp], _int),
     "zdmmv_dmmv_f32": ([_int, _vp, _int, _i64, _i64, _vp, _int, _vp, _vp], _int),
+    "zdmmv_dmmv_argmax": ([_int, _vp, _int, _i64, _i64, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp], _int),
     "zdmmv_expert_gather": ([_int, _vp, _i64, _int, _i64, _i64, _vp, _int, _int, _vp, _i64, _vp, _vp, _vp],
                             _int),
     "zdmmv_expert_gather2": ([_int, _vp, _vp, _i64, _int, _i64, _i64, _vp, _int, _int, _vp, _i64, _vp, _vp,
@@ -187,6 +189,18 @@ def dmmv_f32(fmt: int, w, rows: int, cols: int, x, batch: int = 1, y=None, layou
     y = _out(y, (batch, rows) if batch > 1 else (rows,), w.device)
     _call("zdmmv_dmmv_f32", fmt, _ptr(w), layout, rows, cols, _ptr(x), batch, _ptr(y), _stream(stream))
     return y
+
+
+def dmmv_argmax(fmt: int, w, rows: int, cols: int, xq, workspace=None, out=None, max_out=None,
+                layout: int = GGUF, stream=None):
+    """Index (int32 device tensor [1]) of the largest of W.x, without writing W.x."""
+    if workspace is None:
+        workspace = torch.empty(ARGMAX_WORKSPACE_BYTES, dtype=torch.uint8, device=w.device)
+    if out is None:
+        out = torch.empty(1, dtype=torch.int32, device=w.device)
+    _call("zdmmv_dmmv_argmax", fmt, _ptr(w), layout, rows, cols, _ptr(xq), _ptr(out), _ptr(max_out),
+          _ptr(workspace), _nbytes(workspace), _stream(stream))
+    return out
 
 
 def expert_gather(fmt: int, w_stack, expert_stride: int, rows: int, cols: int, idx, n_experts: int, xq,

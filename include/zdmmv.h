@@ -156,6 +156,28 @@ zdmmv_status zdmmv_dmmv_f32(zdmmv_fmt fmt, const void *w, zdmmv_layout layout, i
                             int64_t cols, const float *x, int batch, float *y,
                             zdmmv_stream_t stream);
 
+/* LM-head DMMV with a fused argmax epilogue: the greedy pick over the logits
+ * W.x without writing them (the M1 decode chain ends "LM head -> argmax":
+ * "Bringing ZINC to NVIDIA", section "The roadmap: from 70 to a coherent
+ * token"; the logits tail is part of the per-token time in the habr article,
+ * "Разбивка по времени"). Each CTA keeps the largest logit of its rows and the
+ * first row holding it, writes one 8-byte partial into `workspace`, and a
+ * one-CTA pass reduces the partials. The logits are the same fp32 values
+ * zdmmv_q{8,4}_0 would write (same kernel arithmetic), so the result is the
+ * first index of their maximum.
+ *   w, layout, rows (1 .. 2^31-1), cols, xq   as zdmmv_q8_0; cols must be a
+ *            multiple of 256 and at most 8192 (else ERR_SHAPE).
+ *   argmax_out  device int32[1]: the row index.
+ *   max_out     nullable device float[1]: the logit at that row.
+ *   workspace   caller-owned device scratch, 16-byte aligned, of at least
+ *               ZDMMV_ARGMAX_WORKSPACE_BYTES; overwritten by each call, so two
+ *               calls in flight at once need two workspaces.
+ * Errors: ERR_NULL, ERR_SHAPE, ERR_ALIGN, ERR_LAYOUT, ERR_FORMAT, ERR_SIZE, ERR_CUDA. */
+#define ZDMMV_ARGMAX_WORKSPACE_BYTES 16384
+zdmmv_status zdmmv_dmmv_argmax(zdmmv_fmt fmt, const void *w, zdmmv_layout layout, int64_t rows,
+                               int64_t cols, const void *xq, int32_t *argmax_out, float *max_out,
+                               void *workspace, size_t workspace_bytes, zdmmv_stream_t stream);
+
 /* MoE expert gather: n matrices picked by index from a stack of n_experts
  * equally shaped matrices, all in ONE launch (routed experts are selected per
  * token by the router: "CUDA backend for ZINC", M1 list "dmmv_q4k_moe";

@@ -77,6 +77,8 @@ def _bind(L):
                                       f64p, f64p]
     L.oracle_expert_gather.argtypes = [ctypes.c_int, u8p, i64, i64, i64, i32p, ctypes.c_int,
                                        ctypes.c_int, u8p, i64, f64p, f64p, i32p]
+    L.oracle_argmax.argtypes = [f64p, i64, f64p]
+    L.oracle_argmax.restype = ctypes.c_int64
     L.oracle_repack.argtypes = [ctypes.c_int, u8p, i64, i64, u8p]
     L.oracle_unpack.argtypes = [ctypes.c_int, u8p, i64, i64, u8p]
     return L
@@ -218,6 +220,14 @@ def expert_gather(fmt: int, w_stack, expert_stride: int, rows: int, cols: int, i
                                       _p(y, ctypes.c_double), _p(e, ctypes.c_double),
                                       ctypes.byref(st)), "expert_gather")
     return y, e, int(st.value)
+
+
+def argmax(y) -> tuple[int, float]:
+    """(first index of the maximum, the maximum)."""
+    y = np.ascontiguousarray(y, dtype=np.float64).reshape(-1)
+    m = ctypes.c_double(0.0)
+    i = lib().oracle_argmax(_p(y, ctypes.c_double), y.size, ctypes.byref(m))
+    return int(i), float(m.value)
 
 
 def repack(fmt: int, src, rows: int, cols: int) -> np.ndarray:

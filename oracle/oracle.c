@@ -269,6 +269,24 @@ int oracle_expert_gather(int fmt, const uint8_t *w_stack, int64_t expert_stride_
     return 0;
 }
 
+/* -------------------------------------------------------------- argmax ---- */
+
+/* Greedy token pick over logits: the first index holding the maximum value
+ * (argmax after the LM head: "Bringing ZINC to NVIDIA", section "The roadmap:
+ * from 70 to a coherent token", the M1 forward order ending in argmax). */
+int64_t oracle_argmax(const double *y, int64_t n, double *max_out)
+{
+    if (n <= 0)
+        return -1;
+    int64_t best = 0;
+    for (int64_t i = 1; i < n; ++i)
+        if (y[i] > y[best])
+            best = i;
+    if (max_out)
+        *max_out = y[best];
+    return best;
+}
+
 /* -------------------------------------------------------------- repack ---- */
 
 int oracle_repack(int fmt, const uint8_t *src, int64_t rows, int64_t cols, uint8_t *dst)

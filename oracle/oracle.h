@@ -96,6 +96,10 @@ int oracle_expert_gather(int fmt, const uint8_t *w_stack, int64_t expert_stride_
                          int n_experts, const uint8_t *xq, int64_t xq_stride_bytes,
                          double *y, double *e, int32_t *status);
 
+/* Index of the largest of n values (the smallest such index on ties), or -1 for
+ * n <= 0; the greedy pick over the LM-head logits. *max_out receives the value. */
+int64_t oracle_argmax(const double *y, int64_t n, double *max_out);
+
 /* GGUF array-of-blocks -> repacked (quant stream + scale array), and back. */
 int oracle_repack(int fmt, const uint8_t *src, int64_t rows, int64_t cols, uint8_t *dst);
 int oracle_unpack(int fmt, const uint8_t *src, int64_t rows, int64_t cols, uint8_t *dst);

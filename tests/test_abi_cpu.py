@@ -82,6 +82,12 @@ def test_other_argument_checks(L):
     assert L.zdmmv_host_step(8, FAKE, 0, 4, 64, FAKE, 0, FAKE, FAKE, 1 << 20, None) == 2
     assert L.zdmmv_device_status(None, 0) == 1
     assert L.zdmmv_selftest_wait_timeout(None, None) == 1
+    a = L.zdmmv_dmmv_argmax
+    assert a(2, FAKE, 0, 100, 160, FAKE, FAKE, None, FAKE, 16384, None) == 2     # off the pipelined widths
+    assert a(2, FAKE, 0, 0, 2048, FAKE, FAKE, None, FAKE, 16384, None) == 2      # no rows
+    assert a(2, FAKE, 0, 100, 2048, FAKE, None, None, FAKE, 16384, None) == 1
+    assert a(2, FAKE, 0, 100, 2048, FAKE, FAKE, None, FAKE, 1024, None) == 6     # workspace too small
+    assert a(2, FAKE, 0, 100, 2048, FAKE, FAKE, None, FAKE + 4, 16384, None) == 3
     f = L.zdmmv_dmmv_f32
     assert f(8, FAKE, 0, 0, 64, None, 1, None, None) == 0                                # rows == 0
     assert f(8, None, 0, 4, 64, FAKE, 1, FAKE, None) == 1

@@ -63,6 +63,13 @@ def test_dense_workload_full_size(cfg):
     y_ref, e_ref = oracle.dmmv(cfg.fmt, w, cfg.rows, cfg.cols, xq_ref)
     check(y, y_ref, e_ref)
     sampled_sums(cfg, w, xq_ref, wd, xqd)
+    # the greedy pick with the fused argmax epilogue: the first index of the
+    # kernel's own logits' maximum, and a valid argmax of the oracle's
+    i = int(Z.dmmv_argmax(cfg.fmt, wd, cfg.rows, cfg.cols, xqd).item())
+    yh = y.cpu().numpy()
+    assert i == int(np.argmax(yh))
+    j, _ = oracle.argmax(y_ref)
+    assert y_ref[i] >= y_ref[j] - 1e-5 * (e_ref[i] + e_ref[j]) - 2e-6
 
 
 @pytest.mark.parametrize("batch", [1, 2, 4, 8])

@@ -42,6 +42,8 @@ MUTANTS = {
     # fp16 rounding by truncation
     "half_truncate": ("double m = rint(v * ldexp(1.0, 10 - expo));",
                       "double m = floor(v * ldexp(1.0, 10 - expo));"),
+    # argmax keeping the last index on ties
+    "argmax_last_tie": ("if (y[i] > y[best])", "if (y[i] >= y[best])"),
     # dp4a reading unsigned bytes
     "dp4a_unsigned": ("int8_t ab = (int8_t)(uint8_t)", "uint8_t ab = (uint8_t)"),
 }
@@ -57,6 +59,7 @@ PINS = [
     pins.test_decode_block_q4_0_offset_and_order,
     lambda m: pins.test_oracle_equals_exact_rational_dmmv(m, 8, 4, 64),
     lambda m: pins.test_oracle_equals_exact_rational_dmmv(m, 2, 3, 160),
+    pins.test_argmax_first_index_of_the_maximum,
 ]
 
 

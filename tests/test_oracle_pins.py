@@ -374,3 +374,15 @@ def test_within_tolerance_criterion(oracle_mod):
     assert ok and worst < 1.0
     ok, _ = oracle_mod.within_tolerance([1.0 + 2e-5], [1.0], [1.0])
     assert not ok
+
+
+# ------------------------------------------------------------------ argmax
+def test_argmax_first_index_of_the_maximum(oracle_mod):
+    assert oracle_mod.argmax([1.0, 3.0, 2.0]) == (1, 3.0)
+    assert oracle_mod.argmax([5.0, 5.0, 1.0])[0] == 0            # ties: the smallest index
+    assert oracle_mod.argmax([-2.0, -1.0, -1.0, -3.0])[0] == 1
+    assert oracle_mod.argmax([7.0])[0] == 0
+    assert oracle_mod.argmax(np.zeros(0))[0] == -1
+    g = np.random.default_rng(4)
+    v = g.standard_normal(10007)
+    assert oracle_mod.argmax(v)[0] == int(np.argmax(v))

@@ -415,3 +415,66 @@ def test_expert_gather2_equals_two_gathers_bitwise(fmt, rows, cols, layout):
     assert torch.isnan(ya[5]).all() and torch.isnan(yb[5]).all()
     y_ref, e_ref, _ = oracle.expert_gather(fmt, sb, per, rows, cols, idx, n_exp, xq, 0)
     check_y(yb[:5], y_ref[:5], e_ref[:5])
+
+
+# ------------------------------------------------------------ argmax epilogue
+def _argmax_case(fmt, rows, cols, layout, seed):
+    w = synth.weight_blocks(fmt, rows, cols, seed=seed)
+    xq = synth.activation_blocks(cols // 32, seed=seed + 1)
+    wd = dev(w)
+    if layout == Z.REPACKED:
+        wd = Z.repack(fmt, wd, rows, cols)
+    return w, xq, wd
+
+
+@pytest.mark.parametrize("layout", [Z.GGUF, Z.REPACKED])
+@pytest.mark.parametrize("fmt,rows,cols", [(Q4_0, 248320 // 8, 2048), (Q8_0, 5000, 4096), (Q4_0, 1, 256),
+                                           (Q8_0, 77, 512), (Q4_0, 3001, 8192)])
+def test_argmax_matches_own_logits_and_oracle(fmt, rows, cols, layout):
+    w, xq, wd = _argmax_case(fmt, rows, cols, layout, seed=rows)
+    xqd = dev(xq)
+    y = nan_out(rows)
+    Z.dmmv(fmt, wd, rows, cols, xqd, y=y, layout=layout)
+    mx = torch.full((1,), float("nan"), device="cuda")
+    idx = Z.dmmv_argmax(fmt, wd, rows, cols, xqd, max_out=mx, layout=layout)
+    torch.cuda.synchronize()
+    yh = y.cpu().numpy()
+    i = int(idx.item())
+    # the same fp32 logits: the first index of their maximum, and that value
+    assert i == int(np.argmax(yh)) and mx.item() == yh[i]
+    # against the oracle: the pick is a valid argmax within the tolerance
+    y_ref, e_ref = oracle.dmmv(fmt, w, rows, cols, xq)
+    j, _ = oracle.argmax(y_ref)
+    tol = REL * (e_ref[i] + e_ref[j]) + 2 * ABS
+    assert y_ref[i] >= y_ref[j] - tol
+
+
+def test_argmax_ties_pick_the_first_row():
+    fmt, rows, cols = Q4_0, 4000, 2048
+    w, xq, wd = _argmax_case(fmt, rows, cols, Z.GGUF, seed=9)
+    xqd = dev(xq)
+    y = Z.dmmv(fmt, wd, rows, cols, xqd)
+    torch.cuda.synchronize()
+    r = int(torch.argmax(y).item())
+    rb = cols // 32 * 18
+    w2 = w.reshape(rows, rb).copy()
+    for p in (3, 1777, 3999):             # identical copies of the maximal row, before and after it
+        w2[p] = w2[r]
+    first = min(3, r)
+    idx = Z.dmmv_argmax(fmt, dev(w2.reshape(-1)), rows, cols, xqd)
+    torch.cuda.synchronize()
+    assert int(idx.item()) == first
+
+
+def test_argmax_workspace_is_reusable_back_to_back():
+    fmt, rows, cols = Q8_0, 2048, 4096
+    outs = []
+    ws = torch.empty(Z.ARGMAX_WORKSPACE_BYTES, dtype=torch.uint8, device="cuda")
+    for seed in (1, 2, 3):
+        w, xq, wd = _argmax_case(fmt, rows, cols, Z.GGUF, seed=seed)
+        outs.append((Z.dmmv_argmax(fmt, wd, rows, cols, dev(xq), workspace=ws), wd, dev(xq)))
+    torch.cuda.synchronize()
+    for idx, wd, xqd in outs:
+        y = Z.dmmv(fmt, wd, rows, cols, xqd)
+        torch.cuda.synchronize()
+        assert int(idx.item()) == int(torch.argmax(y).item())
