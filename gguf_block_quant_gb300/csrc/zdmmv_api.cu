@@ -687,6 +687,29 @@ zdmmv_status argmax_entry(int fmt, const void *w, int layout, int64_t rows, int6
                                         static_cast<int>(ctas), argmax_out, max_out));
 }
 
+}  // namespace
+
+cudaError_t launch_argmax_reduce(const uint2 *parts, int n, int32_t *argmax_out, float *max_out, cudaStream_t st,
+                                 bool pdl) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(1, 1, 1);
+    cfg.blockDim = dim3(256, 1, 1);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, argmax_reduce_kernel, parts, n, argmax_out, max_out);
+}
+
+uint32_t *current_fault_word() {
+    const DeviceInfo *dev = nullptr;
+    return device_info(&dev) == cudaSuccess ? dev->fault : nullptr;
+}
+
+namespace {
+
 zdmmv_status dmmv_f32_entry(int fmt, const void *w, int layout, int64_t rows, int64_t cols, const float *x,
                             int batch, float *y, cudaStream_t st) {
     if (block_bytes(fmt) == 0) return ZDMMV_ERR_FORMAT;

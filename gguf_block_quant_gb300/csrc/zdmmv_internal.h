@@ -98,6 +98,12 @@ cudaError_t launch_batch_q4(const DmmvArgs &a, const BatchPlan &p, int layout, i
 cudaError_t launch_argmax_q8(const DmmvArgs &a, const TmaPlan &p, int layout, int ctas, cudaStream_t st, bool pdl);
 cudaError_t launch_argmax_q4(const DmmvArgs &a, const TmaPlan &p, int layout, int ctas, cudaStream_t st, bool pdl);
 
+// The argmax epilogue's final pass (one CTA over n partials).
+cudaError_t launch_argmax_reduce(const uint2 *parts, int n, int32_t *argmax_out, float *max_out, cudaStream_t st,
+                                 bool pdl);
+// The device fault word of the current device (nullptr on error).
+uint32_t *current_fault_word();
+
 // CTAs of the pipelined kernel that fit on one SM for this plan.
 int tma_ctas_per_sm_q8(int layout, const TmaPlan &p);
 int tma_ctas_per_sm_q4(int layout, const TmaPlan &p);

@@ -56,6 +56,7 @@ _SIGS = {
     "zdmmv_q4_0_batched": ([_vp, _int, _i64, _i64, _vp, _int, _vp, _vp], _int),
     "zdmmv_dmmv_f32": ([_int, _vp, _int, _i64, _i64, _vp, _int, _vp, _vp], _int),
     "zdmmv_dmmv_argmax": ([_int, _vp, _int, _i64, _i64, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp], _int),
+    "zdmmv_dmmv_argmax_noalloc": ([_int, _vp, _int, _i64, _i64, _vp, _vp, _vp, _vp], _int),
     "zdmmv_expert_gather": ([_int, _vp, _i64, _int, _i64, _i64, _vp, _int, _int, _vp, _i64, _vp, _vp, _vp],
                             _int),
     "zdmmv_expert_gather2": ([_int, _vp, _vp, _i64, _int, _i64, _i64, _vp, _int, _int, _vp, _i64, _vp, _vp,
@@ -200,6 +201,17 @@ def dmmv_argmax(fmt: int, w, rows: int, cols: int, xq, workspace=None, out=None,
         out = torch.empty(1, dtype=torch.int32, device=w.device)
     _call("zdmmv_dmmv_argmax", fmt, _ptr(w), layout, rows, cols, _ptr(xq), _ptr(out), _ptr(max_out),
           _ptr(workspace), _nbytes(workspace), _stream(stream))
+    return out
+
+
+def dmmv_argmax_noalloc(fmt: int, w, rows: int, cols: int, xq, out=None, max_out=None, layout: int = GGUF,
+                        stream=None):
+    """The argmax DMMV without a workspace: for callers that cannot allocate
+    device memory (see include/zdmmv.h). Overlapping calls race."""
+    if out is None:
+        out = torch.empty(1, dtype=torch.int32, device=w.device)
+    _call("zdmmv_dmmv_argmax_noalloc", fmt, _ptr(w), layout, rows, cols, _ptr(xq), _ptr(out), _ptr(max_out),
+          _stream(stream))
     return out
 
 

@@ -178,6 +178,32 @@ zdmmv_status zdmmv_dmmv_argmax(zdmmv_fmt fmt, const void *w, zdmmv_layout layout
                                int64_t cols, const void *xq, int32_t *argmax_out, float *max_out,
                                void *workspace, size_t workspace_bytes, zdmmv_stream_t stream);
 
+/* The same greedy pick as zdmmv_dmmv_argmax for callers that cannot allocate
+ * device memory: an engine that plans all device memory when it loads a model
+ * and treats any later allocation as a bug, a plugin whose host program owns
+ * every device allocation, or a decode loop that must not call cudaMalloc
+ * (which may synchronize the device). No workspace argument; the per-CTA
+ * partials go to a fixed 16 KiB array inside the library's device image
+ * (2048 slots), which every GPU that loads the library holds until the process
+ * exits. The pages have no counterpart of this entry point; it is an addition
+ * of this library.
+ *   Arguments as zdmmv_dmmv_argmax without workspace / workspace_bytes; rows
+ *   1 .. 2^31-1 (a launch never needs more than the 2048 slots), cols a
+ *   multiple of 256 and at most 8192; anything else is ERR_SHAPE.
+ *   Allocates nothing: no cudaMalloc, no cudaFree, no allocating library call.
+ *   The first call on a device looks up the array's device address
+ *   (cudaGetSymbolAddress) with that device current; make that first call
+ *   before any stream capture.
+ *   Every call shares the array and leaves the last call's partials in it
+ *   (nothing needs to start at zero: each call writes every slot it reads).
+ *   Calls that overlap on the GPU (other streams or threads) race on the array
+ *   and may return wrong results; serialize them.
+ * Errors: ERR_NULL, ERR_SHAPE, ERR_ALIGN, ERR_LAYOUT, ERR_FORMAT, ERR_CUDA. */
+zdmmv_status zdmmv_dmmv_argmax_noalloc(zdmmv_fmt fmt, const void *w, zdmmv_layout layout,
+                                       int64_t rows, int64_t cols, const void *xq,
+                                       int32_t *argmax_out, float *max_out,
+                                       zdmmv_stream_t stream);
+
 /* MoE expert gather: n matrices picked by index from a stack of n_experts
  * equally shaped matrices, all in ONE launch (routed experts are selected per
  * token by the router: "CUDA backend for ZINC", M1 list "dmmv_q4k_moe";
