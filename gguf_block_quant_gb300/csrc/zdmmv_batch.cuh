@@ -106,30 +106,48 @@ __device__ __forceinline__ void load_block_aligned(const uint8_t *base, int64_t 
     }
 }
 
+// The same from shared memory (base: shared-memory address, 4-byte aligned).
+template <int QW>
+__device__ __forceinline__ void load_block_aligned_smem(uint32_t base, int off, uint32_t (&q)[QW], float &d) {
+    const uint32_t src = base + static_cast<uint32_t>(off & ~3);
+    uint32_t w[QW + 1];
+#pragma unroll
+    for (int k = 0; k <= QW; ++k) w[k] = lds32(src + 4 * k);
+    if (off & 2) {
+        d = half_hi(w[0]);
+#pragma unroll
+        for (int k = 0; k < QW; ++k) q[k] = w[k + 1];
+    } else {
+        d = half_lo(w[0]);
+#pragma unroll
+        for (int k = 0; k < QW; ++k) q[k] = shift2(w[k], w[k + 1]);
+    }
+}
+
 // The aligned quant words and scale of block b of staged row i. GGUF blocks start
 // 0 (even b) or 2 (odd b) bytes into a word; for an even block the quant words are
 // realigned once (one byte permute per word) and then serve every vector.
 template <int FMT, int LAYOUT>
-__device__ __forceinline__ void load_wblock(const uint8_t *stage, int i, int b, int nb, int tile_rows,
+__device__ __forceinline__ void load_wblock(uint32_t stage, int i, int b, int nb, int tile_rows,
                                             uint32_t (&q)[Fmt<FMT>::kQuantBytes / 4], float &dw) {
     constexpr int kBB = Fmt<FMT>::kBlockBytes;
     constexpr int kQB = Fmt<FMT>::kQuantBytes;
     constexpr int kQW = kQB / 4;
     if constexpr (LAYOUT == kLayoutGguf) {
         // rows are 16-byte multiples, so the block's parity decides its alignment
-        load_block_aligned<kQW>(stage, static_cast<int64_t>(i) * nb * kBB + static_cast<int64_t>(b) * kBB, q, dw);
+        load_block_aligned_smem<kQW>(stage, i * nb * kBB + b * kBB, q, dw);
     } else {
-        const uint4 *src = reinterpret_cast<const uint4 *>(stage + (i * nb + b) * kQB);
+        const uint32_t src = stage + static_cast<uint32_t>((i * nb + b) * kQB);
 #pragma unroll
         for (int k = 0; k < kQB / 16; ++k) {
-            const uint4 t = src[k];
+            const uint4 t = lds128(src + 16 * k);
             q[4 * k] = t.x;
             q[4 * k + 1] = t.y;
             q[4 * k + 2] = t.z;
             q[4 * k + 3] = t.w;
         }
-        const uint16_t h = *reinterpret_cast<const uint16_t *>(stage + tile_rows * nb * kQB + (i * nb + b) * 2);
-        dw = __half2float(__ushort_as_half(h));
+        const uint32_t h = lds16(stage + static_cast<uint32_t>(tile_rows * nb * kQB + (i * nb + b) * 2));
+        dw = __half2float(__ushort_as_half(static_cast<unsigned short>(h)));
     }
 }
 
@@ -278,7 +296,7 @@ __global__ void __launch_bounds__(kTmaThreads, (VB >= 8 && FMT == kFmtQ4) ? 2 : 
             if (lane == 0) atomicOr(a.fault, 1u);
             return;
         }
-        const uint8_t *st = stage0 + static_cast<size_t>(s) * a.stage_bytes;
+        const uint32_t st = smem_addr(stage0) + static_cast<uint32_t>(s * a.stage_bytes);
         const int64_t tr0 = r0 + static_cast<int64_t>(t) * T;
         const int nr = static_cast<int>(min(static_cast<int64_t>(T), r1 - tr0));
         for (int pass = 0; pass < npass; ++pass) {

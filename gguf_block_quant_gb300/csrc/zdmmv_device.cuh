@@ -47,6 +47,27 @@ __device__ __forceinline__ uint32_t smem_addr(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// Explicit shared-memory loads (addresses from smem_addr): the compiler cannot
+// always prove that a pointer handed through the block-arithmetic helpers points
+// into shared memory, and a generic load takes the slower global-memory path.
+// They are volatile so that they are never hoisted above the barrier wait that
+// makes the data valid.
+__device__ __forceinline__ uint32_t lds32(uint32_t a) {
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ uint4 lds128(uint32_t a) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ uint32_t lds16(uint32_t a) {
+    unsigned short v;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(a));
+    return v;
+}
+
 // unsigned bytes of a times signed bytes of b, accumulated into c (int32)
 __device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
     int d;
@@ -194,6 +215,11 @@ __device__ __forceinline__ void load_x_pair_words(const uint8_t *xq, int p, uint
 #pragma unroll
     for (int k = 0; k < 17; ++k) v[k] = src[k];
 }
+// The same from activation blocks staged in shared memory at address xs.
+__device__ __forceinline__ void load_x_pair_words_smem(uint32_t xs, int p, uint32_t (&v)[17]) {
+#pragma unroll
+    for (int k = 0; k < 17; ++k) v[k] = lds32(xs + 68 * p + 4 * k);
+}
 
 // Aligned code words of the two activation blocks of a pair:
 // block A's 32 codes start at byte 2, block B's at byte 36 of the pair.
@@ -236,11 +262,11 @@ template <> struct Pair<kFmtQ8, kLayoutGguf> {
 #pragma unroll
         for (int k = 9; k < 17; ++k) sb = dp4a_ss(w[k], x[k], sb);
     }
-    // w: the pair's 17 weight words (shared memory)
-    __device__ __forceinline__ float fma_pair(const uint32_t *w, float acc) const {
+    // w: shared-memory address of the pair's 17 weight words
+    __device__ __forceinline__ float fma_pair(uint32_t w, float acc) const {
         uint32_t r[17];
 #pragma unroll
-        for (int k = 0; k < 17; ++k) r[k] = w[k];
+        for (int k = 0; k < 17; ++k) r[k] = lds32(w + 4 * k);
         int sa, sb;
         sums(r, sa, sb);
         acc = __fmaf_rn(static_cast<float>(sa), __fmul_rn(half_lo(r[0]), dxa), acc);
@@ -299,10 +325,10 @@ template <> struct Pair<kFmtQ4, kLayoutGguf> {
         sa = la + (ha >> 4);
         sb = lb + (hb >> 4);
     }
-    __device__ __forceinline__ float fma_pair(const uint32_t *w, float acc) const {
+    __device__ __forceinline__ float fma_pair(uint32_t w, float acc) const {
         uint32_t r[9];
 #pragma unroll
-        for (int k = 0; k < 9; ++k) r[k] = w[k];
+        for (int k = 0; k < 9; ++k) r[k] = lds32(w + 4 * k);
         int sa, sb;
         sums(r, sa, sb);
         acc = __fmaf_rn(static_cast<float>(sa), __fmul_rn(half_lo(r[0]), dxa), acc);
@@ -337,13 +363,12 @@ template <> struct Pair<kFmtQ8, kLayoutRepacked> {
 #pragma unroll
         for (int k = 8; k < 16; ++k) sb = dp4a_ss(wq[k], x[k], sb);
     }
-    // wq: 16 quant words (16-byte aligned); ws: the pair's scale word
-    __device__ __forceinline__ float fma_pair(const uint32_t *wq, uint32_t ws, float acc) const {
+    // wq: shared-memory address of 16 quant words (16-byte aligned); ws: the pair's scale word
+    __device__ __forceinline__ float fma_pair(uint32_t wq, uint32_t ws, float acc) const {
         uint32_t r[16];
-        const uint4 *q4 = reinterpret_cast<const uint4 *>(wq);
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-            const uint4 t = q4[k];
+            const uint4 t = lds128(wq + 16 * k);
             r[4 * k] = t.x;
             r[4 * k + 1] = t.y;
             r[4 * k + 2] = t.z;
@@ -392,12 +417,11 @@ template <> struct Pair<kFmtQ4, kLayoutRepacked> {
         sa = la + (ha >> 4);
         sb = lb + (hb >> 4);
     }
-    __device__ __forceinline__ float fma_pair(const uint32_t *wq, uint32_t ws, float acc) const {
+    __device__ __forceinline__ float fma_pair(uint32_t wq, uint32_t ws, float acc) const {
         uint32_t r[8];
-        const uint4 *q4 = reinterpret_cast<const uint4 *>(wq);
 #pragma unroll
         for (int k = 0; k < 2; ++k) {
-            const uint4 t = q4[k];
+            const uint4 t = lds128(wq + 16 * k);
             r[4 * k] = t.x;
             r[4 * k + 1] = t.y;
             r[4 * k + 2] = t.z;

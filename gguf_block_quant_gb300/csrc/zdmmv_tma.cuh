@@ -45,31 +45,28 @@ template <int FMT> struct RowGeom<FMT, kLayoutRepacked> {
 };
 
 // One lane's contribution to one row: pairs l, l+LPR, ... (fixed order).
+// stage: shared-memory address of the tile.
 template <int FMT, int LAYOUT, int LPR, int PPL>
-__device__ __forceinline__ float row_partial(const Pair<FMT, LAYOUT> (&xr)[PPL], const uint8_t *stage, int i,
+__device__ __forceinline__ float row_partial(const Pair<FMT, LAYOUT> (&xr)[PPL], uint32_t stage, int i,
                                              int tile_rows, int nb, int l) {
     const int npairs = nb >> 1;
     float acc = 0.0f;
     if constexpr (LAYOUT == kLayoutGguf) {
-        const uint8_t *row = stage + static_cast<size_t>(i) * nb * Fmt<FMT>::kBlockBytes;
+        const uint32_t row = stage + static_cast<uint32_t>(i * nb * Fmt<FMT>::kBlockBytes);
 #pragma unroll
         for (int j = 0; j < PPL; ++j) {
             const int p = l + j * LPR;
-            if (p < npairs)
-                acc = xr[j].fma_pair(reinterpret_cast<const uint32_t *>(row + p * RowGeom<FMT, LAYOUT>::kPairBytes),
-                                     acc);
+            if (p < npairs) acc = xr[j].fma_pair(row + p * RowGeom<FMT, LAYOUT>::kPairBytes, acc);
         }
     } else {
-        const uint8_t *rq = stage + static_cast<size_t>(i) * nb * Fmt<FMT>::kQuantBytes;
-        const uint8_t *rs = stage + static_cast<size_t>(tile_rows) * nb * Fmt<FMT>::kQuantBytes +
-                            static_cast<size_t>(i) * nb * 2;
+        const uint32_t rq = stage + static_cast<uint32_t>(i * nb * Fmt<FMT>::kQuantBytes);
+        const uint32_t rs = stage + static_cast<uint32_t>(tile_rows * nb * Fmt<FMT>::kQuantBytes + i * nb * 2);
 #pragma unroll
         for (int j = 0; j < PPL; ++j) {
             const int p = l + j * LPR;
             if (p < npairs) {
-                const uint32_t ws = *reinterpret_cast<const uint32_t *>(rs + 4 * p);
-                acc = xr[j].fma_pair(
-                    reinterpret_cast<const uint32_t *>(rq + p * RowGeom<FMT, LAYOUT>::kPairQuantBytes), ws, acc);
+                const uint32_t ws = lds32(rs + 4 * p);
+                acc = xr[j].fma_pair(rq + p * RowGeom<FMT, LAYOUT>::kPairQuantBytes, ws, acc);
             }
         }
     }
@@ -221,7 +218,9 @@ __global__ void __launch_bounds__(kTmaThreads, MINB) dmmv_tma_kernel(const DmmvA
     pdl_wait();               // outputs may still be read, and the activation written, by the preceding kernel
     if constexpr (FX) {
         // quantize the fp32 activation into Q8_0 blocks in shared memory: each
-        // warp takes four blocks per iteration (16-byte loads, 8 lanes per block)
+        // warp takes four blocks per iteration (16-byte loads, 8 lanes per
+        // block), kRound iterations at a time in phases (all loads, all block
+        // maxima, all scales, all codes) so independent blocks overlap
         const float *xf = a.xf + sel * a.xf_stride;
         constexpr int kWarps = kConsumerThreads / 32;
         constexpr int kRound = 8;
@@ -231,6 +230,7 @@ __global__ void __launch_bounds__(kTmaThreads, MINB) dmmv_tma_kernel(const DmmvA
         const int nquads = nb >> 2; // nb is a multiple of 8 on this path
         for (int q0 = warp; q0 < nquads; q0 += kWarps * kRound) {
             float4 v[kRound];
+            float m[kRound];
 #pragma unroll
             for (int u = 0; u < kRound; ++u) {
                 const int qd = q0 + u * kWarps;
@@ -238,16 +238,35 @@ __global__ void __launch_bounds__(kTmaThreads, MINB) dmmv_tma_kernel(const DmmvA
                                    : make_float4(0.f, 0.f, 0.f, 0.f);
             }
 #pragma unroll
+            for (int u = 0; u < kRound; ++u)
+                m[u] = fmaxf(fmaxf(fabsf(v[u].x), fabsf(v[u].y)), fmaxf(fabsf(v[u].z), fabsf(v[u].w)));
+#pragma unroll
+            for (int o = 1; o < 8; o <<= 1) {
+#pragma unroll
+                for (int u = 0; u < kRound; ++u) m[u] = fmaxf(m[u], __shfl_xor_sync(0xffffffffu, m[u], o));
+            }
+            float id[kRound];
+            unsigned short db[kRound];
+#pragma unroll
+            for (int u = 0; u < kRound; ++u) {
+                // the operations of quantize_q8_0_lane: IEEE division and reciprocal
+                const float d = __fdiv_rn(m[u], 127.0f);
+                id[u] = d != 0.0f ? __frcp_rn(d) : 0.0f;
+                db[u] = __half_as_ushort(__float2half_rn(d));
+            }
+#pragma unroll
             for (int u = 0; u < kRound; ++u) {
                 const int qd = q0 + u * kWarps;
                 if (qd < nquads) {  // warp-uniform
-                    unsigned short d_bits;
-                    const uint32_t codes = quantize_q8_0_quad(v[u], d_bits);
+                    const uint32_t c0 = static_cast<uint8_t>(static_cast<int8_t>(static_cast<int>(roundf(__fmul_rn(v[u].x, id[u])))));
+                    const uint32_t c1 = static_cast<uint8_t>(static_cast<int8_t>(static_cast<int>(roundf(__fmul_rn(v[u].y, id[u])))));
+                    const uint32_t c2 = static_cast<uint8_t>(static_cast<int8_t>(static_cast<int>(roundf(__fmul_rn(v[u].z, id[u])))));
+                    const uint32_t c3 = static_cast<uint8_t>(static_cast<int8_t>(static_cast<int>(roundf(__fmul_rn(v[u].w, id[u])))));
                     uint8_t *blk = xs + 34 * (4 * qd + sub);
                     uint16_t *dst = reinterpret_cast<uint16_t *>(blk + 2 + 4 * j);  // 2-byte aligned
-                    dst[0] = static_cast<uint16_t>(codes & 0xffffu);
-                    dst[1] = static_cast<uint16_t>(codes >> 16);
-                    if (j == 0) *reinterpret_cast<unsigned short *>(blk) = d_bits;
+                    dst[0] = static_cast<uint16_t>(c0 | (c1 << 8));
+                    dst[1] = static_cast<uint16_t>(c2 | (c3 << 8));
+                    if (j == 0) *reinterpret_cast<unsigned short *>(blk) = db[u];
                 }
             }
         }
@@ -265,7 +284,7 @@ __global__ void __launch_bounds__(kTmaThreads, MINB) dmmv_tma_kernel(const DmmvA
         const int p = l + j * LPR;
         if (p < (nb >> 1)) {
             uint32_t v[17];
-            load_x_pair_words(xs, p, v);
+            load_x_pair_words_smem(smem_addr(xs), p, v);
             xr[j].set(v);
         }
     }
@@ -278,7 +297,7 @@ __global__ void __launch_bounds__(kTmaThreads, MINB) dmmv_tma_kernel(const DmmvA
             if (lane == 0) atomicOr(a.fault, 1u);
             return;
         }
-        const uint8_t *st = stage0 + static_cast<size_t>(s) * a.stage_bytes;
+        const uint32_t st = smem_addr(stage0) + static_cast<uint32_t>(s * a.stage_bytes);
         const int64_t tr0 = r0 + static_cast<int64_t>(t) * T;
         const int nr = static_cast<int>(min(static_cast<int64_t>(T), r1 - tr0));
         // kRowsIlp rows per row group at a time: independent loads, dot chains and
