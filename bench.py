@@ -66,10 +66,14 @@ def peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+# the sources that define the dense pipelined DMMV kernel (its code and arguments)
+DENSE_KERNEL_SOURCES = ("zdmmv_device.cuh", "zdmmv_internal.h", "zdmmv_tma.cuh", "zdmmv_tma_q4.cu")
+
+
 def kernel_sources_sha() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "gguf_block_quant_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
+    for f in DENSE_KERNEL_SOURCES:
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]
