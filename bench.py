@@ -380,16 +380,31 @@ def measure_moe(steps, warmup, world, device, eager, l2_bytes):
             Z.expert_gather(Z.Q8_0, d, dn, m.hidden, m.ffn, idx, m.n_slots, xqd, (m.ffn // 32) * 34, y=yd,
                             status=st)
 
+    h = torch.empty(m.n_sel, m.ffn, device="cuda")
+
+    def step_swiglu():
+        for l in range(layers):
+            g, u, d = stacks[l % n_sets]
+            idx = idxs[l % len(idxs)]
+            Z.expert_swiglu(Z.Q4_0, g, u, m.ffn, m.hidden, xq, idx=idx, expert_stride=gu, n_experts=m.n_slots,
+                            h=h, status=st)
+            Z.expert_gather(Z.Q8_0, d, dn, m.hidden, m.ffn, idx, m.n_slots, xqd, (m.ffn // 32) * 34, y=yd,
+                            status=st)
+
     nbytes = m.algorithmic_bytes()
+    # the SwiGLU epilogue writes h instead of the gate and up outputs
+    nbytes_swiglu = nbytes - m.n_sel * m.ffn * 4
     out = {"layers": layers, "algorithmic_bytes": nbytes,
            "note": "touched experts differ per layer; stack copies alternate (some L2 reuse possible)"}
-    for name, fn, launches in (("three_launch", step3, 3), ("gate_up_fused", step2, 2)):
+    for name, fn, launches, nb_ in (("three_launch", step3, 3, nbytes), ("gate_up_fused", step2, 2, nbytes),
+                                    ("gate_up_swiglu", step_swiglu, 2, nbytes_swiglu)):
         run = graph_or_eager(fn, eager)
         ms, _ = time_fn(run, steps, warmup, world, device)
         per_layer = ms / 1e3 / (steps * layers)
-        out[name] = {"us_per_token_layer": per_layer * 1e6, "gbs": nbytes / per_layer / 1e9,
+        out[name] = {"us_per_token_layer": per_layer * 1e6, "gbs": nb_ / per_layer / 1e9,
+                     "algorithmic_bytes": nb_,
                      "rows_per_s": m.n_sel * (2 * m.ffn + m.hidden) / per_layer, "launches_per_layer": launches}
-    out["gbs"] = max(out["three_launch"]["gbs"], out["gate_up_fused"]["gbs"])
+    out["gbs"] = max(out[k]["gbs"] for k in ("three_launch", "gate_up_fused", "gate_up_swiglu"))
     return out
 
 

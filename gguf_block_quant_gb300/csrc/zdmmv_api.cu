@@ -133,7 +133,7 @@ bool tma_shape_ok(int fmt, int64_t cols) {
     return nb % 8 == 0 && nb / 2 <= 128;
 }
 
-TmaPlan tma_plan(int fmt, int layout, int64_t cols) {
+TmaPlan tma_plan(int fmt, int layout, int64_t cols, int halves) {
     (void)layout;
     TmaPlan p{};
     const int nb = static_cast<int>(cols / kQK);
@@ -151,7 +151,8 @@ TmaPlan tma_plan(int fmt, int layout, int64_t cols) {
     }
     const int rows_par = kConsumerThreads / p.lpr;
     const int row_bytes = nb * block_bytes(fmt);
-    const int stage_target = stage_target_bytes();
+    // a pair stage (halves = 2) holds the same rows of two matrices
+    const int stage_target = stage_target_bytes() / halves;
     // a tile is a whole number of passes of the row groups (kTmaRowsIlp rows each
     // when that fits the stage target)
     int unit_rows = rows_par * kTmaRowsIlp;
@@ -159,7 +160,7 @@ TmaPlan tma_plan(int fmt, int layout, int64_t cols) {
     const int unit = unit_rows * row_bytes;
     const int m = unit >= stage_target ? 1 : stage_target / unit;
     p.tile_rows = unit_rows * m;
-    p.stage_bytes = static_cast<int>(round_up(static_cast<int64_t>(p.tile_rows) * row_bytes, 128));
+    p.stage_bytes = halves * static_cast<int>(round_up(static_cast<int64_t>(p.tile_rows) * row_bytes, 128));
     p.x_bytes_padded = static_cast<int>(round_up(static_cast<int64_t>(nb) * 34, 128));
     p.stages = 4;
     while (p.stages > 2 && kBarrierBytes + p.x_bytes_padded + p.stages * p.stage_bytes > kSmemPerCtaTarget)
@@ -362,7 +363,15 @@ __global__ void __launch_bounds__(256) dmmv_plain_kernel(const DmmvArgs a) {
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-        if (lane == 0) y[static_cast<int64_t>(v) * a.rows + row] = acc;
+        if (lane == 0) {
+            float *dst = y + static_cast<int64_t>(v) * a.rows + row;
+            if (a.accumulate) {
+                const float scale = a.gate != nullptr ? 1.0f / (1.0f + expf(-*a.gate)) : 1.0f;
+                *dst = __fmaf_rn(scale, acc, *dst);
+            } else {
+                *dst = acc;
+            }
+        }
     }
 }
 
@@ -710,6 +719,91 @@ uint32_t *current_fault_word() {
 
 namespace {
 
+zdmmv_status acc_entry(int fmt, const void *w, int layout, int64_t rows, int64_t cols, const void *xq,
+                       const float *gate, float *y, cudaStream_t st) {
+    zdmmv_status s = check_matrix(fmt, w, layout, rows, cols, xq, y);
+    if (s != ZDMMV_OK) return s;
+    if (rows == 0) return ZDMMV_OK;
+    if (gate && !aligned(gate, 4)) return ZDMMV_ERR_ALIGN;
+    const DeviceInfo *dev = nullptr;
+    if (device_info(&dev) != cudaSuccess) return ZDMMV_ERR_CUDA;
+    DmmvArgs a{};
+    a.w = static_cast<const uint8_t *>(w);
+    a.xq = static_cast<const uint8_t *>(xq);
+    a.y = y;
+    a.y_stride = rows;
+    a.rows = rows;
+    a.nb = static_cast<int32_t>(cols / kQK);
+    a.batch = 1;
+    a.gate = gate;
+    a.accumulate = 1;
+    a.fault = dev->fault;
+    if (!tma_shape_ok(fmt, cols)) return from_cuda(launch_plain(fmt, layout, a, 1, st));
+    const TmaPlan p = tma_plan(fmt, layout, cols);
+    a.tile_rows = p.tile_rows;
+    a.stage_bytes = p.stage_bytes;
+    a.x_bytes_padded = p.x_bytes_padded;
+    int per_sm = fmt == kFmtQ8 ? tma_ctas_per_sm_q8(layout, p) : tma_ctas_per_sm_q4(layout, p);
+    const int want = ctas_per_sm_per_launch(rows * a.nb * static_cast<int64_t>(block_bytes(fmt)));
+    if (per_sm > want) per_sm = want;
+    int64_t ctas = static_cast<int64_t>(dev->sms) * per_sm;
+    if (ctas > rows) ctas = rows;
+    if (ctas > 65535) ctas = 65535;
+    return from_cuda(fmt == kFmtQ8 ? launch_acc_q8(a, p, layout, static_cast<int>(ctas), st, pdl_enabled())
+                                   : launch_acc_q4(a, p, layout, static_cast<int>(ctas), st, pdl_enabled()));
+}
+
+zdmmv_status swiglu_entry(int fmt, const void *w_gate, const void *w_up, int64_t expert_stride_bytes, int layout,
+                          int64_t rows, int64_t cols, const int32_t *idx, int n, int n_experts, const void *xq,
+                          int64_t xq_stride_bytes, float *h, int32_t *status_dev, cudaStream_t st) {
+    zdmmv_status s = check_matrix(fmt, w_gate, layout, rows, cols, xq, h);
+    if (s != ZDMMV_OK) return s;
+    if (!tma_shape_ok(fmt, cols)) return ZDMMV_ERR_SHAPE;
+    if (n < 0 || n > 65535 || (!idx && n > 1) || n_experts < 0) return ZDMMV_ERR_SHAPE;
+    if (n == 0 || rows == 0) return ZDMMV_OK;
+    if (!w_up) return ZDMMV_ERR_NULL;
+    if (!aligned(w_up, 16) || (idx && !aligned(idx, 4)) || (status_dev && !aligned(status_dev, 4)))
+        return ZDMMV_ERR_ALIGN;
+    const int64_t nb = cols / kQK;
+    const int64_t mat_bytes = rows * nb * block_bytes(fmt);
+    if (expert_stride_bytes < 0 || xq_stride_bytes < 0) return ZDMMV_ERR_SHAPE;
+    if (idx && n_experts > 1 && expert_stride_bytes < mat_bytes) return ZDMMV_ERR_SHAPE;
+    if (xq_stride_bytes != 0 && xq_stride_bytes < nb * 34) return ZDMMV_ERR_SHAPE;
+    if (expert_stride_bytes % 16 || xq_stride_bytes % 16) return ZDMMV_ERR_ALIGN;
+    const DeviceInfo *dev = nullptr;
+    if (device_info(&dev) != cudaSuccess) return ZDMMV_ERR_CUDA;
+    DmmvArgs a{};
+    a.w = static_cast<const uint8_t *>(w_gate);
+    a.w_b = static_cast<const uint8_t *>(w_up);
+    a.slots_a = n;
+    a.expert_stride = idx ? expert_stride_bytes : 0;
+    a.idx = idx;
+    a.n_experts = n_experts;
+    a.status = status_dev;
+    a.xq = static_cast<const uint8_t *>(xq);
+    a.xq_stride = xq_stride_bytes;
+    a.y = h;
+    a.y_stride = rows;
+    a.rows = rows;
+    a.nb = static_cast<int32_t>(nb);
+    a.batch = 1;
+    a.fault = dev->fault;
+    const TmaPlan p = tma_plan(fmt, layout, cols, 2);
+    a.tile_rows = p.tile_rows;
+    a.stage_bytes = p.stage_bytes;
+    a.x_bytes_padded = p.x_bytes_padded;
+    int per_sm = fmt == kFmtQ8 ? swiglu_ctas_per_sm_q8(layout, p) : swiglu_ctas_per_sm_q4(layout, p);
+    const int want = ctas_per_sm_per_launch(2 * mat_bytes * n);
+    if (per_sm > want) per_sm = want;
+    int64_t ctas = static_cast<int64_t>(dev->sms) * per_sm / n;
+    if (ctas < 1) ctas = 1;
+    if (ctas > rows) ctas = rows;
+    if (ctas > 65535) ctas = 65535;
+    return from_cuda(fmt == kFmtQ8
+                         ? launch_swiglu_q8(a, p, layout, static_cast<int>(ctas), n, st, pdl_enabled())
+                         : launch_swiglu_q4(a, p, layout, static_cast<int>(ctas), n, st, pdl_enabled()));
+}
+
 zdmmv_status dmmv_f32_entry(int fmt, const void *w, int layout, int64_t rows, int64_t cols, const float *x,
                             int batch, float *y, cudaStream_t st) {
     if (block_bytes(fmt) == 0) return ZDMMV_ERR_FORMAT;
@@ -831,6 +925,19 @@ zdmmv_status zdmmv_dmmv_argmax(zdmmv_fmt fmt, const void *w, zdmmv_layout layout
                                size_t workspace_bytes, zdmmv_stream_t stream) {
     return argmax_entry(fmt, w, layout, rows, cols, xq, argmax_out, max_out, workspace, workspace_bytes,
                         reinterpret_cast<cudaStream_t>(stream));
+}
+
+zdmmv_status zdmmv_expert_swiglu(zdmmv_fmt fmt, const void *w_gate, const void *w_up, int64_t expert_stride_bytes,
+                                 zdmmv_layout layout, int64_t rows, int64_t cols, const int32_t *idx, int n,
+                                 int n_experts, const void *xq, int64_t xq_stride_bytes, float *h,
+                                 int32_t *status_dev, zdmmv_stream_t stream) {
+    return swiglu_entry(fmt, w_gate, w_up, expert_stride_bytes, layout, rows, cols, idx, n, n_experts, xq,
+                        xq_stride_bytes, h, status_dev, reinterpret_cast<cudaStream_t>(stream));
+}
+
+zdmmv_status zdmmv_dmmv_acc(zdmmv_fmt fmt, const void *w, zdmmv_layout layout, int64_t rows, int64_t cols,
+                            const void *xq, const float *gate, float *y, zdmmv_stream_t stream) {
+    return acc_entry(fmt, w, layout, rows, cols, xq, gate, y, reinterpret_cast<cudaStream_t>(stream));
 }
 
 size_t zdmmv_repacked_bytes(zdmmv_fmt fmt, int64_t rows, int64_t cols) {

@@ -33,6 +33,8 @@ struct DmmvArgs {
     int32_t stage_bytes;     // shared-memory bytes per stage (pipelined kernel)
     int32_t x_bytes_padded;  // shared-memory bytes of the staged activation
     uint2 *argmax_parts;     // argmax epilogue: per-CTA (max bits, row), or nullptr
+    const float *gate;       // accumulate epilogue: device scalar g, y += sigmoid(g) * W.x; nullptr: y += W.x
+    int32_t accumulate;      // plain kernel: accumulate epilogue instead of store
 };
 
 // Most CTAs an argmax launch uses (its workspace holds one 8-byte partial each).
@@ -77,7 +79,7 @@ inline cudaError_t raise_dynamic_smem_limit(const void *fn, int dev) {
 
 // Whether the pipelined kernel takes this shape, and its plan.
 bool tma_shape_ok(int fmt, int64_t cols);
-TmaPlan tma_plan(int fmt, int layout, int64_t cols);
+TmaPlan tma_plan(int fmt, int layout, int64_t cols, int halves = 1);
 
 // Launchers of the pipelined kernel (one translation unit per format).
 // fused_x: the kernel quantizes the fp32 activation a.xf itself (no a.xq).
@@ -97,6 +99,18 @@ cudaError_t launch_batch_q4(const DmmvArgs &a, const BatchPlan &p, int layout, i
 // The pipelined kernel with the argmax epilogue (no y written; per-CTA partials).
 cudaError_t launch_argmax_q8(const DmmvArgs &a, const TmaPlan &p, int layout, int ctas, cudaStream_t st, bool pdl);
 cudaError_t launch_argmax_q4(const DmmvArgs &a, const TmaPlan &p, int layout, int ctas, cudaStream_t st, bool pdl);
+
+// The pipelined kernel with the accumulate epilogue (y += s * W.x).
+cudaError_t launch_acc_q8(const DmmvArgs &a, const TmaPlan &p, int layout, int ctas, cudaStream_t st, bool pdl);
+cudaError_t launch_acc_q4(const DmmvArgs &a, const TmaPlan &p, int layout, int ctas, cudaStream_t st, bool pdl);
+
+// The pipelined kernel with the SwiGLU pair epilogue (a.w gate, a.w_b up).
+cudaError_t launch_swiglu_q8(const DmmvArgs &a, const TmaPlan &p, int layout, int ctas_per_slot, int slots,
+                             cudaStream_t st, bool pdl);
+cudaError_t launch_swiglu_q4(const DmmvArgs &a, const TmaPlan &p, int layout, int ctas_per_slot, int slots,
+                             cudaStream_t st, bool pdl);
+int swiglu_ctas_per_sm_q8(int layout, const TmaPlan &p);
+int swiglu_ctas_per_sm_q4(int layout, const TmaPlan &p);
 
 // The argmax epilogue's final pass (one CTA over n partials).
 cudaError_t launch_argmax_reduce(const uint2 *parts, int n, int32_t *argmax_out, float *max_out, cudaStream_t st,

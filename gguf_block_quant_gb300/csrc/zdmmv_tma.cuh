@@ -73,29 +73,47 @@ __device__ __forceinline__ float row_partial(const Pair<FMT, LAYOUT> (&xr)[PPL],
     return acc;
 }
 
-// Issue the bulk copy (or copies) of tile t into stage s.
+// Bytes of tile t of a CTA's row range [r0, r1).
+template <int FMT>
+__device__ __forceinline__ uint32_t tile_bytes(const DmmvArgs &a, int64_t r0, int64_t r1, int t) {
+    const int64_t tr0 = r0 + static_cast<int64_t>(t) * a.tile_rows;
+    const int nr = static_cast<int>(min(static_cast<int64_t>(a.tile_rows), r1 - tr0));
+    return static_cast<uint32_t>(nr) * static_cast<uint32_t>(a.nb) * Fmt<FMT>::kBlockBytes;
+}
+
+// Bulk copy (or copies, repacked layout) of tile t of matrix w into dst,
+// completing on bar; the caller has already announced the bytes.
 template <int FMT, int LAYOUT>
-__device__ __forceinline__ void issue_tile(const DmmvArgs &a, const uint8_t *w, int64_t r0, int64_t r1, int t, int s,
-                                           uint8_t *stage0, uint64_t *full, uint64_t pol) {
+__device__ __forceinline__ void copy_tile(const DmmvArgs &a, const uint8_t *w, int64_t r0, int64_t r1, int t,
+                                          uint8_t *dst, uint64_t *bar, uint64_t pol) {
     constexpr int kBB = Fmt<FMT>::kBlockBytes;
     constexpr int kQB = Fmt<FMT>::kQuantBytes;
     const int T = a.tile_rows;
     const int nb = a.nb;
     const int64_t tr0 = r0 + static_cast<int64_t>(t) * T;
     const int nr = static_cast<int>(min(static_cast<int64_t>(T), r1 - tr0));
-    uint8_t *dst = stage0 + static_cast<size_t>(s) * a.stage_bytes;
     if constexpr (LAYOUT == kLayoutGguf) {
-        const uint32_t bytes = static_cast<uint32_t>(nr) * static_cast<uint32_t>(nb) * kBB;
-        mbar_arrive_expect_tx(&full[s], bytes);
-        bulk_copy_g2s(dst, w + tr0 * nb * kBB, bytes, &full[s], pol);
+        bulk_copy_g2s(dst, w + tr0 * nb * kBB, static_cast<uint32_t>(nr) * static_cast<uint32_t>(nb) * kBB, bar, pol);
     } else {
         const uint32_t qbytes = static_cast<uint32_t>(nr) * static_cast<uint32_t>(nb) * kQB;
         const uint32_t sbytes = static_cast<uint32_t>(nr) * static_cast<uint32_t>(nb) * 2u;
-        mbar_arrive_expect_tx(&full[s], qbytes + sbytes);
-        bulk_copy_g2s(dst, w + tr0 * nb * kQB, qbytes, &full[s], pol);
-        bulk_copy_g2s(dst + static_cast<size_t>(T) * nb * kQB, w + a.rows * nb * kQB + tr0 * nb * 2, sbytes,
-                      &full[s], pol);
+        bulk_copy_g2s(dst, w + tr0 * nb * kQB, qbytes, bar, pol);
+        bulk_copy_g2s(dst + static_cast<size_t>(T) * nb * kQB, w + a.rows * nb * kQB + tr0 * nb * 2, sbytes, bar,
+                      pol);
     }
+}
+
+// Issue tile t into stage s (and, with a second matrix w2, the same rows of w2
+// into the stage's second half).
+template <int FMT, int LAYOUT>
+__device__ __forceinline__ void issue_tile(const DmmvArgs &a, const uint8_t *w, int64_t r0, int64_t r1, int t, int s,
+                                           uint8_t *stage0, uint64_t *full, uint64_t pol,
+                                           const uint8_t *w2 = nullptr) {
+    uint8_t *dst = stage0 + static_cast<size_t>(s) * a.stage_bytes;
+    const uint32_t bytes = tile_bytes<FMT>(a, r0, r1, t);
+    mbar_arrive_expect_tx(&full[s], w2 ? 2 * bytes : bytes);
+    copy_tile<FMT, LAYOUT>(a, w, r0, r1, t, dst, &full[s], pol);
+    if (w2) copy_tile<FMT, LAYOUT>(a, w2, r0, r1, t, dst + a.stage_bytes / 2, &full[s], pol);
 }
 
 __device__ __forceinline__ void consumer_barrier() {
@@ -112,7 +130,12 @@ __device__ __forceinline__ bool argmax_better(float v, int row, float bv, int br
 
 // EPI = 0: store y. EPI = 1 (argmax epilogue): keep each row group's running
 // (max, first row) in registers, reduce over the CTA and store one 8-byte partial
-// per CTA in a.argmax_parts; no y is written.
+// per CTA in a.argmax_parts; no y is written. EPI = 2 (accumulate epilogue):
+// y = fma(s, W.x, y) with s = sigmoid(*a.gate), or s = 1 without a gate.
+// EPI = 3 (SwiGLU pair): a.w is the gate matrix (stack) and a.w_b the up matrix
+// (stack) of the same shape; each stage holds the tile's gate rows then the same
+// rows of up, the row group computes a gate row and its up row as its two rows
+// in flight, and y = silu(gate . x) * (up . x) is stored.
 template <int FMT, int LAYOUT, int LPR, int PPL, int STAGES, int MINB, bool FX, int EPI = 0>
 __global__ void __launch_bounds__(kTmaThreads, MINB) dmmv_tma_kernel(const DmmvArgs a) {
     using P = Pair<FMT, LAYOUT>;
@@ -140,10 +163,11 @@ __global__ void __launch_bounds__(kTmaThreads, MINB) dmmv_tma_kernel(const DmmvA
 
     // a second stack (e.g. the up projections next to the gates) takes the slots
     // from slots_a on, with the same selected experts and activations
-    const bool second = a.w_b != nullptr && slot >= a.slots_a;
+    const bool second = EPI != 3 && a.w_b != nullptr && slot >= a.slots_a;
     const int sel = second ? slot - a.slots_a : slot;
     float *y = (second ? a.y_b : a.y) + sel * a.y_stride;
     const uint8_t *w = second ? a.w_b : a.w;
+    const uint8_t *w_up = EPI == 3 ? a.w_b : nullptr;  // SwiGLU pair: the up matrix
     if (a.idx != nullptr) {
         pdl_wait();  // the index list may be written by the preceding kernel
         const int e = a.idx[sel];
@@ -153,6 +177,7 @@ __global__ void __launch_bounds__(kTmaThreads, MINB) dmmv_tma_kernel(const DmmvA
             return;
         }
         w += static_cast<int64_t>(e) * a.expert_stride;
+        if (EPI == 3) w_up += static_cast<int64_t>(e) * a.expert_stride;
     }
     if (r1 <= r0) {
         if constexpr (EPI == 1) {
@@ -181,7 +206,7 @@ __global__ void __launch_bounds__(kTmaThreads, MINB) dmmv_tma_kernel(const DmmvA
         // Weights are read-only parameters: the first STAGES tiles are streamed
         // before waiting for the preceding kernel, overlapping its tail.
         const int npre = ntiles < STAGES ? ntiles : STAGES;
-        for (int t = 0; t < npre; ++t) issue_tile<FMT, LAYOUT>(a, w, r0, r1, t, t, stage0, full, wpol);
+        for (int t = 0; t < npre; ++t) issue_tile<FMT, LAYOUT>(a, w, r0, r1, t, t, stage0, full, wpol, w_up);
         int issued = npre;
         pdl_wait();
         if constexpr (!FX) {
@@ -197,7 +222,7 @@ __global__ void __launch_bounds__(kTmaThreads, MINB) dmmv_tma_kernel(const DmmvA
                 break;
             }
             fence_proxy_async_smem();
-            issue_tile<FMT, LAYOUT>(a, w, r0, r1, t, s, stage0, full, wpol);
+            issue_tile<FMT, LAYOUT>(a, w, r0, r1, t, s, stage0, full, wpol, w_up);
             issued = t + 1;
         }
         if (!ok) atomicOr(a.fault, 1u);
@@ -289,6 +314,10 @@ __global__ void __launch_bounds__(kTmaThreads, MINB) dmmv_tma_kernel(const DmmvA
         }
     }
 
+    float scale = 1.0f;  // accumulate epilogue: the gate's sigmoid
+    if constexpr (EPI == 2) {
+        if (a.gate != nullptr) scale = 1.0f / (1.0f + expf(-*a.gate));
+    }
     float best = 0.0f;  // argmax epilogue: this row group's running maximum and its row
     int best_row = -1;
     for (int t = 0; t < ntiles; ++t) {
@@ -300,6 +329,27 @@ __global__ void __launch_bounds__(kTmaThreads, MINB) dmmv_tma_kernel(const DmmvA
         const uint32_t st = smem_addr(stage0) + static_cast<uint32_t>(s * a.stage_bytes);
         const int64_t tr0 = r0 + static_cast<int64_t>(t) * T;
         const int nr = static_cast<int>(min(static_cast<int64_t>(T), r1 - tr0));
+        if constexpr (EPI == 3) {
+            // a gate row and the same up row in flight; then silu(gate) * up
+            const uint32_t st_up = st + static_cast<uint32_t>(a.stage_bytes / 2);
+            for (int base = 0; base < nr; base += kRowsPar) {
+                const int i = base + g;
+                float gv = 0.0f, uv = 0.0f;
+                if (i < nr) {
+                    gv = row_partial<FMT, LAYOUT, LPR, PPL>(xr, st, i, T, nb, l);
+                    uv = row_partial<FMT, LAYOUT, LPR, PPL>(xr, st_up, i, T, nb, l);
+                }
+#pragma unroll
+                for (int o = LPR / 2; o > 0; o >>= 1) {
+                    gv += __shfl_xor_sync(0xffffffffu, gv, o);
+                    uv += __shfl_xor_sync(0xffffffffu, uv, o);
+                }
+                if (l == 0 && i < nr) y[tr0 + i] = __fmul_rn(__fdiv_rn(gv, 1.0f + expf(-gv)), uv);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[s]);
+            continue;
+        }
         // kRowsIlp rows per row group at a time: independent loads, dot chains and
         // shuffle trees interleave; every row still gets the same reduction tree
         for (int base = 0; base < nr; base += kRowsPar * kRowsIlp) {
@@ -319,6 +369,8 @@ __global__ void __launch_bounds__(kTmaThreads, MINB) dmmv_tma_kernel(const DmmvA
                 const int i = base + r * kRowsPar + g;
                 if constexpr (EPI == 0) {
                     if (l == 0 && i < nr) y[tr0 + i] = acc[r];
+                } else if constexpr (EPI == 2) {
+                    if (l == 0 && i < nr) y[tr0 + i] = __fmaf_rn(scale, acc[r], y[tr0 + i]);
                 } else {
                     // rows reach a row group in increasing order: a strictly larger value replaces
                     if (i < nr && (best_row < 0 || acc[r] > best)) {
@@ -451,14 +503,20 @@ cudaError_t launch_tma_fmt(const DmmvArgs &a, const TmaPlan &p, int layout, bool
     return with_variant<FMT, kLayoutRepacked, false>(p, go);
 }
 
-template <int FMT>
-cudaError_t launch_argmax_fmt(const DmmvArgs &a, const TmaPlan &p, int layout, int ctas, cudaStream_t st, bool pdl) {
-    auto go = [&](auto inst) { return decltype(inst)::launch(a, p, ctas, 1, st, pdl); };
-    if (layout == kLayoutGguf) return with_variant<FMT, kLayoutGguf, false, 1>(p, go);
-    return with_variant<FMT, kLayoutRepacked, false, 1>(p, go);
+template <int FMT, int EPI>
+cudaError_t launch_epi_fmt(const DmmvArgs &a, const TmaPlan &p, int layout, int ctas, cudaStream_t st, bool pdl,
+                           int slots = 1) {
+    auto go = [&](auto inst) { return decltype(inst)::launch(a, p, ctas, slots, st, pdl); };
+    if (layout == kLayoutGguf) return with_variant<FMT, kLayoutGguf, false, EPI>(p, go);
+    return with_variant<FMT, kLayoutRepacked, false, EPI>(p, go);
 }
 
 template <int FMT>
+cudaError_t launch_argmax_fmt(const DmmvArgs &a, const TmaPlan &p, int layout, int ctas, cudaStream_t st, bool pdl) {
+    return launch_epi_fmt<FMT, 1>(a, p, layout, ctas, st, pdl);
+}
+
+template <int FMT, int EPI = 0>
 int tma_ctas_per_sm_fmt(int layout, const TmaPlan &p) {
     int occ = 1;
     auto q = [&](auto inst) {
@@ -466,9 +524,9 @@ int tma_ctas_per_sm_fmt(int layout, const TmaPlan &p) {
         return cudaSuccess;
     };
     if (layout == kLayoutGguf)
-        (void)with_variant<FMT, kLayoutGguf, false>(p, q);
+        (void)with_variant<FMT, kLayoutGguf, false, EPI>(p, q);
     else
-        (void)with_variant<FMT, kLayoutRepacked, false>(p, q);
+        (void)with_variant<FMT, kLayoutRepacked, false, EPI>(p, q);
     return occ;
 }
 

@@ -55,12 +55,15 @@ _SIGS = {
     "zdmmv_q8_0_batched": ([_vp, _int, _i64, _i64, _vp, _int, _vp, _vp], _int),
     "zdmmv_q4_0_batched": ([_vp, _int, _i64, _i64, _vp, _int, _vp, _vp], _int),
     "zdmmv_dmmv_f32": ([_int, _vp, _int, _i64, _i64, _vp, _int, _vp, _vp], _int),
+    "zdmmv_dmmv_acc": ([_int, _vp, _int, _i64, _i64, _vp, _vp, _vp, _vp], _int),
     "zdmmv_dmmv_argmax": ([_int, _vp, _int, _i64, _i64, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp], _int),
     "zdmmv_dmmv_argmax_noalloc": ([_int, _vp, _int, _i64, _i64, _vp, _vp, _vp, _vp], _int),
     "zdmmv_expert_gather": ([_int, _vp, _i64, _int, _i64, _i64, _vp, _int, _int, _vp, _i64, _vp, _vp, _vp],
                             _int),
     "zdmmv_expert_gather2": ([_int, _vp, _vp, _i64, _int, _i64, _i64, _vp, _int, _int, _vp, _i64, _vp, _vp,
                               _vp, _vp], _int),
+    "zdmmv_expert_swiglu": ([_int, _vp, _vp, _i64, _int, _i64, _i64, _vp, _int, _int, _vp, _i64, _vp, _vp,
+                             _vp], _int),
     "zdmmv_repacked_bytes": ([_int, _i64, _i64], ctypes.c_size_t),
     "zdmmv_repack": ([_int, _vp, _i64, _i64, _vp, ctypes.c_size_t, _vp], _int),
     "zdmmv_host_step_workspace_bytes": ([_i64, _i64, _int], ctypes.c_size_t),
@@ -192,6 +195,12 @@ def dmmv_f32(fmt: int, w, rows: int, cols: int, x, batch: int = 1, y=None, layou
     return y
 
 
+def dmmv_acc(fmt: int, w, rows: int, cols: int, xq, y, gate=None, layout: int = GGUF, stream=None):
+    """y += s * W.x in place, s = sigmoid(gate[0]) for a device gate scalar, else 1."""
+    _call("zdmmv_dmmv_acc", fmt, _ptr(w), layout, rows, cols, _ptr(xq), _ptr(gate), _ptr(y), _stream(stream))
+    return y
+
+
 def dmmv_argmax(fmt: int, w, rows: int, cols: int, xq, workspace=None, out=None, max_out=None,
                 layout: int = GGUF, stream=None):
     """Index (int32 device tensor [1]) of the largest of W.x, without writing W.x."""
@@ -238,6 +247,18 @@ def expert_gather2(fmt: int, w_stack_a, w_stack_b, expert_stride: int, rows: int
     _call("zdmmv_expert_gather2", fmt, _ptr(w_stack_a), _ptr(w_stack_b), expert_stride, layout, rows, cols,
           _ptr(idx), n, n_experts, _ptr(xq), xq_stride, _ptr(y_a), _ptr(y_b), _ptr(status), _stream(stream))
     return y_a, y_b
+
+
+def expert_swiglu(fmt: int, w_gate, w_up, rows: int, cols: int, xq, idx=None, expert_stride: int = 0,
+                  n_experts: int = 0, xq_stride: int = 0, h=None, status=None, layout: int = GGUF, stream=None):
+    """h[k] = silu(G_idx[k] . x_k) * (U_idx[k] . x_k) in one launch; idx=None: one gate/up pair."""
+    if idx is not None and idx.dtype != torch.int32:
+        raise ValueError("expert_swiglu: idx must be int32")
+    n = 1 if idx is None else idx.numel()
+    h = _out(h, (n, rows), w_gate.device)
+    _call("zdmmv_expert_swiglu", fmt, _ptr(w_gate), _ptr(w_up), expert_stride, layout, rows, cols, _ptr(idx), n,
+          n_experts, _ptr(xq), xq_stride, _ptr(h), _ptr(status), _stream(stream))
+    return h
 
 
 def repacked_bytes(fmt: int, rows: int, cols: int) -> int:

@@ -156,6 +156,51 @@ zdmmv_status zdmmv_dmmv_f32(zdmmv_fmt fmt, const void *w, zdmmv_layout layout, i
                             int64_t cols, const float *x, int batch, float *y,
                             zdmmv_stream_t stream);
 
+/* Accumulate epilogue: y[r] = y[r] + s * (W.x)[r], one fused fma per row, with
+ * s = 1 when gate is NULL (the templated DMMV's "accumulate mode") or
+ * s = sigmoid(*gate) = 1/(1 + exp(-*gate)) for a device fp32 gate scalar (the
+ * shared expert's "sigmoid_scale_acc"; both in "CUDA backend for ZINC",
+ * "5. The target model & milestone ordering", M1). The gate and y may be
+ * written by the preceding kernel in the stream.
+ *   fmt, w, layout, rows, cols, xq   as zdmmv_q8_0 (any width that is a
+ *                                    multiple of 32).
+ *   gate   nullable device float[1].
+ *   y      device fp32 [rows], read and written.
+ * Errors: as zdmmv_q8_0, plus ERR_FORMAT. */
+zdmmv_status zdmmv_dmmv_acc(zdmmv_fmt fmt, const void *w, zdmmv_layout layout, int64_t rows,
+                            int64_t cols, const void *xq, const float *gate, float *y,
+                            zdmmv_stream_t stream);
+
+/* Gate and up projections of the selected experts with the SwiGLU epilogue,
+ * in ONE launch: h[k][r] = silu(G_{idx[k]}.x_k)[r] * (U_{idx[k]}.x_k)[r] with
+ * silu(g) = g / (1 + exp(-g)). The MoE step runs the gate/up DMMV and then
+ * swiglu ("CUDA backend for ZINC", "5. The target model & milestone ordering",
+ * M1), the plan fuses gate and up into one launch (M3,
+ * "dmmv_*_fused_gate_up*"), and the habr article counts the separate SiLU and
+ * multiply passes as avoidable traffic ("Fused операции"). Each CTA streams the
+ * same row tile of both matrices into one pipeline stage, so the two dot
+ * products of a row are formed side by side and only h is written.
+ *   fmt, layout, rows, cols  as zdmmv_q8_0; cols must be a multiple of 256 and
+ *                            at most 8192 (else ERR_SHAPE).
+ *   w_gate, w_up   device stacks of the same shape: expert e's matrices start at
+ *                  w_gate + e*expert_stride_bytes and w_up + e*expert_stride_bytes
+ *                  (16-byte multiple). With idx == NULL they are one gate and one
+ *                  up matrix (a dense FFN), n must be 1 and expert_stride_bytes
+ *                  and n_experts are ignored.
+ *   idx            nullable DEVICE int32[n], read by the kernel.
+ *   n              number of slots (0..65535; 0 is a no-op).
+ *   xq, xq_stride_bytes, status_dev   as zdmmv_expert_gather.
+ *   h              device fp32 [n][rows].
+ * The gate and up dot products are the fp32 values zdmmv_expert_gather2 writes,
+ * bit for bit; h is silu(g)*u of those in fp32 (an IEEE divide by 1 + expf(-g)
+ * and one multiply), within a few ulp of silu in exact arithmetic.
+ * Errors: as zdmmv_expert_gather. */
+zdmmv_status zdmmv_expert_swiglu(zdmmv_fmt fmt, const void *w_gate, const void *w_up,
+                                 int64_t expert_stride_bytes, zdmmv_layout layout,
+                                 int64_t rows, int64_t cols, const int32_t *idx, int n,
+                                 int n_experts, const void *xq, int64_t xq_stride_bytes,
+                                 float *h, int32_t *status_dev, zdmmv_stream_t stream);
+
 /* LM-head DMMV with a fused argmax epilogue: the greedy pick over the logits
  * W.x without writing them (the M1 decode chain ends "LM head -> argmax":
  * "Bringing ZINC to NVIDIA", section "The roadmap: from 70 to a coherent

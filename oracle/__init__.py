@@ -77,6 +77,9 @@ def _bind(L):
                                       f64p, f64p]
     L.oracle_expert_gather.argtypes = [ctypes.c_int, u8p, i64, i64, i64, i32p, ctypes.c_int,
                                        ctypes.c_int, u8p, i64, f64p, f64p, i32p]
+    L.oracle_dmmv_acc.argtypes = [ctypes.c_int, u8p, i64, i64, u8p, f64p, f64p, f64p]
+    L.oracle_swiglu.argtypes = [f64p, f64p, i64, f64p]
+    L.oracle_swiglu.restype = None
     L.oracle_argmax.argtypes = [f64p, i64, f64p]
     L.oracle_argmax.restype = ctypes.c_int64
     L.oracle_repack.argtypes = [ctypes.c_int, u8p, i64, i64, u8p]
@@ -220,6 +223,25 @@ def expert_gather(fmt: int, w_stack, expert_stride: int, rows: int, cols: int, i
                                       _p(y, ctypes.c_double), _p(e, ctypes.c_double),
                                       ctypes.byref(st)), "expert_gather")
     return y, e, int(st.value)
+
+
+def dmmv_acc(fmt: int, w, rows: int, cols: int, xq, y0, gate=None):
+    """Returns (y0 + s * W.x, s * err_scale), s = sigmoid(gate) or 1."""
+    w, xq = _u8(w), _u8(xq)
+    y = np.array(y0, dtype=np.float64).reshape(-1).copy()
+    e = np.zeros(rows, dtype=np.float64)
+    g = None if gate is None else ctypes.byref(ctypes.c_double(float(gate)))
+    _check(lib().oracle_dmmv_acc(fmt, _p(w, ctypes.c_uint8), rows, cols, _p(xq, ctypes.c_uint8), g,
+                                 _p(y, ctypes.c_double), _p(e, ctypes.c_double)), "dmmv_acc")
+    return y, e
+
+
+def swiglu(g, u) -> np.ndarray:
+    g = np.ascontiguousarray(g, dtype=np.float64).reshape(-1)
+    u = np.ascontiguousarray(u, dtype=np.float64).reshape(-1)
+    h = np.zeros_like(g)
+    lib().oracle_swiglu(_p(g, ctypes.c_double), _p(u, ctypes.c_double), g.size, _p(h, ctypes.c_double))
+    return h
 
 
 def argmax(y) -> tuple[int, float]:

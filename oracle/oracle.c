@@ -22,6 +22,7 @@
 
 #include <math.h>
 #include <stddef.h>
+#include <stdlib.h>
 #include <string.h>
 
 /* ---------------------------------------------------------------- fp16 ---- */
@@ -267,6 +268,43 @@ int oracle_expert_gather(int fmt, const uint8_t *w_stack, int64_t expert_stride_
         oracle_dmmv(fmt, wk, rows, cols, xk, yk, ek);
     }
     return 0;
+}
+
+/* ------------------------------------------------------------ epilogues ---- */
+
+/* The shared expert's output is scaled by the sigmoid of its gate and added to
+ * the MoE output ("sigmoid_scale_acc", M1 MoE chain in "CUDA backend for ZINC",
+ * "5. The target model & milestone ordering"); with no gate the DMMV result is
+ * simply accumulated (the templated DMMV's "accumulate mode", same section). */
+int oracle_dmmv_acc(int fmt, const uint8_t *w, int64_t rows, int64_t cols, const uint8_t *xq,
+                    const double *gate, double *y, double *e)
+{
+    if (!shape_ok(fmt, rows, cols))
+        return -1;
+    double s = gate ? 1.0 / (1.0 + exp(-*gate)) : 1.0;
+    double *d = (double *)malloc((size_t)(rows > 0 ? rows : 1) * 2 * sizeof(double));
+    if (!d)
+        return -1;
+    double *de = d + (rows > 0 ? rows : 1);
+    oracle_dmmv(fmt, w, rows, cols, xq, d, de);
+    for (int64_t r = 0; r < rows; ++r) {
+        y[r] += s * d[r];
+        if (e)
+            e[r] = s * de[r];
+    }
+    free(d);
+    return 0;
+}
+
+/* The MoE expert FFN combines its gate and up projections with swiglu before the
+ * down projection (M1 MoE chain "dmmv_q4k_moe gate/up + swiglu + dmmv_q5k_moe
+ * down" and the fused "dmmv_*_fused_gate_up*" of M3: "CUDA backend for ZINC",
+ * "5. The target model & milestone ordering"). The pages do not print the
+ * formula; this is the standard SwiGLU: silu(gate) times up. */
+void oracle_swiglu(const double *g, const double *u, int64_t n, double *h)
+{
+    for (int64_t i = 0; i < n; ++i)
+        h[i] = g[i] / (1.0 + exp(-g[i])) * u[i];
 }
 
 /* -------------------------------------------------------------- argmax ---- */

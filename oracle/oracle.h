@@ -96,6 +96,16 @@ int oracle_expert_gather(int fmt, const uint8_t *w_stack, int64_t expert_stride_
                          int n_experts, const uint8_t *xq, int64_t xq_stride_bytes,
                          double *y, double *e, int32_t *status);
 
+/* Accumulate epilogue: y[r] += s * (W.x)[r] with s = 1 when gate is NULL, else
+ * s = sigmoid(*gate) = 1 / (1 + exp(-*gate)) (fp64). y is updated in place;
+ * e[r] (nullable) receives s * sum_b |d_w d_x s_b|. */
+int oracle_dmmv_acc(int fmt, const uint8_t *w, int64_t rows, int64_t cols, const uint8_t *xq,
+                    const double *gate, double *y, double *e);
+
+/* SwiGLU of the gate and up projections: h_i = silu(g_i) * u_i with
+ * silu(g) = g / (1 + exp(-g)) (fp64). */
+void oracle_swiglu(const double *g, const double *u, int64_t n, double *h);
+
 /* Index of the largest of n values (the smallest such index on ties), or -1 for
  * n <= 0; the greedy pick over the LM-head logits. *max_out receives the value. */
 int64_t oracle_argmax(const double *y, int64_t n, double *max_out);

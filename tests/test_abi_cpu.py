@@ -82,6 +82,11 @@ def test_other_argument_checks(L):
     assert L.zdmmv_host_step(8, FAKE, 0, 4, 64, FAKE, 0, FAKE, FAKE, 1 << 20, None) == 2
     assert L.zdmmv_device_status(None, 0) == 1
     assert L.zdmmv_selftest_wait_timeout(None, None) == 1
+    c = L.zdmmv_dmmv_acc
+    assert c(8, FAKE, 0, 0, 64, None, None, None, None) == 0        # no rows
+    assert c(8, FAKE, 0, 4, 64, FAKE, None, None, None) == 1        # y null
+    assert c(8, FAKE, 0, 4, 48, FAKE, None, FAKE, None) == 2
+    assert c(8, FAKE, 0, 4, 64, FAKE, FAKE + 2, FAKE, None) == 3    # misaligned gate
     a = L.zdmmv_dmmv_argmax
     assert a(2, FAKE, 0, 100, 160, FAKE, FAKE, None, FAKE, 16384, None) == 2     # off the pipelined widths
     assert a(2, FAKE, 0, 0, 2048, FAKE, FAKE, None, FAKE, 16384, None) == 2      # no rows
@@ -102,3 +107,12 @@ def test_other_argument_checks(L):
     assert g2(2, FAKE, FAKE, 1 << 16, 0, 4, 64, FAKE, 2, 8, FAKE, 0, FAKE, None, None, None) == 1
     assert g2(2, FAKE, FAKE + 8, 1 << 16, 0, 4, 64, FAKE, 2, 8, FAKE, 0, FAKE, FAKE, None, None) == 3
     assert g2(2, FAKE, FAKE, 1 << 16, 0, 4, 64, FAKE, 0, 8, FAKE, 0, FAKE, FAKE, None, None) == 0
+    sw = L.zdmmv_expert_swiglu
+    assert sw(2, FAKE, FAKE, 1 << 16, 0, 4, 160, FAKE, 2, 8, FAKE, 0, FAKE, None, None) == 2  # off the pipelined widths
+    assert sw(2, FAKE, FAKE, 0, 0, 4, 2048, None, 2, 0, FAKE, 0, FAKE, None, None) == 2       # no index, n > 1
+    assert sw(2, FAKE, None, 1 << 16, 0, 4, 2048, FAKE, 2, 8, FAKE, 0, FAKE, None, None) == 1
+    assert sw(2, FAKE, FAKE + 8, 1 << 16, 0, 4, 2048, FAKE, 2, 8, FAKE, 0, FAKE, None, None) == 3
+    assert sw(2, FAKE, FAKE, 1 << 16, 0, 4, 2048, FAKE, 2, 8, FAKE, 100, FAKE, None, None) == 2  # xq stride short
+    assert sw(2, FAKE, FAKE, 1008, 0, 4, 2048, FAKE, 2, 8, FAKE, 0, FAKE, None, None) == 2     # experts overlap
+    assert sw(2, FAKE, FAKE, 1 << 16, 0, 4, 2048, FAKE, 0, 8, FAKE, 0, FAKE, None, None) == 0  # n == 0
+    assert sw(3, FAKE, FAKE, 1 << 16, 0, 4, 2048, FAKE, 2, 8, FAKE, 0, FAKE, None, None) == 5

@@ -42,6 +42,10 @@ MUTANTS = {
     # fp16 rounding by truncation
     "half_truncate": ("double m = rint(v * ldexp(1.0, 10 - expo));",
                       "double m = floor(v * ldexp(1.0, 10 - expo));"),
+    # sigmoid with the wrong sign of the gate
+    "sigmoid_sign": ("1.0 / (1.0 + exp(-*gate))", "1.0 / (1.0 + exp(*gate))"),
+    # silu with the wrong sign inside the exponential
+    "silu_sign": ("h[i] = g[i] / (1.0 + exp(-g[i])) * u[i];", "h[i] = g[i] / (1.0 + exp(g[i])) * u[i];"),
     # argmax keeping the last index on ties
     "argmax_last_tie": ("if (y[i] > y[best])", "if (y[i] >= y[best])"),
     # dp4a reading unsigned bytes
@@ -60,6 +64,8 @@ PINS = [
     lambda m: pins.test_oracle_equals_exact_rational_dmmv(m, 8, 4, 64),
     lambda m: pins.test_oracle_equals_exact_rational_dmmv(m, 2, 3, 160),
     pins.test_argmax_first_index_of_the_maximum,
+    pins.test_accumulate_epilogue_hand_values,
+    pins.test_swiglu_hand_values,
 ]
 
 

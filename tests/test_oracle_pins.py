@@ -386,3 +386,39 @@ def test_argmax_first_index_of_the_maximum(oracle_mod):
     g = np.random.default_rng(4)
     v = g.standard_normal(10007)
     assert oracle_mod.argmax(v)[0] == int(np.argmax(v))
+
+
+# --------------------------------------------------------------- epilogues
+def test_accumulate_epilogue_hand_values(oracle_mod):
+    """Hand-worked: the Q8_0 block of hand_blocks' 'qw=1, qx=127' case gives
+    W.x = 31.75; with gate 0, sigmoid(0) = 1/2 exactly."""
+    case = [c for c in load("hand_blocks.json")["cases"] if c["name"] == "q8_0 qw=1 qx=127"][0]
+    fmt, w, x = _hand_case_blocks(case)
+    y, e = oracle_mod.dmmv_acc(fmt, w, 1, 32, x, [1.0])
+    assert y[0] == 1.0 + 31.75 and e[0] == 31.75
+    y, e = oracle_mod.dmmv_acc(fmt, w, 1, 32, x, [-2.0], gate=0.0)
+    assert y[0] == -2.0 + 0.5 * 31.75 and e[0] == 0.5 * 31.75
+    # a large gate saturates the sigmoid to 1, a very negative one to 0
+    y, _ = oracle_mod.dmmv_acc(fmt, w, 1, 32, x, [0.0], gate=60.0)
+    assert abs(y[0] - 31.75) < 1e-20 * 31.75 + 1e-12
+    y, _ = oracle_mod.dmmv_acc(fmt, w, 1, 32, x, [3.0], gate=-800.0)
+    assert y[0] == 3.0
+
+
+def test_accumulate_equals_dmmv_plus_y(oracle_mod):
+    rows, cols = 7, 96
+    w = synth.weight_blocks(Q4_0, rows, cols, seed=201)
+    xq = synth.activation_blocks(cols // 32, seed=202)
+    y0 = np.linspace(-1, 1, rows)
+    y, e = oracle_mod.dmmv_acc(Q4_0, w, rows, cols, xq, y0)
+    d, de = oracle_mod.dmmv(Q4_0, w, rows, cols, xq)
+    assert np.array_equal(y, y0 + d) and np.array_equal(e, de)
+
+
+def test_swiglu_hand_values(oracle_mod):
+    h = oracle_mod.swiglu([0.0, 1.0, -1.0, 40.0, -40.0, 2.0], [3.0, 2.0, 2.0, 0.5, 7.0, -1.0])
+    e = np.e
+    want = [0.0, 2.0 / (1 + 1 / e), -2.0 / (1 + e), 20.0, -40.0 * 7.0 / (1 + e ** 40), -2.0 / (1 + e ** -2)]
+    np.testing.assert_allclose(h, want, rtol=1e-14, atol=1e-300)
+    assert h[1] == 2.0 / (1.0 + np.exp(-1.0))            # 1.4621171572600098
+    assert abs(h[1] - 1.4621171572600098) < 1e-15

@@ -478,3 +478,113 @@ def test_argmax_workspace_is_reusable_back_to_back():
         y = Z.dmmv(fmt, wd, rows, cols, xqd)
         torch.cuda.synchronize()
         assert int(idx.item()) == int(torch.argmax(y).item())
+
+
+# ------------------------------------------------------- accumulate epilogue
+@pytest.mark.parametrize("layout", [Z.GGUF, Z.REPACKED])
+@pytest.mark.parametrize("fmt,rows,cols", [(Q8_0, 2048, 512), (Q4_0, 1000, 4096), (Q8_0, 57, 96)])
+@pytest.mark.parametrize("gate", [None, 0.0, -1.3, 2.7])
+def test_accumulate_epilogue_matches_oracle(fmt, rows, cols, layout, gate):
+    w = synth.weight_blocks(fmt, rows, cols, seed=rows + 3)
+    xq = synth.activation_blocks(cols // 32, seed=cols + 3)
+    y0 = synth.activations(rows, seed=5, scale=0.05)
+    wd = dev(w)
+    if layout == Z.REPACKED:
+        wd = Z.repack(fmt, wd, rows, cols)
+    y = dev(y0.copy())
+    g = None if gate is None else torch.tensor([gate], dtype=torch.float32, device="cuda")
+    Z.dmmv_acc(fmt, wd, rows, cols, dev(xq), y, gate=g, layout=layout)
+    torch.cuda.synchronize()
+    y_ref, e_ref = oracle.dmmv_acc(fmt, w, rows, cols, xq, y0.astype(np.float64), gate=gate)
+    d_ref, _ = oracle.dmmv(fmt, w, rows, cols, xq)
+    yh = y.double().cpu().numpy()
+    # DMMV bound scaled by the gate, the fp32 sigmoid (a few ulp) times |W.x|, the final rounding
+    bound = REL * e_ref + ABS + 4 * 2.0 ** -24 * np.abs(d_ref) + 2.0 ** -24 * np.abs(y_ref)
+    assert np.all(np.abs(yh - y_ref) <= bound), float(np.max(np.abs(yh - y_ref) / bound))
+
+
+def test_accumulate_without_gate_into_zero_equals_store_bitwise():
+    for fmt, rows, cols in [(Q4_0, 4096, 4096), (Q8_0, 77, 160)]:
+        w = synth.weight_blocks(fmt, rows, cols, seed=17)
+        xq = dev(synth.activation_blocks(cols // 32, seed=18))
+        wd = dev(w)
+        y = torch.zeros(rows, device="cuda")
+        Z.dmmv_acc(fmt, wd, rows, cols, xq, y)
+        ys = Z.dmmv(fmt, wd, rows, cols, xq)
+        torch.cuda.synchronize()
+        assert torch.equal(y, ys)
+
+
+# ---------------------------------------------------------- SwiGLU epilogue
+def _stacks(fmt, rows, cols, n_exp, layout, seed):
+    bb = 18 if fmt == Q4_0 else 34
+    per = rows * cols // 32 * bb
+    sg = synth.weight_blocks(fmt, n_exp * rows, cols, seed=seed)
+    su = synth.weight_blocks(fmt, n_exp * rows, cols, seed=seed + 1, stream=synth.S_WEIGHT2)
+    dg, du = dev(sg), dev(su)
+    if layout == Z.REPACKED:
+        dg = torch.cat([Z.repack(fmt, dg[e * per:(e + 1) * per], rows, cols) for e in range(n_exp)])
+        du = torch.cat([Z.repack(fmt, du[e * per:(e + 1) * per], rows, cols) for e in range(n_exp)])
+    return per, sg, su, dg, du
+
+
+def _swiglu_bound(g_ref, u_ref, e_g, e_u, h_ref):
+    """|h - h_ref| bound from the DMMV tolerances of g and u (|silu'| <= 1.1)
+    plus the fp32 epilogue (exp, divide, multiply: a few ulp of h)."""
+    tg, tu = REL * e_g + ABS, REL * e_u + ABS
+    silu = g_ref / (1.0 + np.exp(-g_ref))
+    return 1.1 * tg * np.abs(u_ref) + np.abs(silu) * tu + 1.1 * tg * tu + 16 * 2.0 ** -24 * np.abs(h_ref) + 1e-12
+
+
+@pytest.mark.parametrize("layout", [Z.GGUF, Z.REPACKED])
+@pytest.mark.parametrize("fmt,rows,cols", [(Q4_0, 512, 2048), (Q8_0, 300, 512), (Q4_0, 37, 256),
+                                           (Q8_0, 1000, 4096)])
+def test_swiglu_epilogue_matches_gather2_and_oracle(fmt, rows, cols, layout):
+    n_exp = 6
+    per, sg, su, dg, du = _stacks(fmt, rows, cols, n_exp, layout, seed=51)
+    idx = np.array([5, 1, 3, 3, 0, 7, 2], dtype=np.int32)   # 7 is out of range
+    xs = np.concatenate([synth.activation_blocks(cols // 32, seed=60 + k) for k in range(len(idx))])
+    xstride = cols // 32 * 34
+    ia, xd = dev(idx), dev(xs)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    h = nan_out(len(idx), rows)
+    Z.expert_swiglu(fmt, dg, du, rows, cols, xd, idx=ia, expert_stride=per, n_experts=n_exp,
+                    xq_stride=xstride, h=h, status=st, layout=layout)
+    ga, ua = Z.expert_gather2(fmt, dg, du, per, rows, cols, ia, n_exp, xd, xstride, layout=layout)
+    torch.cuda.synchronize()
+    assert st.item() == 1
+    good = [k for k in range(len(idx)) if idx[k] < n_exp]
+    assert torch.isnan(h[5]).all()
+    hh = h[good].double().cpu().numpy()
+    # against the kernel's own fp32 gate and up values: the epilogue alone
+    g32 = ga[good].double().cpu().numpy()
+    u32 = ua[good].double().cpu().numpy()
+    h64 = g32 / (1.0 + np.exp(-g32)) * u32
+    assert np.all(np.abs(hh - h64) <= 16 * 2.0 ** -24 * np.abs(h64) + 1e-30)
+    # against the oracle: gate and up in fp64, then swiglu
+    g_ref, e_g, _ = oracle.expert_gather(fmt, sg, per, rows, cols, idx, n_exp, xs, xstride)
+    u_ref, e_u, _ = oracle.expert_gather(fmt, su, per, rows, cols, idx, n_exp, xs, xstride)
+    g_ref, e_g, u_ref, e_u = g_ref[good], e_g[good], u_ref[good], e_u[good]
+    h_ref = oracle.swiglu(g_ref.ravel(), u_ref.ravel()).reshape(g_ref.shape)
+    bound = _swiglu_bound(g_ref, u_ref, e_g, e_u, h_ref)
+    assert np.all(np.abs(hh - h_ref) <= bound), float(np.max(np.abs(hh - h_ref) / bound))
+
+
+@pytest.mark.parametrize("fmt,rows,cols", [(Q8_0, 2048, 2048), (Q4_0, 4096, 4096)])
+def test_swiglu_dense_pair_without_index(fmt, rows, cols):
+    _, sg, su, dg, du = _stacks(fmt, rows, cols, 1, Z.GGUF, seed=70)
+    xq = synth.activation_blocks(cols // 32, seed=72)
+    xd = dev(xq)
+    h = nan_out(1, rows)
+    Z.expert_swiglu(fmt, dg, du, rows, cols, xd, h=h)
+    g = Z.dmmv(fmt, dg, rows, cols, xd)
+    u = Z.dmmv(fmt, du, rows, cols, xd)
+    torch.cuda.synchronize()
+    hh = h[0].double().cpu().numpy()
+    g32, u32 = g.double().cpu().numpy(), u.double().cpu().numpy()
+    h64 = g32 / (1.0 + np.exp(-g32)) * u32
+    assert np.all(np.abs(hh - h64) <= 16 * 2.0 ** -24 * np.abs(h64) + 1e-30)
+    g_ref, e_g = oracle.dmmv(fmt, sg, rows, cols, xq)
+    u_ref, e_u = oracle.dmmv(fmt, su, rows, cols, xq)
+    h_ref = oracle.swiglu(g_ref, u_ref)
+    assert np.all(np.abs(hh - h_ref) <= _swiglu_bound(g_ref, u_ref, e_g, e_u, h_ref))
