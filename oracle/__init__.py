@@ -73,6 +73,7 @@ def _bind(L):
     L.oracle_dequantize.argtypes = [ctypes.c_int, u8p, i64, f64p]
     L.oracle_block_sums.argtypes = [ctypes.c_int, u8p, i64, i64, u8p, i32p]
     L.oracle_dmmv.argtypes = [ctypes.c_int, u8p, i64, i64, u8p, f64p, f64p]
+    L.oracle_dmmv_xf32.argtypes = [ctypes.c_int, u8p, i64, i64, ctypes.POINTER(ctypes.c_float), f64p, f64p]
     L.oracle_dmmv_batched.argtypes = [ctypes.c_int, u8p, i64, i64, u8p, ctypes.c_int,
                                       f64p, f64p]
     L.oracle_expert_gather.argtypes = [ctypes.c_int, u8p, i64, i64, i64, i32p, ctypes.c_int,
@@ -194,6 +195,19 @@ def dmmv(fmt: int, w, rows: int, cols: int, xq) -> tuple[np.ndarray, np.ndarray]
     _check(lib().oracle_dmmv(fmt, _p(w, ctypes.c_uint8), rows, cols,
                              _p(xq, ctypes.c_uint8), _p(y, ctypes.c_double),
                              _p(e, ctypes.c_double)), "dmmv")
+    return y, e
+
+
+def dmmv_xf32(fmt: int, w, rows: int, cols: int, x) -> tuple[np.ndarray, np.ndarray]:
+    """W.x with x taken as fp32 values (no quantization): (y_ref, err_scale), float64 [rows]."""
+    w = _u8(w)
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    if x.size != cols:
+        raise ValueError("dmmv_xf32: x must hold cols values")
+    y = np.zeros(rows, dtype=np.float64)
+    e = np.zeros(rows, dtype=np.float64)
+    _check(lib().oracle_dmmv_xf32(fmt, _p(w, ctypes.c_uint8), rows, cols, _p(x, ctypes.c_float),
+                                  _p(y, ctypes.c_double), _p(e, ctypes.c_double)), "dmmv_xf32")
     return y, e
 
 

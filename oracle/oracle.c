@@ -228,6 +228,43 @@ int oracle_dmmv(int fmt, const uint8_t *w, int64_t rows, int64_t cols,
     return 0;
 }
 
+/* The same product with the activation taken as fp32 values, not quantized:
+ * each weight block is dequantized in registers and multiplied by the fp32
+ * input vector (the ZINC_RT Q8_0 slice takes an f32 input vector: "The first
+ * ZINC_RT model slices that actually count", the kernel ABI; the Vulkan DMMV
+ * multiplies dequantized weights by an fp32 x staged in shared memory: habr
+ * article, "Что такое DMMV" and "Трюк с shared memory"). In fp64:
+ * y[r] = sum_b d_w * sum_i v_i * x_i, v_i the block's signed integer values. */
+int oracle_dmmv_xf32(int fmt, const uint8_t *w, int64_t rows, int64_t cols,
+                     const float *x, double *y, double *e)
+{
+    if (!shape_ok(fmt, rows, cols))
+        return -1;
+    int64_t nb = cols / 32;
+    int bb = oracle_block_bytes(fmt);
+    for (int64_t r = 0; r < rows; ++r) {
+        double acc = 0.0, err = 0.0;
+        for (int64_t b = 0; b < nb; ++b) {
+            uint16_t dh;
+            int32_t v[32];
+            oracle_decode_block(fmt, w + (r * nb + b) * bb, &dh, v);
+            double d = oracle_half_to_double(dh);
+            double t = 0.0, ta = 0.0;
+            for (int i = 0; i < 32; ++i) {
+                double p = (double)v[i] * (double)x[b * 32 + i];
+                t += p;
+                ta += fabs(p);
+            }
+            acc += d * t;
+            err += fabs(d) * ta;
+        }
+        y[r] = acc;
+        if (e)
+            e[r] = err;
+    }
+    return 0;
+}
+
 int oracle_dmmv_batched(int fmt, const uint8_t *w, int64_t rows, int64_t cols,
                         const uint8_t *xq, int batch, double *y, double *e)
 {

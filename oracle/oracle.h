@@ -82,6 +82,12 @@ int oracle_block_sums(int fmt, const uint8_t *w, int64_t rows, int64_t cols,
 int oracle_dmmv(int fmt, const uint8_t *w, int64_t rows, int64_t cols,
                 const uint8_t *xq, double *y, double *e);
 
+/* y[r] = sum_b d_w * sum_i v_i * x_i with the activation x taken as fp32 values
+ * (no quantization); v_i are the block's signed values (Q4_0: q - 8). e[r] =
+ * sum_b sum_i |d_w * v_i * x_i|. Computed in fp64. */
+int oracle_dmmv_xf32(int fmt, const uint8_t *w, int64_t rows, int64_t cols,
+                     const float *x, double *y, double *e);
+
 /* The same for `batch` activation vectors stored [batch][cols/32] blocks;
  * y and e are [batch][rows]. */
 int oracle_dmmv_batched(int fmt, const uint8_t *w, int64_t rows, int64_t cols,

@@ -17,8 +17,8 @@ from tests import test_oracle_pins as pins
 MUTANTS = {
     # a dropped term: the last block of every row is skipped
     "drop_last_block": (
-        "double acc = 0.0, err = 0.0;\n        for (int64_t b = 0; b < nb; ++b) {",
-        "double acc = 0.0, err = 0.0;\n        for (int64_t b = 0; b < nb - 1; ++b) {"),
+        "double acc = 0.0, err = 0.0;\n        for (int64_t b = 0; b < nb; ++b) {\n            uint16_t dw, dx;",
+        "double acc = 0.0, err = 0.0;\n        for (int64_t b = 0; b < nb - 1; ++b) {\n            uint16_t dw, dx;"),
     # a wrong sign of the Q4_0 offset
     "q4_offset_sign": (
         "q[j] = (int32_t)(blk[2 + j] & 0x0f) - 8;",
@@ -48,6 +48,10 @@ MUTANTS = {
     "silu_sign": ("h[i] = g[i] / (1.0 + exp(-g[i])) * u[i];", "h[i] = g[i] / (1.0 + exp(g[i])) * u[i];"),
     # argmax keeping the last index on ties
     "argmax_last_tie": ("if (y[i] > y[best])", "if (y[i] >= y[best])"),
+    # the fp32-activation product reading the first block's activation for every block
+    "xf32_x_index": ("(double)v[i] * (double)x[b * 32 + i]", "(double)v[i] * (double)x[i]"),
+    # the fp32-activation product without the block scale
+    "xf32_scale_dropped": ("acc += d * t;", "acc += t;"),
     # dp4a reading unsigned bytes
     "dp4a_unsigned": ("int8_t ab = (int8_t)(uint8_t)", "uint8_t ab = (uint8_t)"),
 }
@@ -66,6 +70,8 @@ PINS = [
     pins.test_argmax_first_index_of_the_maximum,
     pins.test_accumulate_epilogue_hand_values,
     pins.test_swiglu_hand_values,
+    pins.test_xf32_hand_worked_blocks,
+    lambda m: pins.test_xf32_oracle_equals_exact_rational(m, 2, 3, 160),
 ]
 
 

@@ -422,3 +422,79 @@ def test_swiglu_hand_values(oracle_mod):
     np.testing.assert_allclose(h, want, rtol=1e-14, atol=1e-300)
     assert h[1] == 2.0 / (1.0 + np.exp(-1.0))            # 1.4621171572600098
     assert abs(h[1] - 1.4621171572600098) < 1e-15
+
+
+# ------------------------------------------------- fp32-activation product
+def _exact_dmmv_xf32(fmt, w, rows, cols, x):
+    """Exact W.x for fp32 x via Fractions, decoding blocks with numpy views."""
+    nb = cols // 32
+    if fmt == Q8_0:
+        wb = w.reshape(rows, nb, 34)
+        wv = wb[:, :, 2:].view(np.int8).astype(int)
+    else:
+        wb = w.reshape(rows, nb, 18)
+        qs = wb[:, :, 2:].astype(int)
+        wv = np.concatenate([(qs & 15) - 8, (qs >> 4) - 8], axis=-1)
+    wd = wb[:, :, :2].copy().view(np.float16)[..., 0]
+    xf = [Fraction(float(v)) for v in np.asarray(x, dtype=np.float32)]
+    out, scale = [], []
+    for r in range(rows):
+        acc, err = Fraction(0), Fraction(0)
+        for b in range(nb):
+            d = Fraction(float(wd[r, b]))
+            terms = [d * int(wv[r, b, i]) * xf[32 * b + i] for i in range(32)]
+            acc += sum(terms)
+            err += sum(abs(t) for t in terms)
+        out.append(acc)
+        scale.append(err)
+    return out, scale
+
+
+@pytest.mark.parametrize("fmt", [Q8_0, Q4_0])
+@pytest.mark.parametrize("rows,cols", [(1, 32), (3, 160)])
+def test_xf32_oracle_equals_exact_rational(oracle_mod, fmt, rows, cols):
+    w = synth.weight_blocks(fmt, rows, cols, seed=61 + rows)
+    x = synth.activations(cols, seed=62 + cols)
+    y, e = oracle_mod.dmmv_xf32(fmt, w, rows, cols, x)
+    exact, scale = _exact_dmmv_xf32(fmt, w, rows, cols, x)
+    for r in range(rows):
+        assert abs(Fraction(y[r]) - exact[r]) <= scale[r] * Fraction(1, 10 ** 14)
+        assert abs(Fraction(e[r]) - scale[r]) <= scale[r] * Fraction(1, 10 ** 14)
+
+
+def test_xf32_hand_worked_blocks(oracle_mod):
+    # Q8_0, d = 1.0, every q = 1, x = 0.5 everywhere: 32 * 0.5 = 16
+    w8 = block_q8("0x3c00", [1] * 32)
+    y, e = oracle_mod.dmmv_xf32(Q8_0, w8, 1, 32, np.full(32, 0.5, dtype=np.float32))
+    assert y[0] == 16.0 and e[0] == 16.0
+    # Q4_0, d = 0.5, every qs byte 0xF0: elements 0..15 are 0 - 8, 16..31 are 15 - 8
+    w4 = block_q4("0x3800", [0xF0] * 16)
+    y, e = oracle_mod.dmmv_xf32(Q4_0, w4, 1, 32, np.ones(32, dtype=np.float32))
+    assert y[0] == 0.5 * (16 * -8 + 16 * 7) and e[0] == 0.5 * (16 * 8 + 16 * 7)
+    x = np.zeros(32, dtype=np.float32)
+    x[20] = 3.0                                  # high nibble of qs byte 4: value 7
+    y, _ = oracle_mod.dmmv_xf32(Q4_0, w4, 1, 32, x)
+    assert y[0] == 0.5 * 7 * 3.0
+    # two blocks of a row: the second block's activation is x[32..63]
+    w2 = np.concatenate([block_q8("0x3c00", [1] * 32), block_q8("0x4000", [-2] * 32)])
+    x2 = np.concatenate([np.full(32, 0.25, dtype=np.float32), np.full(32, 1.0, dtype=np.float32)])
+    y, _ = oracle_mod.dmmv_xf32(Q8_0, w2, 1, 64, x2)
+    assert y[0] == 32 * 0.25 + 2.0 * (-2) * 32
+
+
+@pytest.mark.parametrize("fmt", [Q8_0, Q4_0])
+def test_xf32_equals_quantized_product_when_x_is_representable(oracle_mod, fmt):
+    """An x that Q8_0 represents exactly (x = 2^-7 * q, every block holding a
+    +-127) quantizes to itself, so both products are the same sums in the same
+    order: bit for bit equal."""
+    rows, cols = 9, 256
+    w = synth.weight_blocks(fmt, rows, cols, seed=71)
+    rng = np.random.default_rng(72)
+    q = rng.integers(-127, 128, size=cols)
+    q[::32] = 127
+    x = (q * 2.0 ** -7).astype(np.float32)
+    xq = oracle_mod.quantize_q8_0(x)
+    assert np.array_equal(oracle_mod.dequantize(Q8_0, xq), x.astype(np.float64))
+    y1, e1 = oracle_mod.dmmv(fmt, w, rows, cols, xq)
+    y2, e2 = oracle_mod.dmmv_xf32(fmt, w, rows, cols, x)
+    assert np.array_equal(y1, y2)
