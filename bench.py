@@ -310,6 +310,27 @@ def measure_dense(cfg, layers, steps, warmup, world, device, eager, layout=0):
             "rows_per_s": cfg.batch * cfg.rows / per_launch_s, "algorithmic_bytes": nbytes}
 
 
+def measure_xf32(cfg, layers, steps, warmup, world, device, eager):
+    """The DMMV with the fp32 activation taken as is (no quantization), back to
+    back over the layer stack; algorithmic bytes = weights + fp32 x + fp32 y."""
+    import torch
+    pool = DensePool(cfg, layers)
+    Z, c = pool.Z, cfg
+
+    def run_all():
+        for l in range(layers):
+            Z.dmmv_xf32(c.fmt, pool.w[l], c.rows, c.cols, pool.x[l], batch=c.batch, y=pool.y[l])
+
+    run = graph_or_eager(run_all, eager)
+    ms, _ = time_fn(run, steps, warmup, world, device)
+    per = ms / 1e3 / (steps * layers)
+    nbytes = cfg.weight_bytes + c.batch * (4 * c.cols + 4 * c.rows)
+    del pool
+    torch.cuda.empty_cache()
+    return {"us": per * 1e6, "gbs": nbytes / per / 1e9, "algorithmic_bytes": nbytes,
+            "note": "fp32 activation, no quantization: one fp32 fma per weight (ALU-heavy)"}
+
+
 def measure_argmax(cfg, layers, steps, warmup, world, device, eager):
     """The LM head with the fused argmax epilogue (no logits written), back to back."""
     import torch
@@ -494,6 +515,11 @@ def gpu_arm(args):
                                args.eager, layout=1)
             workloads[c.name]["repacked_layout"] = {"dmmv_gbs": rp["dmmv_gbs"], "dmmv_us": rp["dmmv_us"],
                                                     "pct_of_peak": 100 * rp["dmmv_gbs"] / hbm_peak}
+        for c in (synth.DENSE_Q4_0, synth.LM_HEAD_Q4_0, synth.BATCHED_Q8_0[1]):
+            xf = measure_xf32(c, layers_for(c, l2), max(5, args.steps // 4), args.warmup, world, device,
+                              args.eager)
+            xf["pct_of_peak"] = 100 * xf["gbs"] / hbm_peak
+            workloads.setdefault(c.name, {})["xf32_activation"] = xf
         workloads["lm_head_q4_0_248320x2048"]["argmax_epilogue"] = measure_argmax(
             synth.LM_HEAD_Q4_0, layers_for(synth.LM_HEAD_Q4_0, l2), max(5, args.steps // 4), args.warmup, world,
             device, args.eager)

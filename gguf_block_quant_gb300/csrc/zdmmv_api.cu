@@ -169,6 +169,41 @@ TmaPlan tma_plan(int fmt, int layout, int64_t cols, int halves) {
     return p;
 }
 
+bool xf32_plan(int fmt, int layout, int64_t cols, TmaPlan *out) {
+    (void)layout;
+    if (!tma_shape_ok(fmt, cols)) return false;
+    const int nb = static_cast<int>(cols / kQK);
+    TmaPlan p{};
+    p.lpr = nb % 32 == 0 ? 32 : (nb % 16 == 0 ? 16 : 8);
+    const int rows_par = kConsumerThreads / p.lpr;
+    const int row_bytes = nb * block_bytes(fmt);
+    // Prefer a plan that leaves room for 4 CTAs per SM (the kernel is bound by
+    // its fp32 arithmetic, so resident warps matter more than deep pipelining);
+    // wide rows fall back to larger units and 2 CTAs per SM.
+    const int x_bytes = static_cast<int>(round_up(static_cast<int64_t>(nb) * 144, 128));
+    const int small_budget = 56 * 1024 - kBarrierBytes - x_bytes;
+    const int kUnitMax = small_budget >= 2 * 12 * 1024 ? small_budget / 2 : 36 * 1024;
+    const int kStageTarget = kUnitMax;
+    p.ppl = 0;
+    for (int r = 4; r >= 1; r >>= 1)
+        if (rows_par * r * row_bytes <= kUnitMax) {
+            p.ppl = r;
+            break;
+        }
+    if (p.ppl == 0) return false;
+    const int unit_rows = rows_par * p.ppl;
+    const int unit = unit_rows * row_bytes;
+    const int m = unit >= kStageTarget ? 1 : kStageTarget / unit;
+    p.tile_rows = unit_rows * m;
+    p.stage_bytes = static_cast<int>(round_up(static_cast<int64_t>(p.tile_rows) * row_bytes, 128));
+    p.x_bytes_padded = x_bytes;
+    p.stages = kBarrierBytes + p.x_bytes_padded + 3 * p.stage_bytes <= 56 * 1024 ? 3 : 2;
+    p.smem_bytes = kBarrierBytes + p.x_bytes_padded + p.stages * p.stage_bytes;
+    if (p.smem_bytes > 112 * 1024) return false;
+    *out = p;
+    return true;
+}
+
 bool batch_plan(int fmt, int64_t cols, int batch, BatchPlan *out) {
     if (!tma_shape_ok(fmt, cols) || batch < 2 || batch > ZDMMV_MAX_BATCH) return false;
     const int nb = static_cast<int>(cols / kQK);
@@ -804,6 +839,40 @@ zdmmv_status swiglu_entry(int fmt, const void *w_gate, const void *w_up, int64_t
                          : launch_swiglu_q4(a, p, layout, static_cast<int>(ctas), n, st, pdl_enabled()));
 }
 
+zdmmv_status dmmv_xf32_entry(int fmt, const void *w, int layout, int64_t rows, int64_t cols, const float *x,
+                             int batch, float *y, cudaStream_t st) {
+    if (block_bytes(fmt) == 0) return ZDMMV_ERR_FORMAT;
+    if (layout != ZDMMV_LAYOUT_GGUF && layout != ZDMMV_LAYOUT_REPACKED) return ZDMMV_ERR_LAYOUT;
+    if (rows < 0 || cols <= 0 || cols % kQK || cols / kQK > 0x3fffffff) return ZDMMV_ERR_SHAPE;
+    if (batch < 1 || batch > ZDMMV_MAX_BATCH) return ZDMMV_ERR_SHAPE;
+    if (rows == 0) return ZDMMV_OK;
+    if (!w || !x || !y) return ZDMMV_ERR_NULL;
+    if (!aligned(w, 16) || !aligned(x, 16) || !aligned(y, 4)) return ZDMMV_ERR_ALIGN;
+    const DeviceInfo *dev = nullptr;
+    if (device_info(&dev) != cudaSuccess) return ZDMMV_ERR_CUDA;
+    DmmvArgs a{};
+    a.w = static_cast<const uint8_t *>(w);
+    a.xf = x;
+    a.xf_stride = cols;
+    a.y = y;
+    a.y_stride = rows;
+    a.rows = rows;
+    a.nb = static_cast<int32_t>(cols / kQK);
+    a.batch = 1;
+    a.fault = dev->fault;
+    TmaPlan p{};
+    if (xf32_plan(fmt, layout, cols, &p)) {
+        a.tile_rows = p.tile_rows;
+        a.stage_bytes = p.stage_bytes;
+        a.x_bytes_padded = p.x_bytes_padded;
+        // CTAs per slot: one wave of what fits (the launcher queries the occupancy)
+        return from_cuda(fmt == kFmtQ8 ? launch_xf32_q8(a, p, layout, 0, batch, st, pdl_enabled())
+                                       : launch_xf32_q4(a, p, layout, 0, batch, st, pdl_enabled()));
+    }
+    return from_cuda(fmt == kFmtQ8 ? launch_xf32_plain_q8(a, layout, dev->sms, batch, st, pdl_enabled())
+                                   : launch_xf32_plain_q4(a, layout, dev->sms, batch, st, pdl_enabled()));
+}
+
 zdmmv_status dmmv_f32_entry(int fmt, const void *w, int layout, int64_t rows, int64_t cols, const float *x,
                             int batch, float *y, cudaStream_t st) {
     if (block_bytes(fmt) == 0) return ZDMMV_ERR_FORMAT;
@@ -925,6 +994,11 @@ zdmmv_status zdmmv_dmmv_argmax(zdmmv_fmt fmt, const void *w, zdmmv_layout layout
                                size_t workspace_bytes, zdmmv_stream_t stream) {
     return argmax_entry(fmt, w, layout, rows, cols, xq, argmax_out, max_out, workspace, workspace_bytes,
                         reinterpret_cast<cudaStream_t>(stream));
+}
+
+zdmmv_status zdmmv_dmmv_xf32(zdmmv_fmt fmt, const void *w, zdmmv_layout layout, int64_t rows, int64_t cols,
+                             const float *x, int batch, float *y, zdmmv_stream_t stream) {
+    return dmmv_xf32_entry(fmt, w, layout, rows, cols, x, batch, y, reinterpret_cast<cudaStream_t>(stream));
 }
 
 zdmmv_status zdmmv_expert_swiglu(zdmmv_fmt fmt, const void *w_gate, const void *w_up, int64_t expert_stride_bytes,

@@ -112,6 +112,16 @@ cudaError_t launch_swiglu_q4(const DmmvArgs &a, const TmaPlan &p, int layout, in
 int swiglu_ctas_per_sm_q8(int layout, const TmaPlan &p);
 int swiglu_ctas_per_sm_q4(int layout, const TmaPlan &p);
 
+// The DMMV with an fp32 activation taken as is (no quantization): plan (false
+// when the pipelined kernel does not take the shape) and launchers.
+bool xf32_plan(int fmt, int layout, int64_t cols, TmaPlan *out);
+cudaError_t launch_xf32_q8(const DmmvArgs &a, const TmaPlan &p, int layout, int ctas_per_slot, int slots,
+                           cudaStream_t st, bool pdl);
+cudaError_t launch_xf32_q4(const DmmvArgs &a, const TmaPlan &p, int layout, int ctas_per_slot, int slots,
+                           cudaStream_t st, bool pdl);
+cudaError_t launch_xf32_plain_q8(const DmmvArgs &a, int layout, int sms, int slots, cudaStream_t st, bool pdl);
+cudaError_t launch_xf32_plain_q4(const DmmvArgs &a, int layout, int sms, int slots, cudaStream_t st, bool pdl);
+
 // The argmax epilogue's final pass (one CTA over n partials).
 cudaError_t launch_argmax_reduce(const uint2 *parts, int n, int32_t *argmax_out, float *max_out, cudaStream_t st,
                                  bool pdl);

@@ -1,6 +1,6 @@
 // zdmmv_tma.cuh -- the TMA-pipelined decode DMMV kernel for sm_103a.
 //
-// Design (one CTA = 8 consumer warps + 1 producer warp, several CTAs per SM):
+// Design (one CTA = 4 consumer warps + 1 producer warp, several CTAs per SM):
 //  * Each CTA owns a contiguous range of rows. In GGUF layout consecutive rows
 //    are consecutive bytes, so a tile of T rows is ONE contiguous chunk and is
 //    fetched with a single bulk TMA copy (cp.async.bulk) into a shared-memory
@@ -8,7 +8,7 @@
 //    scales. The weight stream is read from HBM exactly once, with an
 //    evict-first L2 policy (it is never re-read).
 //  * The producer lane keeps STAGES tiles in flight (full/empty mbarrier pairs);
-//    the 8 consumer warps never wait on global memory, only on a stage.
+//    the 4 consumer warps never wait on global memory, only on a stage.
 //  * The Q8_0 activation (at most a few KB) is staged once per CTA by one more
 //    bulk copy and then held in REGISTERS: lane l of a row group owns block
 //    pairs l, l+LPR, ... for every row, so the inner loop reads only weights
@@ -346,40 +346,38 @@ __global__ void __launch_bounds__(kTmaThreads, MINB) dmmv_tma_kernel(const DmmvA
                 }
                 if (l == 0 && i < nr) y[tr0 + i] = __fmul_rn(__fdiv_rn(gv, 1.0f + expf(-gv)), uv);
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[s]);
-            continue;
-        }
-        // kRowsIlp rows per row group at a time: independent loads, dot chains and
-        // shuffle trees interleave; every row still gets the same reduction tree
-        for (int base = 0; base < nr; base += kRowsPar * kRowsIlp) {
-            float acc[kRowsIlp];
+        } else {
+            // kRowsIlp rows per row group at a time: independent loads, dot chains and
+            // shuffle trees interleave; every row still gets the same reduction tree
+            for (int base = 0; base < nr; base += kRowsPar * kRowsIlp) {
+                float acc[kRowsIlp];
 #pragma unroll
-            for (int r = 0; r < kRowsIlp; ++r) {
-                const int i = base + r * kRowsPar + g;
-                acc[r] = i < nr ? row_partial<FMT, LAYOUT, LPR, PPL>(xr, st, i, T, nb, l) : 0.0f;
-            }
+                for (int r = 0; r < kRowsIlp; ++r) {
+                    const int i = base + r * kRowsPar + g;
+                    acc[r] = i < nr ? row_partial<FMT, LAYOUT, LPR, PPL>(xr, st, i, T, nb, l) : 0.0f;
+                }
 #pragma unroll
-            for (int o = LPR / 2; o > 0; o >>= 1) {
+                for (int o = LPR / 2; o > 0; o >>= 1) {
 #pragma unroll
-                for (int r = 0; r < kRowsIlp; ++r) acc[r] += __shfl_xor_sync(0xffffffffu, acc[r], o);
-            }
+                    for (int r = 0; r < kRowsIlp; ++r) acc[r] += __shfl_xor_sync(0xffffffffu, acc[r], o);
+                }
 #pragma unroll
-            for (int r = 0; r < kRowsIlp; ++r) {
-                const int i = base + r * kRowsPar + g;
-                if constexpr (EPI == 0) {
-                    if (l == 0 && i < nr) y[tr0 + i] = acc[r];
-                } else if constexpr (EPI == 2) {
-                    if (l == 0 && i < nr) y[tr0 + i] = __fmaf_rn(scale, acc[r], y[tr0 + i]);
-                } else {
-                    // rows reach a row group in increasing order: a strictly larger value replaces
-                    if (i < nr && (best_row < 0 || acc[r] > best)) {
-                        best = acc[r];
-                        best_row = static_cast<int>(tr0 + i);
+                for (int r = 0; r < kRowsIlp; ++r) {
+                    const int i = base + r * kRowsPar + g;
+                    if constexpr (EPI == 0) {
+                        if (l == 0 && i < nr) y[tr0 + i] = acc[r];
+                    } else if constexpr (EPI == 2) {
+                        if (l == 0 && i < nr) y[tr0 + i] = __fmaf_rn(scale, acc[r], y[tr0 + i]);
+                    } else {
+                        // rows reach a row group in increasing order: a strictly larger value replaces
+                        if (i < nr && (best_row < 0 || acc[r] > best)) {
+                            best = acc[r];
+                            best_row = static_cast<int>(tr0 + i);
+                        }
                     }
                 }
             }
-        }
+        }  // EPI != 3
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);
     }

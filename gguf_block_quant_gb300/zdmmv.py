@@ -55,6 +55,7 @@ _SIGS = {
     "zdmmv_q8_0_batched": ([_vp, _int, _i64, _i64, _vp, _int, _vp, _vp], _int),
     "zdmmv_q4_0_batched": ([_vp, _int, _i64, _i64, _vp, _int, _vp, _vp], _int),
     "zdmmv_dmmv_f32": ([_int, _vp, _int, _i64, _i64, _vp, _int, _vp, _vp], _int),
+    "zdmmv_dmmv_xf32": ([_int, _vp, _int, _i64, _i64, _vp, _int, _vp, _vp], _int),
     "zdmmv_dmmv_acc": ([_int, _vp, _int, _i64, _i64, _vp, _vp, _vp, _vp], _int),
     "zdmmv_dmmv_argmax": ([_int, _vp, _int, _i64, _i64, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp], _int),
     "zdmmv_dmmv_argmax_noalloc": ([_int, _vp, _int, _i64, _i64, _vp, _vp, _vp, _vp], _int),
@@ -192,6 +193,15 @@ def dmmv_f32(fmt: int, w, rows: int, cols: int, x, batch: int = 1, y=None, layou
         raise ValueError("dmmv_f32: x must be float32 [batch][cols]")
     y = _out(y, (batch, rows) if batch > 1 else (rows,), w.device)
     _call("zdmmv_dmmv_f32", fmt, _ptr(w), layout, rows, cols, _ptr(x), batch, _ptr(y), _stream(stream))
+    return y
+
+
+def dmmv_xf32(fmt: int, w, rows: int, cols: int, x, batch: int = 1, y=None, layout: int = GGUF, stream=None):
+    """W.x with the fp32 activation taken as is (no quantization); x fp32 [batch][cols]."""
+    if x.dtype != torch.float32:
+        raise ValueError("dmmv_xf32: x must be float32")
+    y = _out(y, (batch, rows) if batch > 1 else (rows,), w.device)
+    _call("zdmmv_dmmv_xf32", fmt, _ptr(w), layout, rows, cols, _ptr(x), batch, _ptr(y), _stream(stream))
     return y
 
 

@@ -156,6 +156,26 @@ zdmmv_status zdmmv_dmmv_f32(zdmmv_fmt fmt, const void *w, zdmmv_layout layout, i
                             int64_t cols, const float *x, int batch, float *y,
                             zdmmv_stream_t stream);
 
+/* The product with the activation taken as fp32 values, NOT quantized:
+ * y[v][r] = sum_b d_w * sum_i v_i * x[v][32b + i], v_i the weight block's signed
+ * values (Q4_0: q - 8). Each weight block is dequantized in registers and
+ * multiplied by the fp32 x staged in shared memory, the form of the ZINC_RT
+ * Q8_0 slice (f32 input vector: "The first ZINC_RT model slices that actually
+ * count", kernel ABI) and of the Vulkan DMMV's shared-memory x (habr article,
+ * "Что такое DMMV", "Трюк с shared memory"). It reads 4 bytes per activation
+ * element instead of 34/32 and spends an fp32 fma per weight instead of a dp4a
+ * per four: an accuracy reference for the quantized-activation path.
+ *   fmt, w, layout, rows, cols   as zdmmv_dmmv_f32 (any multiple of 32 columns;
+ *                                widths off the pipelined path run a plain kernel).
+ *   x      device fp32 [batch][cols], 16-byte aligned; batch 1..8.
+ *   y      device fp32 [batch][rows].
+ * Results are fp32 sums within 1e-5 * sum_b sum_i |d_w v_i x_i| + 1e-6 of the
+ * exact product, deterministic from call to call.
+ * Errors: ERR_NULL, ERR_SHAPE, ERR_ALIGN, ERR_LAYOUT, ERR_FORMAT, ERR_CUDA. */
+zdmmv_status zdmmv_dmmv_xf32(zdmmv_fmt fmt, const void *w, zdmmv_layout layout, int64_t rows,
+                             int64_t cols, const float *x, int batch, float *y,
+                             zdmmv_stream_t stream);
+
 /* Accumulate epilogue: y[r] = y[r] + s * (W.x)[r], one fused fma per row, with
  * s = 1 when gate is NULL (the templated DMMV's "accumulate mode") or
  * s = sigmoid(*gate) = 1/(1 + exp(-*gate)) for a device fp32 gate scalar (the

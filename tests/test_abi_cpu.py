@@ -107,6 +107,14 @@ def test_other_argument_checks(L):
     assert g2(2, FAKE, FAKE, 1 << 16, 0, 4, 64, FAKE, 2, 8, FAKE, 0, FAKE, None, None, None) == 1
     assert g2(2, FAKE, FAKE + 8, 1 << 16, 0, 4, 64, FAKE, 2, 8, FAKE, 0, FAKE, FAKE, None, None) == 3
     assert g2(2, FAKE, FAKE, 1 << 16, 0, 4, 64, FAKE, 0, 8, FAKE, 0, FAKE, FAKE, None, None) == 0
+    xf = L.zdmmv_dmmv_xf32
+    assert xf(8, FAKE, 0, 0, 64, None, 1, None, None) == 0                              # rows == 0
+    assert xf(8, None, 0, 4, 64, FAKE, 1, FAKE, None) == 1
+    assert xf(3, FAKE, 0, 4, 64, FAKE, 1, FAKE, None) == 5
+    assert xf(8, FAKE, 2, 4, 64, FAKE, 1, FAKE, None) == 4
+    assert xf(8, FAKE, 0, 4, 48, FAKE, 1, FAKE, None) == 2                              # cols % 32
+    assert xf(8, FAKE, 0, 4, 64, FAKE, 0, FAKE, None) == 2                              # batch 0
+    assert xf(8, FAKE, 0, 4, 64, FAKE + 4, 1, FAKE, None) == 3                          # x not 16-byte aligned
     sw = L.zdmmv_expert_swiglu
     assert sw(2, FAKE, FAKE, 1 << 16, 0, 4, 160, FAKE, 2, 8, FAKE, 0, FAKE, None, None) == 2  # off the pipelined widths
     assert sw(2, FAKE, FAKE, 0, 0, 4, 2048, None, 2, 0, FAKE, 0, FAKE, None, None) == 2       # no index, n > 1

@@ -588,3 +588,43 @@ def test_swiglu_dense_pair_without_index(fmt, rows, cols):
     u_ref, e_u = oracle.dmmv(fmt, su, rows, cols, xq)
     h_ref = oracle.swiglu(g_ref, u_ref)
     assert np.all(np.abs(hh - h_ref) <= _swiglu_bound(g_ref, u_ref, e_g, e_u, h_ref))
+
+
+# ------------------------------------------------ fp32 (unquantized) activation
+@pytest.mark.parametrize("layout", [Z.GGUF, Z.REPACKED])
+@pytest.mark.parametrize("fmt,rows,cols,batch", [
+    (Q4_0, 1000, 2048, 1), (Q8_0, 777, 4096, 1), (Q4_0, 300, 8192, 2), (Q8_0, 129, 8192, 1),
+    (Q8_0, 200, 768, 3), (Q4_0, 64, 512, 1), (Q8_0, 33, 256, 8),      # 8 and 16 lanes per row
+    (Q4_0, 45, 96, 2), (Q8_0, 20, 160, 1), (Q4_0, 7, 8224, 1),        # plain kernel widths
+])
+def test_xf32_matches_oracle(fmt, rows, cols, batch, layout):
+    w = synth.weight_blocks(fmt, rows, cols, seed=rows + 11)
+    x = synth.activations(cols, seed=cols + 12, batch=batch)
+    wd = dev(w)
+    if layout == Z.REPACKED:
+        wd = Z.repack(fmt, wd, rows, cols)
+    xd = dev(x)
+    y = nan_out(batch, rows)
+    Z.dmmv_xf32(fmt, wd, rows, cols, xd, batch=batch, y=y, layout=layout)
+    y2 = nan_out(batch, rows)
+    Z.dmmv_xf32(fmt, wd, rows, cols, xd, batch=batch, y=y2, layout=layout)
+    torch.cuda.synchronize()
+    assert torch.equal(y, y2), "two calls differ"
+    xs = np.asarray(x, dtype=np.float32).reshape(batch, cols)
+    for v in range(batch):
+        y_ref, e_ref = oracle.dmmv_xf32(fmt, w, rows, cols, xs[v])
+        check_y(y[v], y_ref, e_ref)
+
+
+def test_xf32_ragged_tiles_and_zero_rows():
+    fmt, cols = Q4_0, 2048
+    for rows in (1, 17, 4097):
+        w = synth.weight_blocks(fmt, rows, cols, seed=rows)
+        x = synth.activations(cols, seed=5)
+        y = nan_out(rows)
+        Z.dmmv_xf32(fmt, dev(w), rows, cols, dev(x), y=y)
+        torch.cuda.synchronize()
+        y_ref, e_ref = oracle.dmmv_xf32(fmt, w, rows, cols, x)
+        check_y(y, y_ref, e_ref)
+    # rows == 0 launches nothing and succeeds
+    Z.dmmv_xf32(fmt, dev(synth.weight_blocks(fmt, 1, cols, seed=1)), 0, cols, dev(x), y=nan_out(1))
