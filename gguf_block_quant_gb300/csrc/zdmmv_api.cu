@@ -169,6 +169,48 @@ TmaPlan tma_plan(int fmt, int layout, int64_t cols, int halves) {
     return p;
 }
 
+namespace {
+// Batched kernel choice (environment ZDMMV_BATCH_KERNEL): "vsplit" (default),
+// "stream" (dmmv_batch_kernel) or "slots" (single-vector slots, as ZDMMV_BATCH_SLOTS=1).
+int batch_kernel_choice() {
+    static const int v = [] {
+        const char *e = std::getenv("ZDMMV_BATCH_KERNEL");
+        if (!e) return 0;
+        if (std::strcmp(e, "stream") == 0) return 1;
+        if (std::strcmp(e, "slots") == 0) return 2;
+        return 0;
+    }();
+    return v;
+}
+// Vectors per warp in the vector-split kernel for batches above 2 (environment
+// ZDMMV_VSPLIT_V=1 forces one; the default takes two where the registers allow).
+int vsplit_v_pref() {
+    static const int v = [] {
+        const char *e = std::getenv("ZDMMV_VSPLIT_V");
+        return (e && std::atoi(e) == 1) ? 1 : 2;
+    }();
+    return v;
+}
+}  // namespace
+
+bool vsplit_plan(int fmt, int layout, int64_t cols, int batch, TmaPlan *out, int *v, int *nvg) {
+    if (!tma_shape_ok(fmt, cols) || batch < 2 || batch > ZDMMV_MAX_BATCH) return false;
+    TmaPlan p = tma_plan(fmt, layout, cols);
+    // one vector per warp for two vectors (two row groups of warps each); two
+    // per warp beyond, while their block-pair registers fit (at most 2 pairs per lane)
+    const int vv = (batch > 2 && p.ppl <= 2 && vsplit_v_pref() == 2) ? 2 : 1;
+    const int groups = (batch + vv - 1) / vv;
+    const int ng = groups <= 1 ? 1 : (groups <= 2 ? 2 : (groups <= 4 ? 4 : 0));
+    if (ng == 0 || (vv == 1 && ng == 1)) return false;
+    p.x_bytes_padded = 0;  // each lane loads its activation words into registers
+    p.stages = 3;
+    p.smem_bytes = kBarrierBytes + p.stages * p.stage_bytes;
+    *out = p;
+    *v = vv;
+    *nvg = ng;
+    return true;
+}
+
 bool xf32_plan(int fmt, int layout, int64_t cols, TmaPlan *out) {
     (void)layout;
     if (!tma_shape_ok(fmt, cols)) return false;
@@ -620,7 +662,26 @@ zdmmv_status dmmv_entry(int fmt, const void *w, zdmmv_layout layout, int64_t row
     const int64_t cols_pad = cols;
     (void)cols_pad;
     BatchPlan bp{};
-    if (batch >= 2 && batch_slots_forced() == 0 && batch_plan(fmt, cols, batch, &bp)) {
+    TmaPlan vp{};
+    int vv = 0, nvg = 0;
+    const int choice = batch_slots_forced() ? 2 : batch_kernel_choice();
+    if (batch >= 2 && choice == 0 && vsplit_plan(fmt, layout, cols, batch, &vp, &vv, &nvg)) {
+        // one weight stream, the vectors split over the warps
+        const DeviceInfo *dev = nullptr;
+        if (device_info(&dev) != cudaSuccess) return ZDMMV_ERR_CUDA;
+        a.fault = dev->fault;
+        a.batch = batch;
+        a.xq_stride = static_cast<int64_t>(a.nb) * 34;
+        a.y_stride = rows;
+        a.tile_rows = vp.tile_rows;
+        a.stage_bytes = vp.stage_bytes;
+        a.x_bytes_padded = 0;
+        const int cap = std::getenv("ZDMMV_BATCH_CTAS_PER_SM") ? batch_ctas_per_sm() : 0;
+        cudaError_t e = fmt == kFmtQ8 ? launch_vsplit_q8(a, vp, layout, vv, nvg, cap, st, pdl_enabled())
+                                      : launch_vsplit_q4(a, vp, layout, vv, nvg, cap, st, pdl_enabled());
+        return from_cuda(e);
+    }
+    if (batch >= 2 && choice != 2 && batch_plan(fmt, cols, batch, &bp)) {
         // one weight stream for all vectors
         const DeviceInfo *dev = nullptr;
         if (device_info(&dev) != cudaSuccess) return ZDMMV_ERR_CUDA;

@@ -62,6 +62,43 @@ __device__ __forceinline__ uint4 lds128(uint32_t a) {
     asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
     return v;
 }
+
+// Lane l of a row group of LPR lanes owns block pairs l, l + LPR, ... (pair j of
+// the lane is l + j*LPR): in every layout consecutive lanes read consecutive pair
+// slots, and both layouts sum a row's pairs in the same order.
+template <int LPR>
+__device__ __forceinline__ int owned_pair(int l, int j) { return l + j * LPR; }
+
+// Sum over the G lanes of a row group (G = 8, 16 or 32; groups are aligned lane
+// ranges of a warp) of N values per lane (N a power of two, N <= G), scattered:
+// lane l of the group ends with the group sum of value l / (G / N). The values
+// are exchanged from the highest lane bit down, halving the set at each of the
+// first log2(N) steps; every value is combined over the same pairs of lanes, in
+// the same order of bits, as the plain xor tree (acc += shfl_xor(acc, o) for
+// o = G/2 .. 1), so each sum is bitwise the one that tree gives.
+template <int G, int N>
+__device__ __forceinline__ float group_reduce_scatter(const float (&v)[N], int l) {
+    static_assert(N >= 1 && N <= G && (N & (N - 1)) == 0, "N a power of two <= G");
+    float cur[N];
+#pragma unroll
+    for (int k = 0; k < N; ++k) cur[k] = v[k];
+    int bit = G / 2;
+#pragma unroll
+    for (int width = N; width > 1; width >>= 1, bit >>= 1) {
+        const bool upper = (l & bit) != 0;
+#pragma unroll
+        for (int k = 0; k < width / 2; ++k) {
+            const float send = upper ? cur[k] : cur[width / 2 + k];
+            const float keep = upper ? cur[width / 2 + k] : cur[k];
+            cur[k] = keep + __shfl_xor_sync(0xffffffffu, send, bit);
+        }
+    }
+    float r = cur[0];
+#pragma unroll
+    for (int o = G / (2 * N); o > 0; o >>= 1) r += __shfl_xor_sync(0xffffffffu, r, o);
+    return r;
+}
+
 __device__ __forceinline__ uint32_t lds16(uint32_t a) {
     unsigned short v;
     asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(a));
@@ -262,11 +299,8 @@ template <> struct Pair<kFmtQ8, kLayoutGguf> {
 #pragma unroll
         for (int k = 9; k < 17; ++k) sb = dp4a_ss(w[k], x[k], sb);
     }
-    // w: shared-memory address of the pair's 17 weight words
-    __device__ __forceinline__ float fma_pair(uint32_t w, float acc) const {
-        uint32_t r[17];
-#pragma unroll
-        for (int k = 0; k < 17; ++k) r[k] = lds32(w + 4 * k);
+    // r: the pair's 17 weight words
+    __device__ __forceinline__ float fma_w(const uint32_t (&r)[17], float acc) const {
         int sa, sb;
         sums(r, sa, sb);
         acc = __fmaf_rn(static_cast<float>(sa), __fmul_rn(half_lo(r[0]), dxa), acc);
@@ -325,10 +359,8 @@ template <> struct Pair<kFmtQ4, kLayoutGguf> {
         sa = la + (ha >> 4);
         sb = lb + (hb >> 4);
     }
-    __device__ __forceinline__ float fma_pair(uint32_t w, float acc) const {
-        uint32_t r[9];
-#pragma unroll
-        for (int k = 0; k < 9; ++k) r[k] = lds32(w + 4 * k);
+    // r: the pair's 9 weight words
+    __device__ __forceinline__ float fma_w(const uint32_t (&r)[9], float acc) const {
         int sa, sb;
         sums(r, sa, sb);
         acc = __fmaf_rn(static_cast<float>(sa), __fmul_rn(half_lo(r[0]), dxa), acc);

@@ -112,6 +112,14 @@ cudaError_t launch_swiglu_q4(const DmmvArgs &a, const TmaPlan &p, int layout, in
 int swiglu_ctas_per_sm_q8(int layout, const TmaPlan &p);
 int swiglu_ctas_per_sm_q4(int layout, const TmaPlan &p);
 
+// Batched DMMV with the vectors split over the consumer warps: plan (false when
+// the kernel does not take the shape and batch) and launchers.
+bool vsplit_plan(int fmt, int layout, int64_t cols, int batch, TmaPlan *out, int *v, int *nvg);
+cudaError_t launch_vsplit_q8(const DmmvArgs &a, const TmaPlan &p, int layout, int v, int nvg, int max_per_sm,
+                             cudaStream_t st, bool pdl);
+cudaError_t launch_vsplit_q4(const DmmvArgs &a, const TmaPlan &p, int layout, int v, int nvg, int max_per_sm,
+                             cudaStream_t st, bool pdl);
+
 // The DMMV with an fp32 activation taken as is (no quantization): plan (false
 // when the pipelined kernel does not take the shape) and launchers.
 bool xf32_plan(int fmt, int layout, int64_t cols, TmaPlan *out);

@@ -10,8 +10,8 @@
 //  * The producer lane keeps STAGES tiles in flight (full/empty mbarrier pairs);
 //    the 4 consumer warps never wait on global memory, only on a stage.
 //  * The Q8_0 activation (at most a few KB) is staged once per CTA by one more
-//    bulk copy and then held in REGISTERS: lane l of a row group owns block
-//    pairs l, l+LPR, ... for every row, so the inner loop reads only weights
+//    bulk copy and then held in REGISTERS: lane l of a row group owns PPL block
+//    pairs (owned_pair) for every row, so the inner loop reads only weights
 //    from shared memory (the pages stage the input vector in LDS so that the
 //    weights own the cache: habr ZINC article, "Трюк с shared memory"; here the
 //    activation goes one level further, into registers).
@@ -44,7 +44,7 @@ template <int FMT> struct RowGeom<FMT, kLayoutRepacked> {
     static constexpr int kPairQuantBytes = 2 * Fmt<FMT>::kQuantBytes;
 };
 
-// One lane's contribution to one row: pairs l, l+LPR, ... (fixed order).
+// One lane's contribution to one row: its pairs (owned_pair) in order j = 0..PPL-1.
 // stage: shared-memory address of the tile.
 template <int FMT, int LAYOUT, int LPR, int PPL>
 __device__ __forceinline__ float row_partial(const Pair<FMT, LAYOUT> (&xr)[PPL], uint32_t stage, int i,
@@ -52,18 +52,25 @@ __device__ __forceinline__ float row_partial(const Pair<FMT, LAYOUT> (&xr)[PPL],
     const int npairs = nb >> 1;
     float acc = 0.0f;
     if constexpr (LAYOUT == kLayoutGguf) {
+        constexpr int kW = Pair<FMT, LAYOUT>::kWords;
         const uint32_t row = stage + static_cast<uint32_t>(i * nb * Fmt<FMT>::kBlockBytes);
 #pragma unroll
         for (int j = 0; j < PPL; ++j) {
-            const int p = l + j * LPR;
-            if (p < npairs) acc = xr[j].fma_pair(row + p * RowGeom<FMT, LAYOUT>::kPairBytes, acc);
+            const int p = owned_pair<LPR>(l, j);
+            if (p < npairs) {
+                const uint32_t w = row + static_cast<uint32_t>(p * RowGeom<FMT, LAYOUT>::kPairBytes);
+                uint32_t r[kW];
+#pragma unroll
+                for (int k = 0; k < kW; ++k) r[k] = lds32(w + 4 * k);
+                acc = xr[j].fma_w(r, acc);
+            }
         }
     } else {
         const uint32_t rq = stage + static_cast<uint32_t>(i * nb * Fmt<FMT>::kQuantBytes);
         const uint32_t rs = stage + static_cast<uint32_t>(tile_rows * nb * Fmt<FMT>::kQuantBytes + i * nb * 2);
 #pragma unroll
         for (int j = 0; j < PPL; ++j) {
-            const int p = l + j * LPR;
+            const int p = owned_pair<LPR>(l, j);
             if (p < npairs) {
                 const uint32_t ws = lds32(rs + 4 * p);
                 acc = xr[j].fma_pair(rq + p * RowGeom<FMT, LAYOUT>::kPairQuantBytes, ws, acc);
@@ -306,7 +313,7 @@ __global__ void __launch_bounds__(kTmaThreads, MINB) dmmv_tma_kernel(const DmmvA
     P xr[PPL];
 #pragma unroll
     for (int j = 0; j < PPL; ++j) {
-        const int p = l + j * LPR;
+        const int p = owned_pair<LPR>(l, j);
         if (p < (nb >> 1)) {
             uint32_t v[17];
             load_x_pair_words_smem(smem_addr(xs), p, v);
@@ -356,23 +363,29 @@ __global__ void __launch_bounds__(kTmaThreads, MINB) dmmv_tma_kernel(const DmmvA
                     const int i = base + r * kRowsPar + g;
                     acc[r] = i < nr ? row_partial<FMT, LAYOUT, LPR, PPL>(xr, st, i, T, nb, l) : 0.0f;
                 }
+                if constexpr (EPI == 0) {
+                    // the rows' sums land on lanes 0, LPR/kRowsIlp, ... of the group
+                    const float part = group_reduce_scatter<LPR, kRowsIlp>(acc, l);
+                    constexpr int kSpan = LPR / kRowsIlp;
+                    const int i = base + (l / kSpan) * kRowsPar + g;
+                    if (l % kSpan == 0 && i < nr) y[tr0 + i] = part;
+                } else {
 #pragma unroll
-                for (int o = LPR / 2; o > 0; o >>= 1) {
+                    for (int o = LPR / 2; o > 0; o >>= 1) {
 #pragma unroll
-                    for (int r = 0; r < kRowsIlp; ++r) acc[r] += __shfl_xor_sync(0xffffffffu, acc[r], o);
-                }
+                        for (int r = 0; r < kRowsIlp; ++r) acc[r] += __shfl_xor_sync(0xffffffffu, acc[r], o);
+                    }
 #pragma unroll
-                for (int r = 0; r < kRowsIlp; ++r) {
-                    const int i = base + r * kRowsPar + g;
-                    if constexpr (EPI == 0) {
-                        if (l == 0 && i < nr) y[tr0 + i] = acc[r];
-                    } else if constexpr (EPI == 2) {
-                        if (l == 0 && i < nr) y[tr0 + i] = __fmaf_rn(scale, acc[r], y[tr0 + i]);
-                    } else {
-                        // rows reach a row group in increasing order: a strictly larger value replaces
-                        if (i < nr && (best_row < 0 || acc[r] > best)) {
-                            best = acc[r];
-                            best_row = static_cast<int>(tr0 + i);
+                    for (int r = 0; r < kRowsIlp; ++r) {
+                        const int i = base + r * kRowsPar + g;
+                        if constexpr (EPI == 2) {
+                            if (l == 0 && i < nr) y[tr0 + i] = __fmaf_rn(scale, acc[r], y[tr0 + i]);
+                        } else {
+                            // rows reach a row group in increasing order: a strictly larger value replaces
+                            if (i < nr && (best_row < 0 || acc[r] > best)) {
+                                best = acc[r];
+                                best_row = static_cast<int>(tr0 + i);
+                            }
                         }
                     }
                 }

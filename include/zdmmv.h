@@ -124,14 +124,16 @@ zdmmv_status zdmmv_q4_0(const void *w, zdmmv_layout layout, int64_t rows, int64_
                         const void *xq, float *y, zdmmv_stream_t stream);
 
 /* The same weight matrix against `batch` (1..8) activation vectors in one call:
- * xq is [batch][cols/32] Q8_0 blocks, y is [batch][rows] fp32. For widths of
- * 256 * {1,2,3,4}, 2048, 4096 and 8192 columns each weight tile is streamed from
- * HBM once and dotted against every vector (concurrency headroom of decode
- * slots: habr article, section "RDNA4: что мы узнали о железе"); other widths
- * run the single-vector computation once per vector. batch == 1 is the same
- * computation as zdmmv_q8_0 / zdmmv_q4_0, bit for bit; batch > 1 results are
- * deterministic and within the stated tolerance (their fp32 reduction order
- * differs from the single-vector kernel's).
+ * xq is [batch][cols/32] Q8_0 blocks, y is [batch][rows] fp32. Each weight tile
+ * is streamed from HBM once and dotted against every vector (concurrency
+ * headroom of decode slots: habr article, section "RDNA4: что мы узнали о
+ * железе"). For widths that are multiples of 256 up to 4096 columns (up to 8192
+ * with batch <= 4) the consumer warps split the vectors and every vector's
+ * result is the single-vector computation, bit for bit: y[v] equals zdmmv_q8_0 /
+ * zdmmv_q4_0 on vector v. Widths of 8192 columns with batch > 4 stream the tile
+ * through a kernel whose fp32 reduction order differs (deterministic, within
+ * the stated tolerance); other widths run the single-vector computation once per
+ * vector. batch == 1 is zdmmv_q8_0 / zdmmv_q4_0.
  * Errors: as zdmmv_q8_0, plus ERR_SHAPE for batch outside 1..8. */
 zdmmv_status zdmmv_q8_0_batched(const void *w, zdmmv_layout layout, int64_t rows,
                                 int64_t cols, const void *xq, int batch, float *y,

@@ -235,12 +235,24 @@ def test_batched_matches_oracle_and_single_calls(fmt, rows, cols, batch, layout)
     Z.dmmv_batched(fmt, wd, rows, cols, xq, batch, y=y2, layout=layout)
     torch.cuda.synchronize()
     assert torch.equal(y, y2)
-    if batch == 1:
-        # batch 1 is the single-vector computation, bit for bit
-        ys = nan_out(rows)
-        Z.dmmv(fmt, wd, rows, cols, xq, y=ys, layout=layout)
-        torch.cuda.synchronize()
-        assert torch.equal(ys, y[0])
+    if batch == 1 or _vector_split_shape(cols, batch):
+        # batch 1, and every batch the vector-split kernel takes, is the
+        # single-vector computation per vector, bit for bit
+        nbx = cols // 32 * 34
+        for v in range(batch):
+            ys = nan_out(rows)
+            Z.dmmv(fmt, wd, rows, cols, xq[v * nbx:(v + 1) * nbx].clone(), y=ys, layout=layout)
+            torch.cuda.synchronize()
+            assert torch.equal(ys, y[v]), f"vector {v} differs from its single-vector call"
+
+
+def _vector_split_shape(cols, batch):
+    """Widths and batches the vector-split batched kernel takes: pipelined widths
+    (multiples of 256 up to 8192), two vectors per warp up to 4096 columns, one
+    vector per warp (batch <= 4) beyond."""
+    if batch < 2 or cols % 256 or cols > 8192:
+        return False
+    return cols <= 4096 or batch <= 4
 
 
 @pytest.mark.parametrize("fmt,rows,cols", [(Q8_0, 333, 4096), (Q4_0, 517, 2048), (Q8_0, 130, 1024),
