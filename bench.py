@@ -331,6 +331,37 @@ def measure_xf32(cfg, layers, steps, warmup, world, device, eager):
             "note": "fp32 activation, no quantization: one fp32 fma per weight (ALU-heavy)"}
 
 
+def measure_grouped(cfg, layers, steps, warmup, world, device, eager):
+    """The same dense DMMV over LAYERS distinct matrices issued as ONE launch
+    (the expert-gather entry point over a stack, index k -> matrix k, each slot
+    its own activation): the kernel's streaming rate on this shape once the
+    per-launch latency is amortized. Not a decode chain: the matrices are
+    independent problems."""
+    import numpy as np
+    import torch
+    from gguf_block_quant_gb300 import synth
+    from gguf_block_quant_gb300 import zdmmv as Z
+    w = torch.from_numpy(synth.weight_blocks(cfg.fmt, cfg.rows, cfg.cols, seed=cfg.seed)).cuda()
+    stack = w.repeat(layers)
+    per = w.numel()
+    idx = torch.arange(layers, dtype=torch.int32, device="cuda")
+    x = synth.activations(cfg.cols, seed=cfg.seed, scale=cfg.x_scale, batch=layers)
+    xq = Z.quantize_act_q8_0(torch.from_numpy(np.ascontiguousarray(x).reshape(-1)).cuda())
+    y = torch.empty(layers, cfg.rows, dtype=torch.float32, device="cuda")
+
+    def run_all():
+        Z.expert_gather(cfg.fmt, stack, per, cfg.rows, cfg.cols, idx, layers, xq, cfg.nb * 34, y=y)
+
+    run = graph_or_eager(run_all, eager)
+    ms, _ = time_fn(run, steps, warmup, world, device)
+    per_matrix = ms / 1e3 / (steps * layers)
+    nbytes = cfg.algorithmic_bytes() + 4
+    del stack, w, run
+    torch.cuda.empty_cache()
+    return {"matrices_per_launch": layers, "us_per_matrix": per_matrix * 1e6, "gbs": nbytes / per_matrix / 1e9,
+            "note": "independent matrices in one launch (expert-gather entry point); not a decode chain"}
+
+
 def measure_argmax(cfg, layers, steps, warmup, world, device, eager):
     """The LM head with the fused argmax epilogue (no logits written), back to back."""
     import torch
@@ -520,6 +551,10 @@ def gpu_arm(args):
                               args.eager)
             xf["pct_of_peak"] = 100 * xf["gbs"] / hbm_peak
             workloads.setdefault(c.name, {})["xf32_activation"] = xf
+        gr = measure_grouped(synth.DENSE_Q4_0, layers, max(5, args.steps // 4), args.warmup, world, device,
+                             args.eager)
+        gr["pct_of_peak"] = 100 * gr["gbs"] / hbm_peak
+        workloads.setdefault(synth.DENSE_Q4_0.name, {})["grouped_launch"] = gr
         workloads["lm_head_q4_0_248320x2048"]["argmax_epilogue"] = measure_argmax(
             synth.LM_HEAD_Q4_0, layers_for(synth.LM_HEAD_Q4_0, l2), max(5, args.steps // 4), args.warmup, world,
             device, args.eager)

@@ -202,9 +202,11 @@ bool vsplit_plan(int fmt, int layout, int64_t cols, int batch, TmaPlan *out, int
     const int groups = (batch + vv - 1) / vv;
     const int ng = groups <= 1 ? 1 : (groups <= 2 ? 2 : (groups <= 4 ? 4 : 0));
     if (ng == 0 || (vv == 1 && ng == 1)) return false;
-    p.x_bytes_padded = 0;  // each lane loads its activation words into registers
-    p.stages = 3;
-    p.smem_bytes = kBarrierBytes + p.stages * p.stage_bytes;
+    // the batch's activation blocks are staged once; 3 stages when three CTAs
+    // per SM still fit, else 2
+    p.x_bytes_padded = static_cast<int>(round_up(static_cast<int64_t>(batch) * (cols / kQK) * 34, 128));
+    p.stages = kBarrierBytes + p.x_bytes_padded + 3 * p.stage_bytes <= 72 * 1024 ? 3 : 2;
+    p.smem_bytes = kBarrierBytes + p.x_bytes_padded + p.stages * p.stage_bytes;
     *out = p;
     *v = vv;
     *nvg = ng;
@@ -675,7 +677,7 @@ zdmmv_status dmmv_entry(int fmt, const void *w, zdmmv_layout layout, int64_t row
         a.y_stride = rows;
         a.tile_rows = vp.tile_rows;
         a.stage_bytes = vp.stage_bytes;
-        a.x_bytes_padded = 0;
+        a.x_bytes_padded = vp.x_bytes_padded;
         const int cap = std::getenv("ZDMMV_BATCH_CTAS_PER_SM") ? batch_ctas_per_sm() : 0;
         cudaError_t e = fmt == kFmtQ8 ? launch_vsplit_q8(a, vp, layout, vv, nvg, cap, st, pdl_enabled())
                                       : launch_vsplit_q4(a, vp, layout, vv, nvg, cap, st, pdl_enabled());

@@ -68,7 +68,8 @@ __device__ __forceinline__ float pair_update(const Pair<FMT, LAYOUT> &x, const P
     return acc;
 }
 
-// a.batch vectors at a.xq + v * a.xq_stride; outputs at a.y + v * a.y_stride.
+// a.batch vectors of Q8_0 blocks, contiguous at a.xq (staged in shared memory by
+// one bulk copy); outputs at a.y + v * a.y_stride.
 template <int FMT, int LAYOUT, int LPR, int PPL, int V, int NVG, int STAGES>
 __global__ void __launch_bounds__(kTmaThreads, 3) dmmv_vsplit_kernel(const DmmvArgs a) {
     using P = Pair<FMT, LAYOUT>;
@@ -84,7 +85,9 @@ __global__ void __launch_bounds__(kTmaThreads, 3) dmmv_vsplit_kernel(const DmmvA
     extern __shared__ __align__(128) uint8_t smem[];
     uint64_t *full = reinterpret_cast<uint64_t *>(smem);
     uint64_t *empty = full + STAGES;
-    uint8_t *stage0 = smem + kBarrierBytes;
+    uint64_t *xbar = empty + STAGES;
+    uint8_t *xs = smem + kBarrierBytes;  // the batch's Q8_0 activation blocks, one bulk copy
+    uint8_t *stage0 = xs + a.x_bytes_padded;
 
     const int tid = threadIdx.x;
     const int64_t rows = a.rows;
@@ -103,6 +106,7 @@ __global__ void __launch_bounds__(kTmaThreads, 3) dmmv_vsplit_kernel(const DmmvA
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], kWarps);
         }
+        mbar_init(xbar, 1);
         fence_barrier_init();
     }
     __syncthreads();
@@ -114,6 +118,12 @@ __global__ void __launch_bounds__(kTmaThreads, 3) dmmv_vsplit_kernel(const DmmvA
         const int npre = ntiles < STAGES ? ntiles : STAGES;
         for (int t = 0; t < npre; ++t) issue_tile<FMT, LAYOUT>(a, a.w, r0, r1, t, t, stage0, full, wpol);
         int issued = npre;
+        pdl_wait();  // the activations may be written by the preceding kernel
+        {
+            const uint32_t xbytes = static_cast<uint32_t>(a.batch) * static_cast<uint32_t>(nb) * 34u;
+            mbar_arrive_expect_tx(xbar, xbytes);
+            bulk_copy_g2s(xs, a.xq, xbytes, xbar, l2_evict_last_policy());
+        }
         bool ok = true;
         for (int t = npre; t < ntiles; ++t) {
             const int s = t % STAGES;
@@ -130,6 +140,7 @@ __global__ void __launch_bounds__(kTmaThreads, 3) dmmv_vsplit_kernel(const DmmvA
             const int t_last = (issued - 1 - s) >= 0 ? ((issued - 1 - s) / STAGES) * STAGES + s : -1;
             if (t_last >= 0) (void)mbar_wait(&full[s], static_cast<uint32_t>(t_last / STAGES) & 1u);
         }
+        (void)mbar_wait(xbar, 0);
         return;
     }
 
@@ -140,21 +151,26 @@ __global__ void __launch_bounds__(kTmaThreads, 3) dmmv_vsplit_kernel(const DmmvA
     const int rg = (warp / NVG) * kGroupsPerWarp + lane / LPR;   // row group within it
     const int l = lane % LPR;
     const int npairs = nb >> 1;
-    pdl_wait();  // activations and outputs may belong to the preceding kernel
-    // this warp's vectors, straight from global memory (small and L2-resident)
+    pdl_wait();  // outputs may still be read by the preceding kernel
+    // waits are warp-uniform so a timeout can never split a warp before its shuffles
+    if (!__all_sync(0xffffffffu, mbar_wait(xbar, 0))) {
+        if (lane == 0) atomicOr(a.fault, 1u);
+        return;
+    }
+    // this warp's vectors, from the staged activation blocks
     P xr[V][PPL];
     bool live[V];
 #pragma unroll
     for (int v = 0; v < V; ++v) {
         const int vec = vg * V + v;
         live[v] = vec < a.batch;
-        const uint8_t *xv = a.xq + static_cast<int64_t>(live[v] ? vec : 0) * a.xq_stride;
+        const uint32_t xv = smem_addr(xs) + static_cast<uint32_t>((live[v] ? vec : 0) * nb * 34);
 #pragma unroll
         for (int j = 0; j < PPL; ++j) {
             const int p = owned_pair<LPR>(l, j);
             uint32_t w17[17];
             if (p < npairs) {
-                load_x_pair_words(xv, p, w17);
+                load_x_pair_words_smem(xv, p, w17);
             } else {
 #pragma unroll
                 for (int k = 0; k < 17; ++k) w17[k] = 0;
@@ -271,13 +287,14 @@ struct VsplitInst {
     }
 };
 
-// p.lpr / p.ppl as in the single-vector plan; v vectors per warp, nvg groups; STAGES 3.
+// p.lpr / p.ppl as in the single-vector plan; v vectors per warp, nvg groups; p.stages 2 or 3.
 template <int FMT, int LAYOUT>
 cudaError_t launch_vsplit_layout(const DmmvArgs &a, const TmaPlan &p, int v, int nvg, int max_per_sm,
                                  cudaStream_t st, bool pdl) {
-#define ZDMMV_VS(LPR_, PPL_, V_, NVG_)                                              \
-    if (p.lpr == LPR_ && p.ppl == PPL_ && v == V_ && nvg == NVG_)                   \
-        return VsplitInst<FMT, LAYOUT, LPR_, PPL_, V_, NVG_, 3>::launch(a, p, max_per_sm, st, pdl);
+#define ZDMMV_VS(LPR_, PPL_, V_, NVG_)                                                      \
+    if (p.lpr == LPR_ && p.ppl == PPL_ && v == V_ && nvg == NVG_)                           \
+        return p.stages == 3 ? VsplitInst<FMT, LAYOUT, LPR_, PPL_, V_, NVG_, 3>::launch(a, p, max_per_sm, st, pdl) \
+                             : VsplitInst<FMT, LAYOUT, LPR_, PPL_, V_, NVG_, 2>::launch(a, p, max_per_sm, st, pdl);
 #define ZDMMV_VS_ALL(LPR_, PPL_) \
     ZDMMV_VS(LPR_, PPL_, 1, 2) ZDMMV_VS(LPR_, PPL_, 1, 4) ZDMMV_VS(LPR_, PPL_, 2, 1) ZDMMV_VS(LPR_, PPL_, 2, 2) \
     ZDMMV_VS(LPR_, PPL_, 2, 4)
