@@ -63,6 +63,11 @@ def test_dense_workload_full_size(cfg):
     y_ref, e_ref = oracle.dmmv(cfg.fmt, w, cfg.rows, cfg.cols, xq_ref)
     check(y, y_ref, e_ref)
     sampled_sums(cfg, w, xq_ref, wd, xqd)
+    # the headline step's fused entry point (quantization inside the DMMV launch): the same bits
+    yf = torch.full((cfg.rows,), float("nan"), device="cuda")
+    Z.dmmv_f32(cfg.fmt, wd, cfg.rows, cfg.cols, dev(x), y=yf)
+    torch.cuda.synchronize()
+    assert torch.equal(yf, y)
     # the greedy pick with the fused argmax epilogue: the first index of the
     # kernel's own logits' maximum, and a valid argmax of the oracle's
     i = int(Z.dmmv_argmax(cfg.fmt, wd, cfg.rows, cfg.cols, xqd).item())
@@ -140,3 +145,73 @@ def test_large_matrix_sampled_rows():
     y_ref, e_ref = oracle.dmmv(synth.Q4_0, w.reshape(rows, rb)[pick].reshape(-1), len(pick), cols, xq_ref)
     ok, worst = oracle.within_tolerance(yh[pick], y_ref, e_ref)
     assert ok, worst
+
+
+def _swiglu_bound(g_ref, u_ref, e_g, e_u, h_ref):
+    tg, tu = 1e-5 * e_g + 1e-6, 1e-5 * e_u + 1e-6
+    silu = g_ref / (1.0 + np.exp(-g_ref))
+    return 1.1 * tg * np.abs(u_ref) + np.abs(silu) * tu + 1.1 * tg * tu + 16 * 2.0 ** -24 * np.abs(h_ref) + 1e-12
+
+
+def test_moe_gate_up_swiglu_full_size():
+    """The MoE workload's gate and up projections with the SwiGLU epilogue, in the
+    launch the benchmark times: h = silu(G x) * (U x) for the 9 selected experts."""
+    m = synth.MOE
+    gate = synth.weight_blocks(synth.Q4_0, m.n_slots * m.ffn, m.hidden, seed=m.seed, stream=synth.S_WEIGHT)
+    up = synth.weight_blocks(synth.Q4_0, m.n_slots * m.ffn, m.hidden, seed=m.seed, stream=synth.S_WEIGHT2)
+    idx = synth.expert_indices(m.seed, m.n_routed, m.top_k)
+    x = synth.activations(m.hidden, seed=m.seed)
+    gu_per = m.gate_up_bytes()
+    gd, ud, idx_d = dev(gate), dev(up), dev(idx)
+    xq = Z.quantize_act_q8_0(dev(x))
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    h = torch.full((m.n_sel, m.ffn), float("nan"), device="cuda")
+    Z.expert_swiglu(Z.Q4_0, gd, ud, m.ffn, m.hidden, xq, idx=idx_d, expert_stride=gu_per, n_experts=m.n_slots,
+                    h=h, status=st)
+    ga, ua = Z.expert_gather2(Z.Q4_0, gd, ud, gu_per, m.ffn, m.hidden, idx_d, m.n_slots, xq, 0)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    hh = h.double().cpu().numpy()
+    assert not np.isnan(hh).any()
+    g32, u32 = ga.double().cpu().numpy(), ua.double().cpu().numpy()
+    h64 = g32 / (1.0 + np.exp(-g32)) * u32
+    assert np.all(np.abs(hh - h64) <= 16 * 2.0 ** -24 * np.abs(h64) + 1e-30)
+    xq_ref = oracle.quantize_q8_0(x)
+    g_ref, e_g, _ = oracle.expert_gather(synth.Q4_0, gate, gu_per, m.ffn, m.hidden, idx, m.n_slots, xq_ref, 0)
+    u_ref, e_u, _ = oracle.expert_gather(synth.Q4_0, up, gu_per, m.ffn, m.hidden, idx, m.n_slots, xq_ref, 0)
+    h_ref = oracle.swiglu(g_ref.ravel(), u_ref.ravel()).reshape(g_ref.shape)
+    assert np.all(np.abs(hh - h_ref) <= _swiglu_bound(g_ref, u_ref, e_g, e_u, h_ref))
+
+
+def test_shared_expert_sigmoid_scale_acc_full_size():
+    """The shared expert's down projection (Q8_0 2048 x 512) accumulated into a
+    residual with the sigmoid gate, and the gate-less accumulate mode."""
+    m = synth.MOE
+    rows, cols = m.hidden, m.ffn
+    w = synth.weight_blocks(synth.Q8_0, rows, cols, seed=m.seed, stream=synth.S_WEIGHT3)
+    xq = synth.activation_blocks(cols // 32, seed=m.seed)
+    y0 = synth.activations(rows, seed=m.seed + 1, scale=0.05)
+    wd, xqd = dev(w), dev(xq)
+    d_ref, _ = oracle.dmmv(synth.Q8_0, w, rows, cols, xq)
+    for gate in (None, -0.7):
+        y = dev(y0.copy())
+        g = None if gate is None else torch.tensor([gate], dtype=torch.float32, device="cuda")
+        Z.dmmv_acc(synth.Q8_0, wd, rows, cols, xqd, y, gate=g)
+        torch.cuda.synchronize()
+        y_ref, e_ref = oracle.dmmv_acc(synth.Q8_0, w, rows, cols, xq, y0.astype(np.float64), gate=gate)
+        yh = y.double().cpu().numpy()
+        bound = 1e-5 * e_ref + 1e-6 + 4 * 2.0 ** -24 * np.abs(d_ref) + 2.0 ** -24 * np.abs(y_ref)
+        assert np.all(np.abs(yh - y_ref) <= bound)
+
+
+@pytest.mark.parametrize("cfg", [synth.DENSE_Q4_0, synth.LM_HEAD_Q4_0, synth.BATCHED_Q8_0[1]],
+                         ids=lambda c: c.name)
+def test_xf32_activation_full_size(cfg):
+    """The fp32-activation product at the workloads' full sizes (all rows)."""
+    w = synth.weight_blocks(cfg.fmt, cfg.rows, cfg.cols, seed=cfg.seed)
+    x = synth.activations(cfg.cols, seed=cfg.seed, scale=cfg.x_scale)
+    y = torch.full((cfg.rows,), float("nan"), device="cuda")
+    Z.dmmv_xf32(cfg.fmt, dev(w), cfg.rows, cfg.cols, dev(x), y=y)
+    torch.cuda.synchronize()
+    y_ref, e_ref = oracle.dmmv_xf32(cfg.fmt, w, cfg.rows, cfg.cols, x)
+    check(y, y_ref, e_ref)
