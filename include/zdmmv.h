@@ -46,6 +46,17 @@
  *    between if weights are produced on the device (zdmmv_repack's output may
  *    be used directly: its kernel never releases dependents early). Set the
  *    environment variable ZDMMV_PDL=0 to disable programmatic dependent launch.
+ *  - Launch-shape tuning, read once per process from the environment (all
+ *    optional; results are the same bits whatever they are set to unless stated):
+ *      ZDMMV_STAGE_KB           target KiB per pipeline stage (4..64, default 20)
+ *      ZDMMV_CTAS_PER_SM        CTAs per SM of the single-vector kernel (1..8;
+ *                               default 2 below 32 MB of weights per launch, else 4)
+ *      ZDMMV_BATCH_KERNEL       batched kernel: vsplit (default), stream, or slots
+ *                               (one single-vector slot per vector); "stream"
+ *                               changes the fp32 reduction order of batch > 1
+ *      ZDMMV_BATCH_SLOTS=1      the same as ZDMMV_BATCH_KERNEL=slots
+ *      ZDMMV_VSPLIT_V=1         one vector per warp in the vector-split kernel
+ *      ZDMMV_BATCH_CTAS_PER_SM  CTAs per SM of the batched kernels (1..4)
  *  - There is no CPU fallback: every result is computed by the CUDA kernels.
  *  - Inputs must be finite (a NaN or infinite activation gives unspecified
  *    codes).
