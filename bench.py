@@ -445,20 +445,47 @@ def measure_moe(steps, warmup, world, device, eager, l2_bytes):
             Z.expert_gather(Z.Q8_0, d, dn, m.hidden, m.ffn, idx, m.n_slots, xqd, (m.ffn // 32) * 34, y=yd,
                             status=st)
 
+    hq = torch.empty(m.n_sel * (m.ffn // 32) * 34, dtype=torch.uint8, device="cuda")
+
+    def step_chain():
+        # the same FFN through separate launches: SwiGLU, quantize h, down gather of h
+        for l in range(layers):
+            g, u, d = stacks[l % n_sets]
+            idx = idxs[l % len(idxs)]
+            Z.expert_swiglu(Z.Q4_0, g, u, m.ffn, m.hidden, xq, idx=idx, expert_stride=gu, n_experts=m.n_slots,
+                            h=h, status=st)
+            Z.quantize_act_q8_0(h.reshape(-1), hq)
+            Z.expert_gather(Z.Q8_0, d, dn, m.hidden, m.ffn, idx, m.n_slots, hq, (m.ffn // 32) * 34, y=yd,
+                            status=st)
+
+    ws = Z.expert_ffn_workspace(m.n_sel, m.ffn)
+
+    def step_ffn():
+        for l in range(layers):
+            g, u, d = stacks[l % n_sets]
+            idx = idxs[l % len(idxs)]
+            Z.expert_ffn(Z.Q4_0, g, u, gu, Z.Q8_0, d, dn, m.hidden, m.ffn, idx, m.n_slots, xq, y=yd,
+                         workspace=ws, status=st)
+
     nbytes = m.algorithmic_bytes()
     # the SwiGLU epilogue writes h instead of the gate and up outputs
     nbytes_swiglu = nbytes - m.n_sel * m.ffn * 4
     out = {"layers": layers, "algorithmic_bytes": nbytes,
            "note": "touched experts differ per layer; stack copies alternate (some L2 reuse possible)"}
     for name, fn, launches, nb_ in (("three_launch", step3, 3, nbytes), ("gate_up_fused", step2, 2, nbytes),
-                                    ("gate_up_swiglu", step_swiglu, 2, nbytes_swiglu)):
+                                    ("gate_up_swiglu", step_swiglu, 2, nbytes_swiglu),
+                                    ("ffn_chained_three_launch", step_chain, 3, nbytes_swiglu),
+                                    ("ffn_one_launch", step_ffn, 1, nbytes_swiglu)):
         run = graph_or_eager(fn, eager)
         ms, _ = time_fn(run, steps, warmup, world, device)
         per_layer = ms / 1e3 / (steps * layers)
         out[name] = {"us_per_token_layer": per_layer * 1e6, "gbs": nb_ / per_layer / 1e9,
                      "algorithmic_bytes": nb_,
                      "rows_per_s": m.n_sel * (2 * m.ffn + m.hidden) / per_layer, "launches_per_layer": launches}
-    out["gbs"] = max(out[k]["gbs"] for k in ("three_launch", "gate_up_fused", "gate_up_swiglu"))
+    out["ffn_one_launch"]["note"] = ("gate/up + SwiGLU and the down DMMV of the quantized SwiGLU output in one "
+                                     "launch (the down input is h, not the independent activation)")
+    out["ffn_chained_three_launch"]["note"] = "the same chained FFN as SwiGLU, quantize h, down gather"
+    out["gbs"] = max(out[k]["gbs"] for k in ("three_launch", "gate_up_fused", "gate_up_swiglu", "ffn_one_launch"))
     return out
 
 

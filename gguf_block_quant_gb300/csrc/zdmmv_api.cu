@@ -1064,6 +1064,19 @@ zdmmv_status zdmmv_dmmv_xf32(zdmmv_fmt fmt, const void *w, zdmmv_layout layout, 
     return dmmv_xf32_entry(fmt, w, layout, rows, cols, x, batch, y, reinterpret_cast<cudaStream_t>(stream));
 }
 
+size_t zdmmv_expert_ffn_workspace_bytes(int n, int64_t ffn) { return ffn_workspace_bytes(n, ffn); }
+
+zdmmv_status zdmmv_expert_ffn(zdmmv_fmt fmt_gate_up, const void *w_gate, const void *w_up,
+                              int64_t gate_up_stride_bytes, zdmmv_fmt fmt_down, const void *w_down,
+                              int64_t down_stride_bytes, int64_t hidden, int64_t ffn, const int32_t *idx, int n,
+                              int n_experts, const void *xq, float *y, void *workspace, size_t workspace_bytes,
+                              int32_t *status_dev, zdmmv_stream_t stream) {
+    return static_cast<zdmmv_status>(ffn_entry_status(fmt_gate_up, w_gate, w_up, gate_up_stride_bytes, fmt_down,
+                                                      w_down, down_stride_bytes, hidden, ffn, idx, n, n_experts, xq,
+                                                      y, workspace, workspace_bytes, status_dev,
+                                                      reinterpret_cast<cudaStream_t>(stream), pdl_enabled()));
+}
+
 zdmmv_status zdmmv_expert_swiglu(zdmmv_fmt fmt, const void *w_gate, const void *w_up, int64_t expert_stride_bytes,
                                  zdmmv_layout layout, int64_t rows, int64_t cols, const int32_t *idx, int n,
                                  int n_experts, const void *xq, int64_t xq_stride_bytes, float *h,

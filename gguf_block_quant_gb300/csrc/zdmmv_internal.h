@@ -130,6 +130,19 @@ cudaError_t launch_xf32_q4(const DmmvArgs &a, const TmaPlan &p, int layout, int 
 cudaError_t launch_xf32_plain_q8(const DmmvArgs &a, int layout, int sms, int slots, cudaStream_t st, bool pdl);
 cudaError_t launch_xf32_plain_q4(const DmmvArgs &a, int layout, int sms, int slots, cudaStream_t st, bool pdl);
 
+// The one-launch expert FFN (gate/up + SwiGLU, then down): workspace size,
+// shapes it takes, and the launcher (FfnArgs: zdmmv_ffn.cuh; the launcher fills
+// in the plan fields).
+struct FfnArgs;
+size_t ffn_workspace_bytes(int n, int64_t ffn);
+bool ffn_shape_ok(int fmt_gu, int fmt_dn, int64_t hidden, int64_t ffn);
+cudaError_t launch_ffn(int fmt_gu, int fmt_dn, FfnArgs f, int sms, cudaStream_t st, bool pdl);
+// The expert FFN entry point's checks and launch (status codes of zdmmv.h, as int).
+int ffn_entry_status(int fmt_gu, const void *w_gate, const void *w_up, int64_t gu_stride, int fmt_dn,
+                     const void *w_down, int64_t dn_stride, int64_t hidden, int64_t ffn, const int32_t *idx, int n,
+                     int n_experts, const void *xq, float *y, void *workspace, size_t workspace_bytes,
+                     int32_t *status_dev, cudaStream_t st, bool pdl);
+
 // The argmax epilogue's final pass (one CTA over n partials).
 cudaError_t launch_argmax_reduce(const uint2 *parts, int n, int32_t *argmax_out, float *max_out, cudaStream_t st,
                                  bool pdl);

@@ -65,6 +65,9 @@ _SIGS = {
                               _vp, _vp], _int),
     "zdmmv_expert_swiglu": ([_int, _vp, _vp, _i64, _int, _i64, _i64, _vp, _int, _int, _vp, _i64, _vp, _vp,
                              _vp], _int),
+    "zdmmv_expert_ffn_workspace_bytes": ([_int, _i64], ctypes.c_size_t),
+    "zdmmv_expert_ffn": ([_int, _vp, _vp, _i64, _int, _vp, _i64, _i64, _i64, _vp, _int, _int, _vp, _vp, _vp,
+                          ctypes.c_size_t, _vp, _vp], _int),
     "zdmmv_repacked_bytes": ([_int, _i64, _i64], ctypes.c_size_t),
     "zdmmv_repack": ([_int, _vp, _i64, _i64, _vp, ctypes.c_size_t, _vp], _int),
     "zdmmv_host_step_workspace_bytes": ([_i64, _i64, _int], ctypes.c_size_t),
@@ -269,6 +272,29 @@ def expert_swiglu(fmt: int, w_gate, w_up, rows: int, cols: int, xq, idx=None, ex
     _call("zdmmv_expert_swiglu", fmt, _ptr(w_gate), _ptr(w_up), expert_stride, layout, rows, cols, _ptr(idx), n,
           n_experts, _ptr(xq), xq_stride, _ptr(h), _ptr(status), _stream(stream))
     return h
+
+
+def expert_ffn_workspace(n: int, ffn: int, device="cuda"):
+    """A zero-filled workspace for expert_ffn (reusable across calls on one stream)."""
+    nbytes = lib().zdmmv_expert_ffn_workspace_bytes(n, ffn)
+    return torch.zeros(nbytes, dtype=torch.uint8, device=device)
+
+
+def expert_ffn(fmt_gate_up: int, w_gate, w_up, gate_up_stride: int, fmt_down: int, w_down, down_stride: int,
+               hidden: int, ffn: int, idx, n_experts: int, xq, y=None, workspace=None, status=None, stream=None):
+    """The selected experts' gate/up DMMVs, SwiGLU and down DMMV in one launch:
+    y[k] = D_idx[k] . q8_0(silu(G_idx[k] . x) * (U_idx[k] . x)). Returns (y, h)."""
+    if idx.dtype != torch.int32:
+        raise ValueError("expert_ffn: idx must be int32")
+    n = idx.numel()
+    y = _out(y, (n, hidden), w_gate.device)
+    if workspace is None:
+        workspace = expert_ffn_workspace(n, ffn, w_gate.device)
+    _call("zdmmv_expert_ffn", fmt_gate_up, _ptr(w_gate), _ptr(w_up), gate_up_stride, fmt_down, _ptr(w_down),
+          down_stride, hidden, ffn, _ptr(idx), n, n_experts, _ptr(xq), _ptr(y), _ptr(workspace),
+          _nbytes(workspace), _ptr(status), _stream(stream))
+    h = workspace[: 4 * n * ffn].view(torch.float32).view(n, ffn)
+    return y, h
 
 
 def repacked_bytes(fmt: int, rows: int, cols: int) -> int:

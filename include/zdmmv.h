@@ -57,6 +57,8 @@
  *      ZDMMV_BATCH_SLOTS=1      the same as ZDMMV_BATCH_KERNEL=slots
  *      ZDMMV_VSPLIT_V=1         one vector per warp in the vector-split kernel
  *      ZDMMV_BATCH_CTAS_PER_SM  CTAs per SM of the batched kernels (1..4)
+ *      ZDMMV_FFN_STAGES=3       three pipeline stages in zdmmv_expert_ffn (default 2)
+ *      ZDMMV_FFN_CTAS_PER_SM    CTAs per SM of zdmmv_expert_ffn (1..8, default up to 4)
  *  - There is no CPU fallback: every result is computed by the CUDA kernels.
  *  - Inputs must be finite (a NaN or infinite activation gives unspecified
  *    codes).
@@ -233,6 +235,43 @@ zdmmv_status zdmmv_expert_swiglu(zdmmv_fmt fmt, const void *w_gate, const void *
                                  int64_t rows, int64_t cols, const int32_t *idx, int n,
                                  int n_experts, const void *xq, int64_t xq_stride_bytes,
                                  float *h, int32_t *status_dev, zdmmv_stream_t stream);
+
+/* The selected experts' whole FFN in ONE launch: for k < n, with e = idx[k],
+ *   h_k = silu(G_e . x) * (U_e . x)            (gate/up DMMVs, SwiGLU epilogue)
+ *   y_k = D_e . q8_0(h_k)                       (down DMMV of the quantized h_k)
+ * the MoE step's gate/up DMMV, swiglu and down DMMV ("CUDA backend for ZINC",
+ * "5. The target model & milestone ordering", M1) as one dispatch for all
+ * experts (habr article, "Gap analysis"; "RTX 5090: Batched Prefill & CUDA
+ * Graphs in ZINC", "What's next"). One grid holds gate/up CTAs and down CTAs;
+ * the down CTAs stream their weights while the gate/up CTAs run, then wait
+ * (bounded) on a per-expert counter in the workspace before reading h_k.
+ *   fmt_gate_up  format of the gate and up stacks (Q4_0 or Q8_0), GGUF layout;
+ *                expert e's [ffn x hidden] matrices at w_gate / w_up +
+ *                e*gate_up_stride_bytes.
+ *   fmt_down     format of the down stack, GGUF layout; expert e's [hidden x ffn]
+ *                matrix at w_down + e*down_stride_bytes. Strides are 16-byte
+ *                multiples (>= the matrix size when n_experts > 1).
+ *   hidden       a multiple of 256, at most 4096; ffn a multiple of 256, at most
+ *                2048 (else ERR_SHAPE). n == 0 is a no-op.
+ *   idx, n, n_experts, status_dev   as zdmmv_expert_gather (n <= 4096); a bad
+ *                index gives NaN rows of h_k and y_k.
+ *   xq           device Q8_0 blocks of the hidden activation, shared by all slots.
+ *   y            device fp32 [n][hidden].
+ *   workspace    device, 256-byte aligned, >= zdmmv_expert_ffn_workspace_bytes(n,
+ *                ffn) bytes, ZERO-FILLED before its first use; every call leaves
+ *                its counters zero again. Bytes [0, 4*n*ffn) hold h after the
+ *                call. One workspace per call in flight. After a call that
+ *                reported ZDMMV_FAULT_WAIT_TIMEOUT, zero it again.
+ * h_k is the zdmmv_expert_swiglu value and y_k the zdmmv_expert_gather value on
+ * zdmmv_quantize_act_q8_0(h_k), bit for bit.
+ * Errors: ERR_NULL, ERR_SHAPE, ERR_ALIGN, ERR_FORMAT, ERR_SIZE, ERR_CUDA. */
+size_t zdmmv_expert_ffn_workspace_bytes(int n, int64_t ffn);
+zdmmv_status zdmmv_expert_ffn(zdmmv_fmt fmt_gate_up, const void *w_gate, const void *w_up,
+                              int64_t gate_up_stride_bytes, zdmmv_fmt fmt_down, const void *w_down,
+                              int64_t down_stride_bytes, int64_t hidden, int64_t ffn,
+                              const int32_t *idx, int n, int n_experts, const void *xq, float *y,
+                              void *workspace, size_t workspace_bytes, int32_t *status_dev,
+                              zdmmv_stream_t stream);
 
 /* LM-head DMMV with a fused argmax epilogue: the greedy pick over the logits
  * W.x without writing them (the M1 decode chain ends "LM head -> argmax":

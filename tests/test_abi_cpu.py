@@ -115,6 +115,21 @@ def test_other_argument_checks(L):
     assert xf(8, FAKE, 0, 4, 48, FAKE, 1, FAKE, None) == 2                              # cols % 32
     assert xf(8, FAKE, 0, 4, 64, FAKE, 0, FAKE, None) == 2                              # batch 0
     assert xf(8, FAKE, 0, 4, 64, FAKE + 4, 1, FAKE, None) == 3                          # x not 16-byte aligned
+    ff = L.zdmmv_expert_ffn
+    wsb = L.zdmmv_expert_ffn_workspace_bytes(9, 512)
+    assert wsb >= 9 * 512 * 4 + 2 * 9 * 4
+    args = lambda **k: [k.get("fgu", 2), FAKE, FAKE, 1 << 21, k.get("fdn", 8), FAKE, 1 << 21,
+                        k.get("hidden", 2048), k.get("ffn", 512), FAKE, k.get("n", 9), 129, FAKE, FAKE,
+                        k.get("ws", FAKE), k.get("wsb", wsb), None, None]
+    assert ff(*args(fgu=3)) == 5
+    assert ff(*args(hidden=2048 + 32)) == 2          # off the pipelined widths
+    assert ff(*args(ffn=4096)) == 2                  # down rows wider than the kernel takes
+    assert ff(*args(n=0)) == 0
+    assert ff(*args(ws=None)) == 1
+    assert ff(*args(ws=FAKE + 16)) == 3              # workspace not 256-byte aligned
+    assert ff(*args(wsb=wsb - 1)) == 6
+    small = [2, FAKE, FAKE, 1 << 16, 8, FAKE, 1 << 21, 2048, 512, FAKE, 9, 129, FAKE, FAKE, FAKE, wsb, None, None]
+    assert ff(*small) == 2                           # experts of the gate/up stack overlap
     sw = L.zdmmv_expert_swiglu
     assert sw(2, FAKE, FAKE, 1 << 16, 0, 4, 160, FAKE, 2, 8, FAKE, 0, FAKE, None, None) == 2  # off the pipelined widths
     assert sw(2, FAKE, FAKE, 0, 0, 4, 2048, None, 2, 0, FAKE, 0, FAKE, None, None) == 2       # no index, n > 1

@@ -640,3 +640,74 @@ def test_xf32_ragged_tiles_and_zero_rows():
         check_y(y, y_ref, e_ref)
     # rows == 0 launches nothing and succeeds
     Z.dmmv_xf32(fmt, dev(synth.weight_blocks(fmt, 1, cols, seed=1)), 0, cols, dev(x), y=nan_out(1))
+
+
+# ------------------------------------------------- one-launch expert FFN
+def _ffn_case(fmt_gu, fmt_dn, hidden, ffn, n_exp, idx, seed):
+    bgu = 18 if fmt_gu == Q4_0 else 34
+    bdn = 18 if fmt_dn == Q4_0 else 34
+    gu_per = ffn * hidden // 32 * bgu
+    dn_per = hidden * ffn // 32 * bdn
+    g = synth.weight_blocks(fmt_gu, n_exp * ffn, hidden, seed=seed)
+    u = synth.weight_blocks(fmt_gu, n_exp * ffn, hidden, seed=seed, stream=synth.S_WEIGHT2)
+    d = synth.weight_blocks(fmt_dn, n_exp * hidden, ffn, seed=seed, stream=synth.S_WEIGHT3)
+    x = synth.activations(hidden, seed=seed + 1)
+    return dict(g=g, u=u, d=d, x=x, gu_per=gu_per, dn_per=dn_per, idx=np.asarray(idx, dtype=np.int32))
+
+
+@pytest.mark.parametrize("fmt_gu,fmt_dn,hidden,ffn", [(Q4_0, Q8_0, 2048, 512), (Q8_0, Q8_0, 4096, 1024),
+                                                      (Q4_0, Q4_0, 1024, 256), (Q8_0, Q4_0, 2560, 2048)])
+def test_expert_ffn_equals_swiglu_then_down_gather(fmt_gu, fmt_dn, hidden, ffn):
+    n_exp = 6
+    c = _ffn_case(fmt_gu, fmt_dn, hidden, ffn, n_exp, [5, 0, 3, 3, 2, 1, 4], seed=hidden + ffn)
+    gd, ud, dd, ia = dev(c["g"]), dev(c["u"]), dev(c["d"]), dev(c["idx"])
+    xq = Z.quantize_act_q8_0(dev(c["x"]))
+    n = len(c["idx"])
+    ws = Z.expert_ffn_workspace(n, ffn)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    outs = []
+    for _ in range(3):  # the counters are reset by every call: repeated calls agree
+        y, h = Z.expert_ffn(fmt_gu, gd, ud, c["gu_per"], fmt_dn, dd, c["dn_per"], hidden, ffn, ia, n_exp, xq,
+                            y=nan_out(n, hidden), workspace=ws, status=st)
+        torch.cuda.synchronize()
+        outs.append((y.clone(), h.clone()))
+    assert st.item() == 0
+    for y, h in outs[1:]:
+        assert torch.equal(y, outs[0][0]) and torch.equal(h, outs[0][1])
+    y, h = outs[0]
+    # the same results through the separate entry points, bit for bit
+    h2 = Z.expert_swiglu(fmt_gu, gd, ud, ffn, hidden, xq, idx=ia, expert_stride=c["gu_per"], n_experts=n_exp)
+    hq = Z.quantize_act_q8_0(h2.reshape(-1))
+    y2 = Z.expert_gather(fmt_dn, dd, c["dn_per"], hidden, ffn, ia, n_exp, hq, ffn // 32 * 34)
+    torch.cuda.synchronize()
+    assert torch.equal(h, h2)
+    assert torch.equal(y, y2)
+    # against the oracle: the down DMMV of the kernel's own h, quantized by the oracle
+    hh = h.cpu().numpy()
+    hq_ref = oracle.quantize_q8_0(hh.reshape(-1))
+    assert np.array_equal(hq.cpu().numpy(), hq_ref)
+    y_ref, e_ref, s = oracle.expert_gather(fmt_dn, c["d"], c["dn_per"], hidden, ffn, c["idx"], n_exp, hq_ref,
+                                           ffn // 32 * 34)
+    assert s == 0
+    check_y(y, y_ref, e_ref)
+
+
+def test_expert_ffn_bad_index_then_reuse_workspace():
+    fmt_gu, fmt_dn, hidden, ffn, n_exp = Q4_0, Q8_0, 2048, 512, 4
+    c = _ffn_case(fmt_gu, fmt_dn, hidden, ffn, n_exp, [1, 9, 0], seed=77)   # 9 is out of range
+    gd, ud, dd = dev(c["g"]), dev(c["u"]), dev(c["d"])
+    xq = Z.quantize_act_q8_0(dev(c["x"]))
+    ws = Z.expert_ffn_workspace(3, ffn)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    y, h = Z.expert_ffn(fmt_gu, gd, ud, c["gu_per"], fmt_dn, dd, c["dn_per"], hidden, ffn, dev(c["idx"]), n_exp,
+                        xq, y=nan_out(3, hidden), workspace=ws, status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 1
+    assert torch.isnan(y[1]).all() and torch.isnan(h[1]).all()
+    assert not torch.isnan(y[0]).any() and not torch.isnan(y[2]).any()
+    # the workspace's counters are back to zero: a second call with good indices is right
+    good = dev(np.array([1, 3, 0], dtype=np.int32))
+    y2, _ = Z.expert_ffn(fmt_gu, gd, ud, c["gu_per"], fmt_dn, dd, c["dn_per"], hidden, ffn, good, n_exp, xq,
+                         y=nan_out(3, hidden), workspace=ws)
+    torch.cuda.synchronize()
+    assert torch.equal(y2[0], y[0]) and torch.equal(y2[2], y[2]) and not torch.isnan(y2[1]).any()
