@@ -537,7 +537,6 @@ __global__ void __launch_bounds__(256) block_sums_kernel(const uint8_t *__restri
         sums[row * nb + 2 * p + 1] = sb;
     } else {
         if (t >= rows * nb) return;
-        const int64_t row = t / nb;
         const int b = static_cast<int>(t % nb);
         uint32_t q[8], xw[8];
         float dw, dx;
@@ -546,7 +545,6 @@ __global__ void __launch_bounds__(256) block_sums_kernel(const uint8_t *__restri
         else
             Block<FMT>::load_repacked(w + t * kQB, w + rows * nb * kQB + t * 2, q, dw);
         load_x_block(xq + static_cast<int64_t>(b) * 34, xw, dx);
-        (void)row;
         sums[t] = Block<FMT>::dot(q, xw);
     }
 }
@@ -661,8 +659,6 @@ zdmmv_status dmmv_entry(int fmt, const void *w, zdmmv_layout layout, int64_t row
     a.y = y;
     a.rows = rows;
     a.nb = static_cast<int32_t>(cols / kQK);
-    const int64_t cols_pad = cols;
-    (void)cols_pad;
     BatchPlan bp{};
     TmaPlan vp{};
     int vv = 0, nvg = 0;

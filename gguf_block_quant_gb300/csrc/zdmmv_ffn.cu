@@ -27,37 +27,34 @@ cudaError_t dispatch_dn_st(const FfnArgs &f, int ldn, int pdn, int smem, cudaStr
     return cudaErrorInvalidConfiguration;
 }
 
-// pipeline depth of the FFN launch (2 or 3): the plan's choice, passed through a global
-// set by launch_ffn just before dispatching (one host thread per call)
-thread_local int t_ffn_stages = 2;
-
+// stages: the pipeline depth of the launch (2 or 3)
 template <int FGU, int LGU, int PGU, int FDN>
-cudaError_t dispatch_dn(const FfnArgs &f, int ldn, int pdn, int smem, cudaStream_t st, bool pdl, bool query,
-                        int *occ) {
-    if (t_ffn_stages == 3) return dispatch_dn_st<FGU, LGU, PGU, FDN, 3>(f, ldn, pdn, smem, st, pdl, query, occ);
+cudaError_t dispatch_dn(const FfnArgs &f, int stages, int ldn, int pdn, int smem, cudaStream_t st, bool pdl,
+                        bool query, int *occ) {
+    if (stages == 3) return dispatch_dn_st<FGU, LGU, PGU, FDN, 3>(f, ldn, pdn, smem, st, pdl, query, occ);
     return dispatch_dn_st<FGU, LGU, PGU, FDN, 2>(f, ldn, pdn, smem, st, pdl, query, occ);
 }
 
 template <int FGU, int FDN>
-cudaError_t dispatch_gu(const FfnArgs &f, int lgu, int pgu, int ldn, int pdn, int smem, cudaStream_t st, bool pdl,
-                        bool query, int *occ) {
-    if (lgu == 8 && pgu == 1) return dispatch_dn<FGU, 8, 1, FDN>(f, ldn, pdn, smem, st, pdl, query, occ);
-    if (lgu == 16 && pgu == 1) return dispatch_dn<FGU, 16, 1, FDN>(f, ldn, pdn, smem, st, pdl, query, occ);
-    if (lgu == 32 && pgu == 1) return dispatch_dn<FGU, 32, 1, FDN>(f, ldn, pdn, smem, st, pdl, query, occ);
-    if (lgu == 32 && pgu == 2) return dispatch_dn<FGU, 32, 2, FDN>(f, ldn, pdn, smem, st, pdl, query, occ);
+cudaError_t dispatch_gu(const FfnArgs &f, int stages, int lgu, int pgu, int ldn, int pdn, int smem, cudaStream_t st,
+                        bool pdl, bool query, int *occ) {
+    if (lgu == 8 && pgu == 1) return dispatch_dn<FGU, 8, 1, FDN>(f, stages, ldn, pdn, smem, st, pdl, query, occ);
+    if (lgu == 16 && pgu == 1) return dispatch_dn<FGU, 16, 1, FDN>(f, stages, ldn, pdn, smem, st, pdl, query, occ);
+    if (lgu == 32 && pgu == 1) return dispatch_dn<FGU, 32, 1, FDN>(f, stages, ldn, pdn, smem, st, pdl, query, occ);
+    if (lgu == 32 && pgu == 2) return dispatch_dn<FGU, 32, 2, FDN>(f, stages, ldn, pdn, smem, st, pdl, query, occ);
     return cudaErrorInvalidConfiguration;
 }
 
-cudaError_t dispatch(int fmt_gu, int fmt_dn, const FfnArgs &f, int lgu, int pgu, int ldn, int pdn, int smem,
-                     cudaStream_t st, bool pdl, bool query, int *occ) {
+cudaError_t dispatch(int fmt_gu, int fmt_dn, const FfnArgs &f, int stages, int lgu, int pgu, int ldn, int pdn,
+                     int smem, cudaStream_t st, bool pdl, bool query, int *occ) {
     if (fmt_gu == kFmtQ4 && fmt_dn == kFmtQ8)
-        return dispatch_gu<kFmtQ4, kFmtQ8>(f, lgu, pgu, ldn, pdn, smem, st, pdl, query, occ);
+        return dispatch_gu<kFmtQ4, kFmtQ8>(f, stages, lgu, pgu, ldn, pdn, smem, st, pdl, query, occ);
     if (fmt_gu == kFmtQ8 && fmt_dn == kFmtQ8)
-        return dispatch_gu<kFmtQ8, kFmtQ8>(f, lgu, pgu, ldn, pdn, smem, st, pdl, query, occ);
+        return dispatch_gu<kFmtQ8, kFmtQ8>(f, stages, lgu, pgu, ldn, pdn, smem, st, pdl, query, occ);
     if (fmt_gu == kFmtQ4 && fmt_dn == kFmtQ4)
-        return dispatch_gu<kFmtQ4, kFmtQ4>(f, lgu, pgu, ldn, pdn, smem, st, pdl, query, occ);
+        return dispatch_gu<kFmtQ4, kFmtQ4>(f, stages, lgu, pgu, ldn, pdn, smem, st, pdl, query, occ);
     if (fmt_gu == kFmtQ8 && fmt_dn == kFmtQ4)
-        return dispatch_gu<kFmtQ8, kFmtQ4>(f, lgu, pgu, ldn, pdn, smem, st, pdl, query, occ);
+        return dispatch_gu<kFmtQ8, kFmtQ4>(f, stages, lgu, pgu, ldn, pdn, smem, st, pdl, query, occ);
     return cudaErrorInvalidConfiguration;
 }
 
@@ -150,10 +147,10 @@ cudaError_t launch_ffn(int fmt_gu, int fmt_dn, FfnArgs f, int sms, cudaStream_t 
         const int n = e ? std::atoi(e) : 0;
         return (n >= 1 && n <= 8) ? n : 4;
     }();
-    t_ffn_stages = env_stages;
     const int smem = kBarrierBytes + f.x_bytes_padded + env_stages * pitch;
     int occ = 0;
-    cudaError_t e = dispatch(fmt_gu, fmt_dn, f, pg.lpr, pg.ppl, pd.lpr, pd.ppl, smem, st, pdl, true, &occ);
+    cudaError_t e = dispatch(fmt_gu, fmt_dn, f, env_stages, pg.lpr, pg.ppl, pd.lpr, pd.ppl, smem, st, pdl, true,
+                             &occ);
     if (e != cudaSuccess) return e;
     if (occ < 1) return cudaErrorInvalidConfiguration;
     if (occ > env_cap) occ = env_cap;
@@ -164,7 +161,7 @@ cudaError_t launch_ffn(int fmt_gu, int fmt_dn, FfnArgs f, int sms, cudaStream_t 
     if (per > min_rows) per = static_cast<int>(min_rows);
     f.gu_per = per;
     f.dn_per = per;
-    return dispatch(fmt_gu, fmt_dn, f, pg.lpr, pg.ppl, pd.lpr, pd.ppl, smem, st, pdl, false, &occ);
+    return dispatch(fmt_gu, fmt_dn, f, env_stages, pg.lpr, pg.ppl, pd.lpr, pd.ppl, smem, st, pdl, false, &occ);
 }
 
 }  // namespace zdmmv
