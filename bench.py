@@ -753,6 +753,27 @@ def profile_mode(name: str):
     from gguf_block_quant_gb300 import synth
     from gguf_block_quant_gb300 import zdmmv as Z
     Z.lib()
+    if name == synth.MOE.name:
+        # the MoE step three ways, 3 times: gate/up+SwiGLU, quantize h, down gather; then the one-launch FFN
+        m = synth.MOE
+        gate = torch.from_numpy(synth.weight_blocks(synth.Q4_0, m.n_slots * m.ffn, m.hidden, seed=m.seed)).cuda()
+        up = torch.from_numpy(synth.weight_blocks(synth.Q4_0, m.n_slots * m.ffn, m.hidden, seed=m.seed,
+                                                  stream=synth.S_WEIGHT2)).cuda()
+        down = torch.from_numpy(synth.weight_blocks(synth.Q8_0, m.n_slots * m.hidden, m.ffn, seed=m.seed,
+                                                    stream=synth.S_WEIGHT3)).cuda()
+        idx = torch.from_numpy(synth.expert_indices(m.seed, m.n_routed, m.top_k)).cuda()
+        xq = Z.quantize_act_q8_0(torch.from_numpy(synth.activations(m.hidden, seed=m.seed)).cuda())
+        gu, dn = m.gate_up_bytes(), m.down_bytes()
+        ws = Z.expert_ffn_workspace(m.n_sel, m.ffn)
+        for _ in range(3):
+            h = Z.expert_swiglu(Z.Q4_0, gate, up, m.ffn, m.hidden, xq, idx=idx, expert_stride=gu,
+                                n_experts=m.n_slots)
+            hq = Z.quantize_act_q8_0(h.reshape(-1))
+            Z.expert_gather(Z.Q8_0, down, dn, m.hidden, m.ffn, idx, m.n_slots, hq, (m.ffn // 32) * 34)
+            Z.expert_ffn(Z.Q4_0, gate, up, gu, Z.Q8_0, down, dn, m.hidden, m.ffn, idx, m.n_slots, xq, workspace=ws)
+        torch.cuda.synchronize()
+        print(json.dumps({"profile": name, "fault": Z.device_status()}))
+        return
     workloads = {c.name: c for c in (synth.SSM_ALPHA_BETA, synth.DENSE_Q4_0, synth.LM_HEAD_Q4_0,
                                      *synth.BATCHED_Q8_0.values())}
     cfg = workloads[name]
