@@ -581,6 +581,37 @@ def e2e_dense(cfg, layers, steps, warmup, world, device, eager=False):
                       ": pinned H2D of the step's activations, fused quantize + DMMV per layer, pinned D2H of the outputs"}
 
 
+def e2e_host_step(cfg, layers, steps, warmup, world, device, eager=False):
+    """End to end through the host-buffer C-ABI call: one zdmmv_host_step per
+    layer, each copying its layer's fp32 activation from pinned host memory,
+    running the fused quantize + DMMV and copying the layer's output back."""
+    import numpy as np
+    import torch
+    from gguf_block_quant_gb300 import synth
+    from gguf_block_quant_gb300 import zdmmv as Z
+    w = torch.from_numpy(synth.weight_blocks(cfg.fmt, cfg.rows, cfg.cols, seed=cfg.seed)).cuda()
+    ws_ = [w] + [w.clone() for _ in range(layers - 1)]
+    x = synth.activations(cfg.cols, seed=cfg.seed, scale=cfg.x_scale)
+    xh = torch.from_numpy(np.ascontiguousarray(np.tile(x, (layers, 1)))).pin_memory()
+    yh = torch.empty(layers, cfg.rows, dtype=torch.float32).pin_memory()
+    wsb = Z.host_step_workspace_bytes(cfg.rows, cfg.cols)
+    work = [torch.empty(wsb, dtype=torch.uint8, device="cuda") for _ in range(layers)]
+
+    def step():
+        for l in range(layers):
+            Z.host_step(cfg.fmt, ws_[l], cfg.rows, cfg.cols, xh[l], yh[l], work[l])
+
+    run = graph_or_eager(step, eager)
+    ms, _ = time_fn(run, steps, warmup, world, device)
+    per_step = ms / 1e3 / steps
+    return {"value": layers * cfg.algorithmic_bytes() * world / per_step / 1e9, "unit": "GB/s",
+            "h2d_bytes_per_step": xh.numel() * 4, "d2h_bytes_per_step": yh.numel() * 4,
+            "ms_per_step": ms / steps,
+            "launch": ("eager" if eager else "cuda_graph replay") +
+                      ": zdmmv_host_step per layer (pinned H2D of the layer's activation, fused quantize + DMMV, "
+                      "pinned D2H of its output)"}
+
+
 def gpu_arm(args):
     import torch
     world, rank, local = dist_setup(args)
@@ -622,6 +653,9 @@ def gpu_arm(args):
     torch.cuda.empty_cache()
 
     e2e = e2e_dense(cfg, min(layers, 64), max(3, args.steps // 4), args.warmup, world, device, args.eager)
+    # the host-buffer C-ABI call made once per layer (each layer's copies in its own call)
+    e2e["per_layer_host_step"] = e2e_host_step(cfg, min(layers, 64), max(3, args.steps // 8), args.warmup, world,
+                                               device, args.eager)
 
     workloads = {}
     if not args.no_extra:

@@ -1138,9 +1138,14 @@ zdmmv_status zdmmv_host_step(zdmmv_fmt fmt, const void *w, zdmmv_layout layout, 
     float *yd = reinterpret_cast<float *>(ws + xb + qb);
     cudaError_t e = cudaMemcpyAsync(xd, x_host, static_cast<size_t>(batch) * cols * 4, cudaMemcpyHostToDevice, st);
     if (e != cudaSuccess) return ZDMMV_ERR_CUDA;
-    zdmmv_status s = zdmmv_quantize_act_q8_0(xd, static_cast<int64_t>(batch) * cols, xqd, stream);
-    if (s != ZDMMV_OK) return s;
-    s = dmmv_entry(fmt, w, layout, rows, cols, xqd, batch, yd, st);
+    zdmmv_status s;
+    if (tma_shape_ok(fmt, cols) && batch == 1) {
+        // quantize + DMMV in one launch: the same bits as the quantizer followed by the DMMV
+        s = dmmv_f32_entry(fmt, w, layout, rows, cols, xd, batch, yd, st);
+    } else {
+        s = zdmmv_quantize_act_q8_0(xd, static_cast<int64_t>(batch) * cols, xqd, stream);
+        if (s == ZDMMV_OK) s = dmmv_entry(fmt, w, layout, rows, cols, xqd, batch, yd, st);
+    }
     if (s != ZDMMV_OK) return s;
     if (rows > 0) {
         e = cudaMemcpyAsync(y_host, yd, static_cast<size_t>(batch) * rows * 4, cudaMemcpyDeviceToHost, st);

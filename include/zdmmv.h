@@ -378,9 +378,10 @@ zdmmv_status zdmmv_repack(zdmmv_fmt fmt, const void *src, int64_t rows, int64_t 
 
 /* One decode step with HOST activations and outputs: copies x_host
  * ([batch][cols] fp32; pinned memory gives asynchronous copies) to the device,
- * quantizes it, runs the DMMV on the resident weights and copies y back to
- * y_host ([batch][rows] fp32), all ordered on `stream`. The caller synchronizes
- * the stream before reading y_host.
+ * quantizes it and runs the DMMV on the resident weights (one fused launch, as
+ * zdmmv_dmmv_f32, for a single vector on the pipelined widths) and copies y back
+ * to y_host ([batch][rows] fp32), all ordered on `stream`. The caller
+ * synchronizes the stream before reading y_host.
  *   workspace_dev  device, >= zdmmv_host_step_workspace_bytes(rows, cols, batch),
  *                  16-byte aligned; holds x, its Q8_0 blocks and y.
  * Errors: as zdmmv_q8_0_batched, plus ERR_SIZE. */
