@@ -12,6 +12,7 @@
 #include "zdmmv.h"
 #include "zdmmv_device.cuh"
 #include "zdmmv_internal.h"
+#include "zdmmv_mma.h"
 
 namespace zdmmv {
 
@@ -171,13 +172,16 @@ TmaPlan tma_plan(int fmt, int layout, int64_t cols, int halves) {
 
 namespace {
 // Batched kernel choice (environment ZDMMV_BATCH_KERNEL): "vsplit" (default),
-// "stream" (dmmv_batch_kernel) or "slots" (single-vector slots, as ZDMMV_BATCH_SLOTS=1).
+// "mma" (the integer tensor-core kernel where it takes the shape, else the
+// vector split; slower on this part, kept for the measurement), "stream"
+// (dmmv_batch_kernel) or "slots" (single-vector slots, as ZDMMV_BATCH_SLOTS=1).
 int batch_kernel_choice() {
     static const int v = [] {
         const char *e = std::getenv("ZDMMV_BATCH_KERNEL");
         if (!e) return 0;
         if (std::strcmp(e, "stream") == 0) return 1;
         if (std::strcmp(e, "slots") == 0) return 2;
+        if (std::strcmp(e, "mma") == 0) return 3;
         return 0;
     }();
     return v;
@@ -663,7 +667,28 @@ zdmmv_status dmmv_entry(int fmt, const void *w, zdmmv_layout layout, int64_t row
     TmaPlan vp{};
     int vv = 0, nvg = 0;
     const int choice = batch_slots_forced() ? 2 : batch_kernel_choice();
-    if (batch >= 2 && choice == 0 && vsplit_plan(fmt, layout, cols, batch, &vp, &vv, &nvg)) {
+    MmaPlan mp{};
+    if (batch >= 2 && choice == 3 && mma_plan(fmt, layout, rows, cols, batch, &mp)) {
+        // one weight stream, all vectors on the tensor cores
+        const DeviceInfo *dev = nullptr;
+        if (device_info(&dev) != cudaSuccess) return ZDMMV_ERR_CUDA;
+        MmaArgs m{};
+        m.w = a.w;
+        m.xq = a.xq;
+        m.y = y;
+        m.fault = dev->fault;
+        m.rows = rows;
+        m.y_stride = rows;
+        m.nb = a.nb;
+        m.batch = batch;
+        m.cb = mp.cb;
+        m.nchunks = mp.nchunks;
+        m.pitch = mp.pitch;
+        m.x_region = mp.x_region;
+        cudaError_t e = fmt == kFmtQ8 ? launch_mma_q8(m, mp, st, pdl_enabled()) : launch_mma_q4(m, mp, st, pdl_enabled());
+        return from_cuda(e);
+    }
+    if (batch >= 2 && (choice == 0 || choice == 3) && vsplit_plan(fmt, layout, cols, batch, &vp, &vv, &nvg)) {
         // one weight stream, the vectors split over the warps
         const DeviceInfo *dev = nullptr;
         if (device_info(&dev) != cudaSuccess) return ZDMMV_ERR_CUDA;

@@ -117,6 +117,26 @@ def activation_blocks(nblocks: int, seed: int, stream: int = S_ACT_BLOCKS,
     return blk.view(np.uint8).reshape(-1)
 
 
+def extreme_code_blocks(fmt: int, nblocks: int, seed: int, stream: int = S_ACT_BLOCKS) -> np.ndarray:
+    """Blocks whose codes take only their format's extreme values, scale 1.0:
+    Q8_0 codes in {-128, 127}, Q4_0 4-bit values in {0, 15}. With few blocks per
+    row every fp32 partial sum of a DMMV is still an exact integer, while every
+    product is as large as the format allows."""
+    g = rng(seed, stream)
+    if fmt == Q8_0:
+        blk = np.empty(nblocks, dtype=np.dtype([("d", "<f2"), ("qs", "i1", (32,))]))
+        blk["qs"] = np.where(g.integers(0, 2, size=(nblocks, 32)) == 1, 127, -128).astype(np.int8)
+    elif fmt == Q4_0:
+        blk = np.empty(nblocks, dtype=np.dtype([("d", "<f2"), ("qs", "u1", (16,))]))
+        lo = np.where(g.integers(0, 2, size=(nblocks, 16)) == 1, 15, 0)
+        hi = np.where(g.integers(0, 2, size=(nblocks, 16)) == 1, 15, 0)
+        blk["qs"] = (lo | (hi << 4)).astype(np.uint8)
+    else:
+        raise ValueError(f"unknown format {fmt}")
+    blk["d"] = np.float16(1.0)
+    return blk.view(np.uint8).reshape(-1)
+
+
 def expert_indices(seed: int, n_routed: int = 128, top_k: int = 8,
                    with_shared: bool = True) -> np.ndarray:
     """top_k distinct routed expert ids from a seeded permutation of 0..n_routed-1,

@@ -51,9 +51,15 @@
  *      ZDMMV_STAGE_KB           target KiB per pipeline stage (4..64, default 20)
  *      ZDMMV_CTAS_PER_SM        CTAs per SM of the single-vector kernel (1..8;
  *                               default 2 below 32 MB of weights per launch, else 4)
- *      ZDMMV_BATCH_KERNEL       batched kernel: vsplit (default), stream, or slots
- *                               (one single-vector slot per vector); "stream"
- *                               changes the fp32 reduction order of batch > 1
+ *      ZDMMV_BATCH_KERNEL       batched kernel: vsplit (default), mma, stream, or
+ *                               slots (one single-vector slot per vector); "mma"
+ *                               (integer tensor cores, GGUF rows of 256-column
+ *                               multiples up to 4096 and >= 16 rows, else vsplit)
+ *                               and "stream" change the fp32 reduction order of
+ *                               batch > 1
+ *      ZDMMV_MMA_WARPS=16       16 consumer warps in the "mma" kernel (default 8)
+ *      ZDMMV_MMA_STAGES         pipeline stages of the "mma" kernel (2..6, default
+ *                               as many as fit)
  *      ZDMMV_BATCH_SLOTS=1      the same as ZDMMV_BATCH_KERNEL=slots
  *      ZDMMV_VSPLIT_V=1         one vector per warp in the vector-split kernel
  *      ZDMMV_BATCH_CTAS_PER_SM  CTAs per SM of the batched kernels (1..4)

@@ -246,6 +246,24 @@ def test_batched_matches_oracle_and_single_calls(fmt, rows, cols, batch, layout)
             assert torch.equal(ys, y[v]), f"vector {v} differs from its single-vector call"
 
 
+@pytest.mark.parametrize("fmt", [Q8_0, Q4_0])
+@pytest.mark.parametrize("cols", [256, 512])
+@pytest.mark.parametrize("batch", [2, 8])
+def test_batched_extreme_codes_exact(fmt, cols, batch):
+    """Only the formats' extreme codes (Q8_0 -128 / 127, Q4_0 0 / 15 against
+    activation codes -128 / 127), unit scales, at most 16 blocks a row: every
+    output is an exact integer below 2^24, so the batched kernel's block sums
+    must give the oracle's values bit for bit."""
+    rows = 77
+    w = synth.extreme_code_blocks(fmt, rows * cols // 32, seed=cols + batch, stream=synth.S_WEIGHT)
+    xq = synth.extreme_code_blocks(Q8_0, batch * cols // 32, seed=cols * batch)
+    y = nan_out(batch, rows)
+    Z.dmmv_batched(fmt, dev(w), rows, cols, dev(xq), batch, y=y)
+    torch.cuda.synchronize()
+    y_ref, _ = oracle.dmmv_batched(fmt, w, rows, cols, xq, batch)
+    assert np.array_equal(y.double().cpu().numpy(), y_ref)
+
+
 def _vector_split_shape(cols, batch):
     """Widths and batches the vector-split batched kernel takes: pipelined widths
     (multiples of 256 up to 8192), two vectors per warp up to 4096 columns, one

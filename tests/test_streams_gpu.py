@@ -71,3 +71,32 @@ def _run_child(env_extra):
 
 def test_results_do_not_depend_on_programmatic_dependent_launch():
     assert _run_child({"ZDMMV_PDL": "0"}) == _run_child({"ZDMMV_PDL": "1"})
+
+
+_CHILD_VSPLIT = r"""
+import sys, numpy as np, torch
+sys.path.insert(0, {root!r})
+from gguf_block_quant_gb300 import synth
+from gguf_block_quant_gb300 import zdmmv as Z
+for fmt, rows, cols, batch in [(Z.Q8_0, 1434, 4096, 8), (Z.Q4_0, 901, 2048, 3)]:
+    w = torch.from_numpy(synth.weight_blocks(fmt, rows, cols, seed=batch)).cuda()
+    xq = Z.quantize_act_q8_0(torch.from_numpy(synth.activations(cols, seed=batch + 3, batch=batch)).cuda())
+    yb = Z.dmmv_batched(fmt, w, rows, cols, xq, batch)
+    nbx = cols // 32 * 34
+    for v in range(batch):
+        ys = Z.dmmv(fmt, w, rows, cols, xq[v * nbx:(v + 1) * nbx].clone())
+        torch.cuda.synchronize()
+        assert torch.equal(ys, yb[v]), (fmt, cols, batch, v)
+print("ok")
+"""
+
+
+def test_vector_split_kernel_equals_single_vector_calls_bitwise():
+    """ZDMMV_BATCH_KERNEL=vsplit (read once per process, hence a child process)
+    names the default explicitly: each vector's output equals its single-vector
+    call bit for bit."""
+    env = dict(os.environ, ZDMMV_BATCH_KERNEL="vsplit")
+    r = subprocess.run([sys.executable, "-c", _CHILD_VSPLIT.format(root=ROOT)], env=env, capture_output=True,
+                       text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    assert r.stdout.strip().splitlines()[-1] == "ok"
