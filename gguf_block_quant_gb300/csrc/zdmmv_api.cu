@@ -2,6 +2,8 @@
 // the small kernels (activation quantizer, repack, plain DMMV, debug sums, dp4a
 // self-test). The TMA-pipelined DMMV kernels live in zdmmv_tma_q8.cu /
 // zdmmv_tma_q4.cu. The library allocates no device memory.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -1146,6 +1148,42 @@ size_t zdmmv_host_step_workspace_bytes(int64_t rows, int64_t cols, int batch) {
     return static_cast<size_t>(xb + qb + yb);
 }
 
+namespace {
+// The device address of a host buffer of `bytes` bytes when the whole buffer is
+// page-locked memory of ONE allocation mapped into the current context (a
+// kernel may then read or write it directly, over the chip-to-chip link on a
+// Grace system), else nullptr: both ends are looked up and must be host memory
+// of the same allocation (buffer id) at linear device addresses.
+void *mapped_host_buffer(const void *p, size_t bytes) {
+    static const PFN_cuPointerGetAttributes_v7000 get = [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuPointerGetAttributes", &f, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return static_cast<PFN_cuPointerGetAttributes_v7000>(nullptr);
+        return reinterpret_cast<PFN_cuPointerGetAttributes_v7000>(f);
+    }();
+    if (!get || !p || bytes == 0) return nullptr;
+    struct End {
+        unsigned int type = 0;
+        CUdeviceptr dptr = 0;
+        unsigned long long id = 0;
+    } e[2];
+    const uintptr_t a[2] = {reinterpret_cast<uintptr_t>(p), reinterpret_cast<uintptr_t>(p) + bytes - 1};
+    for (int i = 0; i < 2; ++i) {
+        CUpointer_attribute at[3] = {CU_POINTER_ATTRIBUTE_MEMORY_TYPE, CU_POINTER_ATTRIBUTE_DEVICE_POINTER,
+                                     CU_POINTER_ATTRIBUTE_BUFFER_ID};
+        void *data[3] = {&e[i].type, &e[i].dptr, &e[i].id};
+        // an address CUDA does not know yields zeros, not an error
+        if (get(3, at, data, static_cast<CUdeviceptr>(a[i])) != CUDA_SUCCESS) return nullptr;
+        if (e[i].type != CU_MEMORYTYPE_HOST || e[i].dptr == 0 || e[i].id == 0) return nullptr;
+    }
+    if (e[0].id != e[1].id || e[1].dptr - e[0].dptr != bytes - 1) return nullptr;
+    return reinterpret_cast<void *>(e[0].dptr);
+}
+}  // namespace
+
 zdmmv_status zdmmv_host_step(zdmmv_fmt fmt, const void *w, zdmmv_layout layout, int64_t rows, int64_t cols,
                              const float *x_host, int batch, float *y_host, void *workspace_dev,
                              size_t workspace_bytes, zdmmv_stream_t stream) {
@@ -1161,7 +1199,21 @@ zdmmv_status zdmmv_host_step(zdmmv_fmt fmt, const void *w, zdmmv_layout layout, 
     float *xd = reinterpret_cast<float *>(ws);
     uint8_t *xqd = ws + xb;
     float *yd = reinterpret_cast<float *>(ws + xb + qb);
-    cudaError_t e = cudaMemcpyAsync(xd, x_host, static_cast<size_t>(batch) * cols * 4, cudaMemcpyHostToDevice, st);
+    const size_t x_bytes = static_cast<size_t>(batch) * cols * 4;
+    const size_t y_bytes = static_cast<size_t>(batch) * rows * 4;
+    if (rows > 0) {
+        // page-locked host buffers: no copies; the quantizer reads x from host
+        // memory once and the DMMV stores y into host memory (the same bits as
+        // the fused launch)
+        const float *xm = static_cast<const float *>(mapped_host_buffer(x_host, x_bytes));
+        float *ym = static_cast<float *>(mapped_host_buffer(y_host, y_bytes));
+        if (xm && ym && aligned(ym, 4)) {
+            zdmmv_status s = zdmmv_quantize_act_q8_0(xm, static_cast<int64_t>(batch) * cols, xqd, stream);
+            if (s != ZDMMV_OK) return s;
+            return dmmv_entry(fmt, w, layout, rows, cols, xqd, batch, ym, st);
+        }
+    }
+    cudaError_t e = cudaMemcpyAsync(xd, x_host, x_bytes, cudaMemcpyHostToDevice, st);
     if (e != cudaSuccess) return ZDMMV_ERR_CUDA;
     zdmmv_status s;
     if (tma_shape_ok(fmt, cols) && batch == 1) {
@@ -1173,7 +1225,7 @@ zdmmv_status zdmmv_host_step(zdmmv_fmt fmt, const void *w, zdmmv_layout layout, 
     }
     if (s != ZDMMV_OK) return s;
     if (rows > 0) {
-        e = cudaMemcpyAsync(y_host, yd, static_cast<size_t>(batch) * rows * 4, cudaMemcpyDeviceToHost, st);
+        e = cudaMemcpyAsync(y_host, yd, y_bytes, cudaMemcpyDeviceToHost, st);
         if (e != cudaSuccess) return ZDMMV_ERR_CUDA;
     }
     return ZDMMV_OK;

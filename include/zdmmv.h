@@ -382,14 +382,19 @@ size_t zdmmv_repacked_bytes(zdmmv_fmt fmt, int64_t rows, int64_t cols);
 zdmmv_status zdmmv_repack(zdmmv_fmt fmt, const void *src, int64_t rows, int64_t cols,
                           void *dst, size_t dst_bytes, zdmmv_stream_t stream);
 
-/* One decode step with HOST activations and outputs: copies x_host
- * ([batch][cols] fp32; pinned memory gives asynchronous copies) to the device,
- * quantizes it and runs the DMMV on the resident weights (one fused launch, as
- * zdmmv_dmmv_f32, for a single vector on the pipelined widths) and copies y back
- * to y_host ([batch][rows] fp32), all ordered on `stream`. The caller
+/* One decode step with HOST activations and outputs: x_host ([batch][cols]
+ * fp32) in, y_host ([batch][rows] fp32) out, quantized and multiplied on the
+ * resident weights, all ordered on `stream`. When each buffer lies in one
+ * page-locked allocation mapped into the device's address space (cudaHostAlloc,
+ * torch pin_memory), the kernels use the host memory in place: the quantizer
+ * reads x_host and the DMMV stores y_host (over the chip-to-chip link on a
+ * Grace system; no copy calls). Otherwise x is copied to the workspace, the
+ * fused quantize + DMMV (as zdmmv_dmmv_f32) runs there and y is copied back.
+ * Both routes give the same bits. The caller keeps x_host unchanged and
  * synchronizes the stream before reading y_host.
  *   workspace_dev  device, >= zdmmv_host_step_workspace_bytes(rows, cols, batch),
- *                  16-byte aligned; holds x, its Q8_0 blocks and y.
+ *                  16-byte aligned; holds x, its Q8_0 blocks and y (only the
+ *                  Q8_0 blocks when the host buffers are used in place).
  * Errors: as zdmmv_q8_0_batched, plus ERR_SIZE. */
 size_t zdmmv_host_step_workspace_bytes(int64_t rows, int64_t cols, int batch);
 zdmmv_status zdmmv_host_step(zdmmv_fmt fmt, const void *w, zdmmv_layout layout,

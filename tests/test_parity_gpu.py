@@ -360,6 +360,43 @@ def test_host_step_matches_oracle(fmt, rows, cols, batch):
     check_y(yh, y_ref, e_ref)
 
 
+@pytest.mark.parametrize("fmt,rows,cols,batch", [(Q4_0, 4096, 4096, 1), (Q8_0, 1000, 4096, 4),
+                                                 (Q8_0, 33, 96, 2)])
+def test_host_step_mapped_and_copied_buffers_agree_bitwise(fmt, rows, cols, batch):
+    """Page-locked host buffers are read and written by the kernels in place;
+    pageable ones are copied through the workspace; an interior slice of a larger
+    page-locked buffer is in place too. All give the same bits."""
+    w = dev(synth.weight_blocks(fmt, rows, cols, seed=31))
+    x = np.ascontiguousarray(synth.activations(cols, seed=32, batch=batch)).reshape(batch, cols)
+    ws = torch.empty(Z.host_step_workspace_bytes(rows, cols, batch), dtype=torch.uint8, device="cuda")
+    outs = []
+    for pinned, interior in ((True, False), (False, False), (True, True), (False, True)):
+        if interior:
+            big_x = torch.zeros(batch * cols + 64, dtype=torch.float32)
+            big_y = torch.full((batch * rows + 96,), float("nan"), dtype=torch.float32)
+            if pinned:
+                big_x, big_y = big_x.pin_memory(), big_y.pin_memory()
+            xh = big_x[16:16 + batch * cols].view(batch, cols)
+            yh = big_y[32:32 + batch * rows].view(batch, rows)
+            xh.copy_(torch.from_numpy(x))
+        else:
+            xh = torch.from_numpy(x.copy())
+            yh = torch.full((batch, rows), float("nan"), dtype=torch.float32)
+            if pinned:
+                xh, yh = xh.pin_memory(), yh.pin_memory()
+        Z.host_step(fmt, w, rows, cols, xh, yh, ws, batch=batch)
+        torch.cuda.synchronize()
+        if interior:
+            # the bytes around the slice are untouched
+            assert torch.isnan(big_y[:32]).all() and torch.isnan(big_y[32 + batch * rows:]).all()
+        outs.append(yh.clone())
+    for o in outs[1:]:
+        assert torch.equal(outs[0], o)
+    y_ref, e_ref = oracle.dmmv_batched(fmt, synth.weight_blocks(fmt, rows, cols, seed=31), rows, cols,
+                                       oracle.quantize_q8_0(x if batch > 1 else x[0]), batch)
+    check_y(outs[0], y_ref, e_ref)
+
+
 # ------------------------------------------------------- fused fp32 activation
 @pytest.mark.parametrize("layout", [Z.GGUF, Z.REPACKED])
 @pytest.mark.parametrize("fmt,rows,cols,batch", [(Q4_0, 4096, 4096, 1), (Q8_0, 1531, 2048, 1),
