@@ -390,8 +390,10 @@ zdmmv_status zdmmv_repack(zdmmv_fmt fmt, const void *src, int64_t rows, int64_t 
  * reads x_host and the DMMV stores y_host (over the chip-to-chip link on a
  * Grace system; no copy calls). Otherwise x is copied to the workspace, the
  * fused quantize + DMMV (as zdmmv_dmmv_f32) runs there and y is copied back.
- * Both routes give the same bits. The caller keeps x_host unchanged and
- * synchronizes the stream before reading y_host.
+ * Both routes give the same bits. The caller keeps both host buffers allocated
+ * and x_host unchanged until the stream has passed the call (kernels may still
+ * be reading and writing them), and synchronizes the stream before reading
+ * y_host.
  *   workspace_dev  device, >= zdmmv_host_step_workspace_bytes(rows, cols, batch),
  *                  16-byte aligned; holds x, its Q8_0 blocks and y (only the
  *                  Q8_0 blocks when the host buffers are used in place).
