@@ -384,14 +384,14 @@ struct BatchInst {
         return occ > 0 ? occ : 1;
     }
     static cudaError_t launch(const DmmvArgs &a, int smem, int ctas, cudaStream_t st, bool pdl) {
-        static bool done[64] = {};
+        static std::atomic<bool> done[64];  // smem limit raised, per device
         int dev = 0;
         cudaError_t e = cudaGetDevice(&dev);
         if (e != cudaSuccess) return e;
-        if (dev >= 0 && dev < 64 && !done[dev]) {
+        if (dev >= 0 && dev < 64 && !done[dev].load(std::memory_order_acquire)) {
             e = raise_dynamic_smem_limit(reinterpret_cast<const void *>(kKernel), dev);
             if (e != cudaSuccess) return e;
-            done[dev] = true;
+            done[dev].store(true, std::memory_order_release);
         }
         // never more CTAs than fit in one wave (cached per device and size)
         static std::atomic<uint64_t> occ_cache[64];

@@ -323,15 +323,15 @@ __global__ void __launch_bounds__(kTmaThreads, 3) moe_ffn_kernel(const FfnArgs f
 template <int FGU, int LGU, int PGU, int FDN, int LDN, int PDN, int STAGES>
 cudaError_t prepare_ffn_inst() {
     auto kern = moe_ffn_kernel<FGU, LGU, PGU, FDN, LDN, PDN, STAGES>;
-    static bool done[64] = {};
+    static std::atomic<bool> done[64];  // smem limit raised, per device
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (!done[dev]) {
+    if (!done[dev].load(std::memory_order_acquire)) {
         e = raise_dynamic_smem_limit(reinterpret_cast<const void *>(kern), dev);
         if (e != cudaSuccess) return e;
-        done[dev] = true;
+        done[dev].store(true, std::memory_order_release);
     }
     return cudaSuccess;
 }

@@ -400,15 +400,15 @@ template <int FMT, int NW, int STAGES>
 struct MmaInst {
     static constexpr auto kKernel = &dmmv_mma_kernel<FMT, NW, STAGES>;
     static cudaError_t launch(const MmaArgs &a, const CUtensorMap &wmap, int smem_bytes, cudaStream_t st, bool pdl) {
-        static bool done[64] = {};
+        static std::atomic<bool> done[64];  // smem limit raised, per device
         int dev = 0;
         cudaError_t e = cudaGetDevice(&dev);
         if (e != cudaSuccess) return e;
         if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-        if (!done[dev]) {
+        if (!done[dev].load(std::memory_order_acquire)) {
             e = raise_dynamic_smem_limit(reinterpret_cast<const void *>(kKernel), dev);
             if (e != cudaSuccess) return e;
-            done[dev] = true;
+            done[dev].store(true, std::memory_order_release);
         }
         int sms = 0;
         e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);

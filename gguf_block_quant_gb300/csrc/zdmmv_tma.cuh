@@ -425,14 +425,14 @@ struct TmaInst {
 
     static cudaError_t prepare() {
         // raise the dynamic shared-memory limit once per device
-        static bool done[64] = {};
+        static std::atomic<bool> done[64];  // smem limit raised, per device
         int dev = 0;
         cudaError_t e = cudaGetDevice(&dev);
         if (e != cudaSuccess) return e;
-        if (dev < 64 && done[dev]) return cudaSuccess;
+        if (dev < 64 && done[dev].load(std::memory_order_acquire)) return cudaSuccess;
         e = raise_dynamic_smem_limit(fn(), dev);
         if (e != cudaSuccess) return e;
-        if (dev < 64) done[dev] = true;
+        if (dev < 64) done[dev].store(true, std::memory_order_release);
         return cudaSuccess;
     }
 

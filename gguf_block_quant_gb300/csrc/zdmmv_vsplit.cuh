@@ -244,16 +244,16 @@ struct VsplitInst {
     static constexpr auto kKernel = &dmmv_vsplit_kernel<FMT, LAYOUT, LPR, PPL, V, NVG, STAGES>;
     // one wave of the CTAs that fit (occupancy cached per device and size)
     static cudaError_t launch(const DmmvArgs &a, const TmaPlan &p, int max_per_sm, cudaStream_t st, bool pdl) {
-        static bool done[64] = {};
+        static std::atomic<bool> done[64];  // smem limit raised, per device
         static std::atomic<uint64_t> occ_cache[64];
         int dev = 0;
         cudaError_t e = cudaGetDevice(&dev);
         if (e != cudaSuccess) return e;
         if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-        if (!done[dev]) {
+        if (!done[dev].load(std::memory_order_acquire)) {
             e = raise_dynamic_smem_limit(reinterpret_cast<const void *>(kKernel), dev);
             if (e != cudaSuccess) return e;
-            done[dev] = true;
+            done[dev].store(true, std::memory_order_release);
         }
         int per_sm = 0;
         const uint64_t c = occ_cache[dev].load(std::memory_order_relaxed);

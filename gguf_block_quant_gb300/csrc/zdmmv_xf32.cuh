@@ -279,16 +279,16 @@ struct Xf32Inst {
     // ctas_per_slot <= 0: one wave of the CTAs that fit on the device, split over the slots
     static cudaError_t launch(const DmmvArgs &a, const TmaPlan &p, int ctas_per_slot, int slots, cudaStream_t st,
                               bool pdl) {
-        static bool done[64] = {};
+        static std::atomic<bool> done[64];  // smem limit raised, per device
         static std::atomic<uint64_t> occ_cache[64];  // (smem << 32) | CTAs per SM, per device
         int dev = 0;
         cudaError_t e = cudaGetDevice(&dev);
         if (e != cudaSuccess) return e;
         if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-        if (!done[dev]) {
+        if (!done[dev].load(std::memory_order_acquire)) {
             e = raise_dynamic_smem_limit(reinterpret_cast<const void *>(kKernel), dev);
             if (e != cudaSuccess) return e;
-            done[dev] = true;
+            done[dev].store(true, std::memory_order_release);
         }
         if (ctas_per_slot <= 0) {
             int per_sm = 0;
