@@ -976,7 +976,26 @@ zdmmv_status dmmv_f32_entry(int fmt, const void *w, int layout, int64_t rows, in
     a.y_stride = rows;
     a.rows = rows;
     a.nb = static_cast<int32_t>(cols / kQK);
+    TmaPlan vp{};
+    int vv = 0, nvg = 0;
+    if (batch >= 2 && !batch_slots_forced() && batch_kernel_choice() == 0 &&
+        vsplit_plan(fmt, layout, cols, batch, &vp, &vv, &nvg)) {
+        // one weight stream for the batch, its activations quantized in the prologue
+        const DeviceInfo *dev = nullptr;
+        if (device_info(&dev) != cudaSuccess) return ZDMMV_ERR_CUDA;
+        a.fault = dev->fault;
+        a.batch = batch;
+        a.tile_rows = vp.tile_rows;
+        a.stage_bytes = vp.stage_bytes;
+        a.x_bytes_padded = vp.x_bytes_padded;
+        const int cap = std::getenv("ZDMMV_BATCH_CTAS_PER_SM") ? batch_ctas_per_sm() : 0;
+        cudaError_t e = fmt == kFmtQ8 ? launch_vsplit_fx_q8(a, vp, layout, vv, nvg, cap, st, pdl_enabled())
+                                      : launch_vsplit_fx_q4(a, vp, layout, vv, nvg, cap, st, pdl_enabled());
+        return from_cuda(e);
+    }
     if (tma_shape_ok(fmt, cols)) {
+        // single vectors, or batches the vector split does not take: one
+        // fused single-vector launch with a slot per vector
         a.batch = 1;
         return run_dmmv(fmt, layout, a, batch, st, true);
     }

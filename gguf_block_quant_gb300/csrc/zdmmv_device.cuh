@@ -236,6 +236,64 @@ __device__ __forceinline__ uint32_t quantize_q8_0_quad(float4 v, unsigned short 
     return q0 | (q1 << 8) | (q2 << 16) | (q3 << 24);
 }
 
+// Quantize 4 * nquads consecutive Q8_0 blocks of the fp32 values at xf into
+// shared memory at xs (34 bytes per block), with the stand-alone quantizer's
+// arithmetic (quantize_q8_0_lane: fp32 amax, IEEE d = amax / 127 and 1 / d,
+// codes round(x * id) with ties away from zero, fp16 scale RNE), so the bytes are
+// that quantizer's. The kWarps warps of the calling group (this one is `warp`)
+// each take four blocks per iteration (16-byte loads, 8 lanes per block),
+// kRound iterations at a time in phases (all loads, all block maxima, all
+// scales, all codes) so independent blocks overlap. The caller synchronizes the
+// group before the blocks are read.
+template <int kWarps, int kRound = 8>
+__device__ __forceinline__ void quantize_quads_to_smem(const float *xf, int nquads, uint8_t *xs, int warp,
+                                                       int lane) {
+    const int sub = lane >> 3;  // block within the quad
+    const int j = lane & 7;     // 4-element group within the block
+    for (int q0 = warp; q0 < nquads; q0 += kWarps * kRound) {
+        float4 v[kRound];
+        float m[kRound];
+#pragma unroll
+        for (int u = 0; u < kRound; ++u) {
+            const int qd = q0 + u * kWarps;
+            v[u] = qd < nquads ? *reinterpret_cast<const float4 *>(xf + static_cast<int64_t>(4 * qd + sub) * kQK + 4 * j)
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int u = 0; u < kRound; ++u)
+            m[u] = fmaxf(fmaxf(fabsf(v[u].x), fabsf(v[u].y)), fmaxf(fabsf(v[u].z), fabsf(v[u].w)));
+#pragma unroll
+        for (int o = 1; o < 8; o <<= 1) {
+#pragma unroll
+            for (int u = 0; u < kRound; ++u) m[u] = fmaxf(m[u], __shfl_xor_sync(0xffffffffu, m[u], o));
+        }
+        float id[kRound];
+        unsigned short db[kRound];
+#pragma unroll
+        for (int u = 0; u < kRound; ++u) {
+            // the operations of quantize_q8_0_lane: IEEE division and reciprocal
+            const float d = __fdiv_rn(m[u], 127.0f);
+            id[u] = d != 0.0f ? __frcp_rn(d) : 0.0f;
+            db[u] = __half_as_ushort(__float2half_rn(d));
+        }
+#pragma unroll
+        for (int u = 0; u < kRound; ++u) {
+            const int qd = q0 + u * kWarps;
+            if (qd < nquads) {  // warp-uniform
+                const uint32_t c0 = static_cast<uint8_t>(static_cast<int8_t>(static_cast<int>(roundf(__fmul_rn(v[u].x, id[u])))));
+                const uint32_t c1 = static_cast<uint8_t>(static_cast<int8_t>(static_cast<int>(roundf(__fmul_rn(v[u].y, id[u])))));
+                const uint32_t c2 = static_cast<uint8_t>(static_cast<int8_t>(static_cast<int>(roundf(__fmul_rn(v[u].z, id[u])))));
+                const uint32_t c3 = static_cast<uint8_t>(static_cast<int8_t>(static_cast<int>(roundf(__fmul_rn(v[u].w, id[u])))));
+                uint8_t *blk = xs + 34 * (4 * qd + sub);
+                uint16_t *dst = reinterpret_cast<uint16_t *>(blk + 2 + 4 * j);  // 2-byte aligned
+                dst[0] = static_cast<uint16_t>(c0 | (c1 << 8));
+                dst[1] = static_cast<uint16_t>(c2 | (c3 << 8));
+                if (j == 0) *reinterpret_cast<unsigned short *>(blk) = db[u];
+            }
+        }
+    }
+}
+
 // Sum of the 32 int8 codes of an activation block, times -8 (the Q4_0 offset
 // term), from its eight aligned code words.
 __device__ __forceinline__ int q4_offset_term(const uint32_t (&xw)[8]) {

@@ -119,6 +119,11 @@ cudaError_t launch_vsplit_q8(const DmmvArgs &a, const TmaPlan &p, int layout, in
                              cudaStream_t st, bool pdl);
 cudaError_t launch_vsplit_q4(const DmmvArgs &a, const TmaPlan &p, int layout, int v, int nvg, int max_per_sm,
                              cudaStream_t st, bool pdl);
+// The same with the fp32 activations a.xf quantized in the kernel's prologue.
+cudaError_t launch_vsplit_fx_q8(const DmmvArgs &a, const TmaPlan &p, int layout, int v, int nvg, int max_per_sm,
+                                cudaStream_t st, bool pdl);
+cudaError_t launch_vsplit_fx_q4(const DmmvArgs &a, const TmaPlan &p, int layout, int v, int nvg, int max_per_sm,
+                                cudaStream_t st, bool pdl);
 
 // The DMMV with an fp32 activation taken as is (no quantization): plan (false
 // when the pipelined kernel does not take the shape) and launchers.

@@ -69,8 +69,11 @@ __device__ __forceinline__ float pair_update(const Pair<FMT, LAYOUT> &x, const P
 }
 
 // a.batch vectors of Q8_0 blocks, contiguous at a.xq (staged in shared memory by
-// one bulk copy); outputs at a.y + v * a.y_stride.
-template <int FMT, int LAYOUT, int LPR, int PPL, int V, int NVG, int STAGES>
+// one bulk copy); outputs at a.y + v * a.y_stride. FX = true: the consumers
+// quantize the fp32 activations a.xf ([batch][cols], contiguous) into the same
+// shared-memory blocks themselves (the stand-alone quantizer's bytes), so the
+// results are those of the quantizer followed by the batched call.
+template <int FMT, int LAYOUT, int LPR, int PPL, int V, int NVG, int STAGES, bool FX = false>
 __global__ void __launch_bounds__(kTmaThreads, 3) dmmv_vsplit_kernel(const DmmvArgs a) {
     using P = Pair<FMT, LAYOUT>;
     using W = PairW<FMT, LAYOUT>;
@@ -119,7 +122,7 @@ __global__ void __launch_bounds__(kTmaThreads, 3) dmmv_vsplit_kernel(const DmmvA
         for (int t = 0; t < npre; ++t) issue_tile<FMT, LAYOUT>(a, a.w, r0, r1, t, t, stage0, full, wpol);
         int issued = npre;
         pdl_wait();  // the activations may be written by the preceding kernel
-        {
+        if constexpr (!FX) {
             const uint32_t xbytes = static_cast<uint32_t>(a.batch) * static_cast<uint32_t>(nb) * 34u;
             mbar_arrive_expect_tx(xbar, xbytes);
             bulk_copy_g2s(xs, a.xq, xbytes, xbar, l2_evict_last_policy());
@@ -140,7 +143,7 @@ __global__ void __launch_bounds__(kTmaThreads, 3) dmmv_vsplit_kernel(const DmmvA
             const int t_last = (issued - 1 - s) >= 0 ? ((issued - 1 - s) / STAGES) * STAGES + s : -1;
             if (t_last >= 0) (void)mbar_wait(&full[s], static_cast<uint32_t>(t_last / STAGES) & 1u);
         }
-        (void)mbar_wait(xbar, 0);
+        if constexpr (!FX) (void)mbar_wait(xbar, 0);
         return;
     }
 
@@ -151,11 +154,17 @@ __global__ void __launch_bounds__(kTmaThreads, 3) dmmv_vsplit_kernel(const DmmvA
     const int rg = (warp / NVG) * kGroupsPerWarp + lane / LPR;   // row group within it
     const int l = lane % LPR;
     const int npairs = nb >> 1;
-    pdl_wait();  // outputs may still be read by the preceding kernel
-    // waits are warp-uniform so a timeout can never split a warp before its shuffles
-    if (!__all_sync(0xffffffffu, mbar_wait(xbar, 0))) {
-        if (lane == 0) atomicOr(a.fault, 1u);
-        return;
+    pdl_wait();  // outputs may still be read, and the activations written, by the preceding kernel
+    if constexpr (FX) {
+        // nb is a multiple of 8 on this path: whole quads of blocks per vector
+        quantize_quads_to_smem<kWarps>(a.xf, a.batch * (nb >> 2), xs, warp, lane);
+        consumer_barrier();
+    } else {
+        // waits are warp-uniform so a timeout can never split a warp before its shuffles
+        if (!__all_sync(0xffffffffu, mbar_wait(xbar, 0))) {
+            if (lane == 0) atomicOr(a.fault, 1u);
+            return;
+        }
     }
     // this warp's vectors, from the staged activation blocks
     P xr[V][PPL];
@@ -239,9 +248,9 @@ __global__ void __launch_bounds__(kTmaThreads, 3) dmmv_vsplit_kernel(const DmmvA
     }
 }
 
-template <int FMT, int LAYOUT, int LPR, int PPL, int V, int NVG, int STAGES>
+template <int FMT, int LAYOUT, int LPR, int PPL, int V, int NVG, int STAGES, bool FX>
 struct VsplitInst {
-    static constexpr auto kKernel = &dmmv_vsplit_kernel<FMT, LAYOUT, LPR, PPL, V, NVG, STAGES>;
+    static constexpr auto kKernel = &dmmv_vsplit_kernel<FMT, LAYOUT, LPR, PPL, V, NVG, STAGES, FX>;
     // one wave of the CTAs that fit (occupancy cached per device and size)
     static cudaError_t launch(const DmmvArgs &a, const TmaPlan &p, int max_per_sm, cudaStream_t st, bool pdl) {
         static std::atomic<bool> done[64];  // smem limit raised, per device
@@ -288,13 +297,13 @@ struct VsplitInst {
 };
 
 // p.lpr / p.ppl as in the single-vector plan; v vectors per warp, nvg groups; p.stages 2 or 3.
-template <int FMT, int LAYOUT>
+template <int FMT, int LAYOUT, bool FX>
 cudaError_t launch_vsplit_layout(const DmmvArgs &a, const TmaPlan &p, int v, int nvg, int max_per_sm,
                                  cudaStream_t st, bool pdl) {
-#define ZDMMV_VS(LPR_, PPL_, V_, NVG_)                                                      \
-    if (p.lpr == LPR_ && p.ppl == PPL_ && v == V_ && nvg == NVG_)                           \
-        return p.stages == 3 ? VsplitInst<FMT, LAYOUT, LPR_, PPL_, V_, NVG_, 3>::launch(a, p, max_per_sm, st, pdl) \
-                             : VsplitInst<FMT, LAYOUT, LPR_, PPL_, V_, NVG_, 2>::launch(a, p, max_per_sm, st, pdl);
+#define ZDMMV_VS(LPR_, PPL_, V_, NVG_)                                                                        \
+    if (p.lpr == LPR_ && p.ppl == PPL_ && v == V_ && nvg == NVG_)                                             \
+        return p.stages == 3 ? VsplitInst<FMT, LAYOUT, LPR_, PPL_, V_, NVG_, 3, FX>::launch(a, p, max_per_sm, st, pdl) \
+                             : VsplitInst<FMT, LAYOUT, LPR_, PPL_, V_, NVG_, 2, FX>::launch(a, p, max_per_sm, st, pdl);
 #define ZDMMV_VS_ALL(LPR_, PPL_) \
     ZDMMV_VS(LPR_, PPL_, 1, 2) ZDMMV_VS(LPR_, PPL_, 1, 4) ZDMMV_VS(LPR_, PPL_, 2, 1) ZDMMV_VS(LPR_, PPL_, 2, 2) \
     ZDMMV_VS(LPR_, PPL_, 2, 4)
@@ -309,11 +318,11 @@ cudaError_t launch_vsplit_layout(const DmmvArgs &a, const TmaPlan &p, int v, int
     return cudaErrorInvalidConfiguration;
 }
 
-template <int FMT>
+template <int FMT, bool FX>
 cudaError_t launch_vsplit_fmt(const DmmvArgs &a, const TmaPlan &p, int layout, int v, int nvg, int max_per_sm,
                               cudaStream_t st, bool pdl) {
-    if (layout == kLayoutGguf) return launch_vsplit_layout<FMT, kLayoutGguf>(a, p, v, nvg, max_per_sm, st, pdl);
-    return launch_vsplit_layout<FMT, kLayoutRepacked>(a, p, v, nvg, max_per_sm, st, pdl);
+    if (layout == kLayoutGguf) return launch_vsplit_layout<FMT, kLayoutGguf, FX>(a, p, v, nvg, max_per_sm, st, pdl);
+    return launch_vsplit_layout<FMT, kLayoutRepacked, FX>(a, p, v, nvg, max_per_sm, st, pdl);
 }
 
 }  // namespace zdmmv

@@ -5,7 +5,7 @@ namespace zdmmv {
 
 cudaError_t launch_vsplit_q8(const DmmvArgs &a, const TmaPlan &p, int layout, int v, int nvg, int max_per_sm,
                              cudaStream_t st, bool pdl) {
-    return launch_vsplit_fmt<kFmtQ8>(a, p, layout, v, nvg, max_per_sm, st, pdl);
+    return launch_vsplit_fmt<kFmtQ8, false>(a, p, layout, v, nvg, max_per_sm, st, pdl);
 }
 
 }  // namespace zdmmv

@@ -170,6 +170,11 @@ zdmmv_status zdmmv_q4_0_batched(const void *w, zdmmv_layout layout, int64_t rows
  *   fmt    ZDMMV_Q8_0 or ZDMMV_Q4_0 weights; w, layout, rows, cols as zdmmv_q8_0.
  *   x      device fp32 [batch][cols], 16-byte aligned; batch 1..8.
  *   y      device fp32 [batch][rows].
+ * Batches of 2..8 on the batched kernel's shapes stream the weights once (every
+ * CTA quantizes the whole batch); other batches run one fused launch with a
+ * slot per vector. For batches the two calls (zdmmv_quantize_act_q8_0, then
+ * zdmmv_q{8,4}_0_batched) are faster: the quantization is done once instead of
+ * in every CTA.
  * Shapes off the pipelined path (cols % 256 != 0 or cols > 8192) need
  * batch*cols/32*34 <= 200 KiB of shared memory, else ERR_SHAPE.
  * Errors: as zdmmv_q8_0_batched, plus ERR_FORMAT. */

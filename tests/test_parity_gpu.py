@@ -401,7 +401,9 @@ def test_host_step_mapped_and_copied_buffers_agree_bitwise(fmt, rows, cols, batc
 @pytest.mark.parametrize("layout", [Z.GGUF, Z.REPACKED])
 @pytest.mark.parametrize("fmt,rows,cols,batch", [(Q4_0, 4096, 4096, 1), (Q8_0, 1531, 2048, 1),
                                                  (Q8_0, 700, 512, 3), (Q4_0, 99, 8192, 8),
-                                                 (Q8_0, 37, 96, 1), (Q4_0, 77, 160, 5), (Q8_0, 5, 14336, 2)])
+                                                 (Q8_0, 37, 96, 1), (Q4_0, 77, 160, 5), (Q8_0, 5, 14336, 2),
+                                                 (Q8_0, 1434, 4096, 8), (Q4_0, 901, 2048, 4), (Q8_0, 333, 4096, 2),
+                                                 (Q4_0, 300, 8192, 3)])
 def test_fused_f32_equals_quantize_then_dmmv_bitwise(fmt, rows, cols, batch, layout):
     w = synth.weight_blocks(fmt, rows, cols, seed=cols + batch)
     x = synth.activations(cols, seed=rows, batch=batch)
