@@ -339,7 +339,7 @@ template <> struct Pair<kFmtQ8, kLayoutGguf> {
     uint32_t x[17];  // x[0..8]: block A codes at w's alignment (zeros facing dA, dB); x[9..16]: block B
     float dxa, dxb;
 
-    __device__ __forceinline__ void set(const uint32_t (&v)[17]) {
+    __device__ __forceinline__ void set(const uint32_t (&v)[17], int /*p*/ = 0) {
         x[0] = v[0] & 0xffff0000u;
 #pragma unroll
         for (int k = 1; k < 8; ++k) x[k] = v[k];
@@ -377,7 +377,7 @@ template <> struct Pair<kFmtQ4, kLayoutGguf> {
     int inita, initb; // -8 * sum of the block's codes
     float dxa, dxb;
 
-    __device__ __forceinline__ void set(const uint32_t (&v)[17]) {
+    __device__ __forceinline__ void set(const uint32_t (&v)[17], int /*p*/ = 0) {
         // activation pair bytes: v0 = [dxA dxA x0 x1], v_k = x(4k-2)..x(4k+1), v8 = [x30 x31 dxB dxB]
         xlo[0] = v[0] & 0xffff0000u;         // [0 0 x0 x1]
         xlo[1] = v[1];                       // x2..x5
@@ -427,42 +427,68 @@ template <> struct Pair<kFmtQ4, kLayoutGguf> {
     }
 };
 
-// Q8_0, repacked layout: 16 aligned quant words (block A words 0..7, block B
-// 8..15) plus one scale word (dA low half, dB high half).
+// Q8_0, repacked layout: 16 aligned quant words per pair, four 16-byte chunks
+// (block A: chunks 0, 1; block B: chunks 2, 3), plus one scale word. Pairs are
+// 64 bytes apart, so if every lane loaded its chunks in order, the 8 lanes of a
+// 128-bit load phase would hit 2 of the 8 bank quads. The lane owning pair p
+// loads chunk (s + rot) & 3 at step s, rot = (p >> 1) & 3 (8 distinct bank
+// quads per phase), holds its activation words in the same order, and adds the
+// per-chunk sums back into the two block sums: the same integers.
 template <> struct Pair<kFmtQ8, kLayoutRepacked> {
     static constexpr int kWords = 16;
-    uint32_t x[16];
+    static constexpr int kChunks = 4;
+    uint32_t x[16];  // x[4s..4s+3]: the activation words facing chunk (s + rot) & 3
+    int rot;
     float dxa, dxb;
 
-    __device__ __forceinline__ void set(const uint32_t (&v)[17]) {
+    __device__ __forceinline__ static int rotation(int p) { return (p >> 1) & 3; }
+
+    __device__ __forceinline__ void set(const uint32_t (&v)[17], int p = 0) {
         uint32_t xa[8], xb[8];
         x_aligned_words(v, xa, xb);
+        uint32_t c[16];
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
-            x[k] = xa[k];
-            x[8 + k] = xb[k];
+            c[k] = xa[k];
+            c[8 + k] = xb[k];
+        }
+        rot = rotation(p);
+#pragma unroll
+        for (int s = 0; s < 4; ++s) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const uint32_t r0 = c[4 * (s & 3) + i], r1 = c[4 * ((s + 1) & 3) + i];
+                const uint32_t r2 = c[4 * ((s + 2) & 3) + i], r3 = c[4 * ((s + 3) & 3) + i];
+                x[4 * s + i] = rot == 0 ? r0 : (rot == 1 ? r1 : (rot == 2 ? r2 : r3));
+            }
         }
         dxa = half_lo(v[0]);
         dxb = half_hi(v[8]);
     }
+    // wq: the weight words in load order (chunk (s + rot) & 3 at words 4s..4s+3)
     __device__ __forceinline__ void sums(const uint32_t *wq, int &sa, int &sb) const {
-        sa = 0;
-        sb = 0;
+        int q[4];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) sa = dp4a_ss(wq[k], x[k], sa);
+        for (int s = 0; s < 4; ++s) {
+            q[s] = 0;
 #pragma unroll
-        for (int k = 8; k < 16; ++k) sb = dp4a_ss(wq[k], x[k], sb);
+            for (int i = 0; i < 4; ++i) q[s] = dp4a_ss(wq[4 * s + i], x[4 * s + i], q[s]);
+        }
+        // block A is chunks 0 and 1: load steps (0 - rot) & 3 and (1 - rot) & 3
+        const int q01 = q[0] + q[1], q12 = q[1] + q[2], q23 = q[2] + q[3], q30 = q[3] + q[0];
+        sa = rot == 0 ? q01 : (rot == 1 ? q30 : (rot == 2 ? q23 : q12));
+        sb = rot == 0 ? q23 : (rot == 1 ? q12 : (rot == 2 ? q01 : q30));
     }
-    // wq: shared-memory address of 16 quant words (16-byte aligned); ws: the pair's scale word
+    // wq: shared-memory address of the pair's 16 quant words (16-byte aligned); ws: its scale word
     __device__ __forceinline__ float fma_pair(uint32_t wq, uint32_t ws, float acc) const {
         uint32_t r[16];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const uint4 t = lds128(wq + 16 * k);
-            r[4 * k] = t.x;
-            r[4 * k + 1] = t.y;
-            r[4 * k + 2] = t.z;
-            r[4 * k + 3] = t.w;
+        for (int s = 0; s < 4; ++s) {
+            const uint4 t = lds128(wq + 16u * static_cast<uint32_t>((s + rot) & 3));
+            r[4 * s] = t.x;
+            r[4 * s + 1] = t.y;
+            r[4 * s + 2] = t.z;
+            r[4 * s + 3] = t.w;
         }
         int sa, sb;
         sums(r, sa, sb);
@@ -472,50 +498,62 @@ template <> struct Pair<kFmtQ8, kLayoutRepacked> {
     }
 };
 
-// Q4_0, repacked layout: 8 aligned quant words (block A qs words 0..3, block B
-// 4..7) plus one scale word.
+// Q4_0, repacked layout: 8 aligned quant words per pair, two 16-byte chunks
+// (block A, block B) 32 bytes apart from pair to pair, plus one scale word. The
+// lane owning pair p loads its chunks in swapped order when rot = (p >> 2) & 1
+// is 1 (8 distinct bank quads per 128-bit load phase) and holds its activation
+// words and offset terms in the same order; the block sums are the same integers.
 template <> struct Pair<kFmtQ4, kLayoutRepacked> {
     static constexpr int kWords = 8;
-    uint32_t xlo[8], xhi[8];
-    int inita, initb;
+    static constexpr int kChunks = 2;
+    uint32_t xlo[8], xhi[8];  // words 4s..4s+3: facing chunk s ^ rot
+    int init0, init1;         // the -8 offset terms of chunk 0 ^ rot and 1 ^ rot
+    int rot;
     float dxa, dxb;
 
-    __device__ __forceinline__ void set(const uint32_t (&v)[17]) {
+    __device__ __forceinline__ static int rotation(int p) { return (p >> 2) & 1; }
+
+    __device__ __forceinline__ void set(const uint32_t (&v)[17], int p = 0) {
         uint32_t xa[8], xb[8];
         x_aligned_words(v, xa, xb);
+        rot = rotation(p);
+        const bool sw = rot != 0;
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-            xlo[k] = xa[k];
-            xhi[k] = xa[4 + k];
-            xlo[4 + k] = xb[k];
-            xhi[4 + k] = xb[4 + k];
+            xlo[k] = sw ? xb[k] : xa[k];
+            xhi[k] = sw ? xb[4 + k] : xa[4 + k];
+            xlo[4 + k] = sw ? xa[k] : xb[k];
+            xhi[4 + k] = sw ? xa[4 + k] : xb[4 + k];
         }
-        inita = q4_offset_term(xa);
-        initb = q4_offset_term(xb);
+        const int ia = q4_offset_term(xa), ib = q4_offset_term(xb);
+        init0 = sw ? ib : ia;
+        init1 = sw ? ia : ib;
         dxa = half_lo(v[0]);
         dxb = half_hi(v[8]);
     }
+    // wq: the weight words in load order (chunk s ^ rot at words 4s..4s+3)
     __device__ __forceinline__ void sums(const uint32_t *wq, int &sa, int &sb) const {
-        int la = inita, ha = 0, lb = initb, hb = 0;
+        int l0 = init0, h0 = 0, l1 = init1, h1 = 0;
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-            la = dp4a_ss(wq[k] & kLoNib, xlo[k], la);
-            ha = dp4a_us(wq[k] & kHiNib, xhi[k], ha);
-            lb = dp4a_ss(wq[4 + k] & kLoNib, xlo[4 + k], lb);
-            hb = dp4a_us(wq[4 + k] & kHiNib, xhi[4 + k], hb);
+            l0 = dp4a_ss(wq[k] & kLoNib, xlo[k], l0);
+            h0 = dp4a_us(wq[k] & kHiNib, xhi[k], h0);
+            l1 = dp4a_ss(wq[4 + k] & kLoNib, xlo[4 + k], l1);
+            h1 = dp4a_us(wq[4 + k] & kHiNib, xhi[4 + k], h1);
         }
-        sa = la + (ha >> 4);
-        sb = lb + (hb >> 4);
+        const int s0 = l0 + (h0 >> 4), s1 = l1 + (h1 >> 4);
+        sa = rot ? s1 : s0;
+        sb = rot ? s0 : s1;
     }
     __device__ __forceinline__ float fma_pair(uint32_t wq, uint32_t ws, float acc) const {
         uint32_t r[8];
 #pragma unroll
-        for (int k = 0; k < 2; ++k) {
-            const uint4 t = lds128(wq + 16 * k);
-            r[4 * k] = t.x;
-            r[4 * k + 1] = t.y;
-            r[4 * k + 2] = t.z;
-            r[4 * k + 3] = t.w;
+        for (int s = 0; s < 2; ++s) {
+            const uint4 t = lds128(wq + 16u * static_cast<uint32_t>(s ^ rot));
+            r[4 * s] = t.x;
+            r[4 * s + 1] = t.y;
+            r[4 * s + 2] = t.z;
+            r[4 * s + 3] = t.w;
         }
         int sa, sb;
         sums(r, sa, sb);

@@ -267,7 +267,7 @@ __global__ void __launch_bounds__(kTmaThreads, MINB) dmmv_tma_kernel(const DmmvA
         if (p < (nb >> 1)) {
             uint32_t v[17];
             load_x_pair_words_smem(smem_addr(xs), p, v);
-            xr[j].set(v);
+            xr[j].set(v, p);
         }
     }
 

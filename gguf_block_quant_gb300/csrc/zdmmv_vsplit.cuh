@@ -37,15 +37,19 @@ template <int FMT> struct PairW<FMT, kLayoutGguf> {
 };
 
 template <int FMT> struct PairW<FMT, kLayoutRepacked> {
-    static constexpr int kW = Pair<FMT, kLayoutRepacked>::kWords;
+    using P = Pair<FMT, kLayoutRepacked>;
+    static constexpr int kW = P::kWords;
     uint32_t r[kW];
     uint32_t ws;
-    // row: address of the row's quant words; scales: address of its scale array
+    // row: address of the row's quant words; scales: address of its scale array.
+    // The chunks are loaded in the pair's rotated order (Pair::rotation), the
+    // order the lane's activation words are held in.
     __device__ __forceinline__ void load(uint32_t row, uint32_t scales, int p) {
         const uint32_t a = row + static_cast<uint32_t>(p * RowGeom<FMT, kLayoutRepacked>::kPairQuantBytes);
+        const int rot = P::rotation(p);
 #pragma unroll
-        for (int k = 0; k < kW / 4; ++k) {
-            const uint4 t = lds128(a + 16 * k);
+        for (int k = 0; k < P::kChunks; ++k) {
+            const uint4 t = lds128(a + 16u * static_cast<uint32_t>((k + rot) & (P::kChunks - 1)));
             r[4 * k] = t.x;
             r[4 * k + 1] = t.y;
             r[4 * k + 2] = t.z;
@@ -184,7 +188,7 @@ __global__ void __launch_bounds__(kTmaThreads, 3) dmmv_vsplit_kernel(const DmmvA
 #pragma unroll
                 for (int k = 0; k < 17; ++k) w17[k] = 0;
             }
-            xr[v][j].set(w17);
+            xr[v][j].set(w17, p);
         }
     }
 
