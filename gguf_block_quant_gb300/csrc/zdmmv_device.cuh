@@ -431,13 +431,14 @@ template <> struct Pair<kFmtQ4, kLayoutGguf> {
 // (block A: chunks 0, 1; block B: chunks 2, 3), plus one scale word. Pairs are
 // 64 bytes apart, so if every lane loaded its chunks in order, the 8 lanes of a
 // 128-bit load phase would hit 2 of the 8 bank quads. The lane owning pair p
-// loads chunk (s + rot) & 3 at step s, rot = (p >> 1) & 3 (8 distinct bank
-// quads per phase), holds its activation words in the same order, and adds the
-// per-chunk sums back into the two block sums: the same integers.
+// loads chunk s ^ rot at step s, rot = (p >> 1) & 3 (the four lane pairs of a
+// phase take four different chunks: 8 distinct bank quads), and holds its
+// activation words in the same order. Steps 0, 1 then hold one whole block
+// (A when rot < 2) and steps 2, 3 the other: the block sums are the same integers.
 template <> struct Pair<kFmtQ8, kLayoutRepacked> {
     static constexpr int kWords = 16;
     static constexpr int kChunks = 4;
-    uint32_t x[16];  // x[4s..4s+3]: the activation words facing chunk (s + rot) & 3
+    uint32_t x[16];  // x[4s..4s+3]: the activation words facing chunk s ^ rot
     int rot;
     float dxa, dxb;
 
@@ -457,34 +458,30 @@ template <> struct Pair<kFmtQ8, kLayoutRepacked> {
         for (int s = 0; s < 4; ++s) {
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                const uint32_t r0 = c[4 * (s & 3) + i], r1 = c[4 * ((s + 1) & 3) + i];
-                const uint32_t r2 = c[4 * ((s + 2) & 3) + i], r3 = c[4 * ((s + 3) & 3) + i];
+                const uint32_t r0 = c[4 * s + i], r1 = c[4 * (s ^ 1) + i];
+                const uint32_t r2 = c[4 * (s ^ 2) + i], r3 = c[4 * (s ^ 3) + i];
                 x[4 * s + i] = rot == 0 ? r0 : (rot == 1 ? r1 : (rot == 2 ? r2 : r3));
             }
         }
         dxa = half_lo(v[0]);
         dxb = half_hi(v[8]);
     }
-    // wq: the weight words in load order (chunk (s + rot) & 3 at words 4s..4s+3)
+    // wq: the weight words in load order (chunk s ^ rot at words 4s..4s+3)
     __device__ __forceinline__ void sums(const uint32_t *wq, int &sa, int &sb) const {
-        int q[4];
+        int lo = 0, hi = 0;  // steps 0, 1 and steps 2, 3
 #pragma unroll
-        for (int s = 0; s < 4; ++s) {
-            q[s] = 0;
+        for (int k = 0; k < 8; ++k) lo = dp4a_ss(wq[k], x[k], lo);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) q[s] = dp4a_ss(wq[4 * s + i], x[4 * s + i], q[s]);
-        }
-        // block A is chunks 0 and 1: load steps (0 - rot) & 3 and (1 - rot) & 3
-        const int q01 = q[0] + q[1], q12 = q[1] + q[2], q23 = q[2] + q[3], q30 = q[3] + q[0];
-        sa = rot == 0 ? q01 : (rot == 1 ? q30 : (rot == 2 ? q23 : q12));
-        sb = rot == 0 ? q23 : (rot == 1 ? q12 : (rot == 2 ? q01 : q30));
+        for (int k = 8; k < 16; ++k) hi = dp4a_ss(wq[k], x[k], hi);
+        sa = rot < 2 ? lo : hi;
+        sb = rot < 2 ? hi : lo;
     }
     // wq: shared-memory address of the pair's 16 quant words (16-byte aligned); ws: its scale word
     __device__ __forceinline__ float fma_pair(uint32_t wq, uint32_t ws, float acc) const {
         uint32_t r[16];
 #pragma unroll
         for (int s = 0; s < 4; ++s) {
-            const uint4 t = lds128(wq + 16u * static_cast<uint32_t>((s + rot) & 3));
+            const uint4 t = lds128(wq + 16u * static_cast<uint32_t>(s ^ rot));
             r[4 * s] = t.x;
             r[4 * s + 1] = t.y;
             r[4 * s + 2] = t.z;

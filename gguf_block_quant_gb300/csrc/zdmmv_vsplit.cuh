@@ -49,7 +49,7 @@ template <int FMT> struct PairW<FMT, kLayoutRepacked> {
         const int rot = P::rotation(p);
 #pragma unroll
         for (int k = 0; k < P::kChunks; ++k) {
-            const uint4 t = lds128(a + 16u * static_cast<uint32_t>((k + rot) & (P::kChunks - 1)));
+            const uint4 t = lds128(a + 16u * static_cast<uint32_t>(k ^ rot));
             r[4 * k] = t.x;
             r[4 * k + 1] = t.y;
             r[4 * k + 2] = t.z;
