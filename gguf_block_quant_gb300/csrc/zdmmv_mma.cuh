@@ -37,6 +37,7 @@
 
 #include <cuda.h>
 
+#include "zdmmv.h"
 #include "zdmmv_mma.h"
 #include "zdmmv_tma.cuh"
 
@@ -254,7 +255,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) dmmv_mma_kernel(const MmaArg
     // tensor copies land on 128-byte boundaries (the host plan keeps every stage
     // offset a multiple of 128; this guards the base)
     if ((smem_addr(stage0) & 127u) != 0u) {
-        if (tid == 0) atomicOr(a.fault, 1u);
+        if (tid == 0) atomicOr(a.fault, ZDMMV_FAULT_SMEM_ALIGN);
         return;
     }
 

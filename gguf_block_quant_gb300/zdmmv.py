@@ -26,6 +26,7 @@ QK = 32
 MAX_BATCH = 8
 BLOCK_BYTES = {Q4_0: 18, Q8_0: 34}
 FAULT_WAIT_TIMEOUT = 1
+FAULT_SMEM_ALIGN = 2
 ARGMAX_WORKSPACE_BYTES = 16384
 
 STATUS = {0: "ok", 1: "null pointer", 2: "bad shape", 3: "misaligned pointer or stride",

@@ -104,6 +104,8 @@ typedef enum { ZDMMV_LAYOUT_GGUF = 0, ZDMMV_LAYOUT_REPACKED = 1 } zdmmv_layout;
 
 /* Device fault bits reported by zdmmv_device_status. */
 #define ZDMMV_FAULT_WAIT_TIMEOUT 1u  /* a bounded wait on a copy or a pipeline stage gave up */
+#define ZDMMV_FAULT_SMEM_ALIGN   2u  /* a kernel found its shared-memory stages off the
+                                        alignment its tensor copies need and computed nothing */
 
 /* Human-readable name of a status code (static string). */
 const char *zdmmv_status_str(zdmmv_status st);
