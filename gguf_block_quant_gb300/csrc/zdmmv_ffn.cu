@@ -145,7 +145,7 @@ cudaError_t launch_ffn(int fmt_gu, int fmt_dn, FfnArgs f, int sms, cudaStream_t 
     static const int env_cap = [] {
         const char *e = std::getenv("ZDMMV_FFN_CTAS_PER_SM");
         const int n = e ? std::atoi(e) : 0;
-        return (n >= 1 && n <= 8) ? n : 4;
+        return (n >= 1 && n <= 8) ? n : 8;  // default: as many as fit (measured best)
     }();
     const int smem = kBarrierBytes + f.x_bytes_padded + env_stages * pitch;
     int occ = 0;

@@ -64,7 +64,8 @@
  *      ZDMMV_VSPLIT_V=1         one vector per warp in the vector-split kernel
  *      ZDMMV_BATCH_CTAS_PER_SM  CTAs per SM of the batched kernels (1..4)
  *      ZDMMV_FFN_STAGES=3       three pipeline stages in zdmmv_expert_ffn (default 2)
- *      ZDMMV_FFN_CTAS_PER_SM    CTAs per SM of zdmmv_expert_ffn (1..8, default up to 4)
+ *      ZDMMV_FFN_CTAS_PER_SM    CTAs per SM of zdmmv_expert_ffn (1..8, default as
+ *                               many as fit)
  *  - There is no CPU fallback: every result is computed by the CUDA kernels.
  *  - Inputs must be finite (a NaN or infinite activation gives unspecified
  *    codes).
