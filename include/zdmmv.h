@@ -50,7 +50,8 @@
  *    optional; results are the same bits whatever they are set to unless stated):
  *      ZDMMV_STAGE_KB           target KiB per pipeline stage (4..64, default 20)
  *      ZDMMV_CTAS_PER_SM        CTAs per SM of the single-vector kernel (1..8;
- *                               default 2 below 32 MB of weights per launch, else 4)
+ *                               default 2 below 32 MB of weights per launch, else 4;
+ *                               expert gathers as many as fit)
  *      ZDMMV_BATCH_KERNEL       batched kernel: vsplit (default), mma, stream, or
  *                               slots (one single-vector slot per vector); "mma"
  *                               (integer tensor cores, GGUF rows of 256-column
