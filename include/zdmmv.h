@@ -67,6 +67,8 @@
  *      ZDMMV_FFN_STAGES=3       three pipeline stages in zdmmv_expert_ffn (default 2)
  *      ZDMMV_FFN_CTAS_PER_SM    CTAs per SM of zdmmv_expert_ffn (1..8, default as
  *                               many as fit)
+ *      ZDMMV_FFN_GU_PERCENT     share of zdmmv_expert_ffn's CTAs on gate/up rows
+ *                               (20..80, default 60; the rest on down rows)
  *  - There is no CPU fallback: every result is computed by the CUDA kernels.
  *  - Inputs must be finite (a NaN or infinite activation gives unspecified
  *    codes).
