@@ -125,7 +125,9 @@ int ffn_entry_status(int fmt_gu, const void *w_gate, const void *w_up, int64_t g
     f.y = y;
     f.hidden = static_cast<int32_t>(hidden);
     f.ffn = static_cast<int32_t>(ffn);
-    return launch_ffn(fmt_gu, fmt_dn, f, sms, st, pdl) == cudaSuccess ? ZDMMV_OK : ZDMMV_ERR_CUDA;
+    const cudaError_t e = launch_ffn(fmt_gu, fmt_dn, f, sms, st, pdl);
+    if (e == cudaErrorNotSupported) return ZDMMV_ERR_SHAPE;  // n above what one resident grid holds
+    return e == cudaSuccess ? ZDMMV_OK : ZDMMV_ERR_CUDA;
 }
 
 cudaError_t launch_ffn(int fmt_gu, int fmt_dn, FfnArgs f, int sms, cudaStream_t st, bool pdl) {
@@ -164,7 +166,7 @@ cudaError_t launch_ffn(int fmt_gu, int fmt_dn, FfnArgs f, int sms, cudaStream_t 
     const int slots_per_expert = sms * occ / f.n;
     int gu = slots_per_expert * env_gu_pct / 100;
     int dn = slots_per_expert - gu;
-    if (gu < 1 || dn < 1) return cudaErrorInvalidConfiguration;
+    if (gu < 1 || dn < 1) return cudaErrorNotSupported;  // too many experts to be co-resident
     if (gu > f.ffn) gu = static_cast<int>(f.ffn);
     if (dn > f.hidden) dn = static_cast<int>(f.hidden);
     f.gu_per = gu;

@@ -270,7 +270,10 @@ zdmmv_status zdmmv_expert_swiglu(zdmmv_fmt fmt, const void *w_gate, const void *
  *                multiples (>= the matrix size when n_experts > 1).
  *   hidden       a multiple of 256, at most 4096; ffn a multiple of 256, at most
  *                2048 (else ERR_SHAPE). n == 0 is a no-op.
- *   idx, n, n_experts, status_dev   as zdmmv_expert_gather (n <= 4096); a bad
+ *   idx, n, n_experts, status_dev   as zdmmv_expert_gather; n <= 4096 and at
+ *                most half the CTAs that fit on the device at once (every CTA of
+ *                the grid must be resident: 380 on a 152-SM GB300 at 5 CTAs per SM),
+ *                else ERR_SHAPE; a bad
  *                index gives NaN rows of h_k and y_k.
  *   xq           device Q8_0 blocks of the hidden activation, shared by all slots.
  *   y            device fp32 [n][hidden].

@@ -768,3 +768,20 @@ def test_expert_ffn_bad_index_then_reuse_workspace():
                          y=nan_out(3, hidden), workspace=ws)
     torch.cuda.synchronize()
     assert torch.equal(y2[0], y[0]) and torch.equal(y2[2], y[2]) and not torch.isnan(y2[1]).any()
+
+
+def test_expert_ffn_too_many_experts_for_one_resident_grid_is_a_shape_error():
+    """Every CTA of the one-launch FFN must be resident at once (a waiting down CTA
+    must never hold a slot a gate/up CTA needs), so a selection larger than half
+    the CTAs that fit returns ERR_SHAPE before any launch, and the device is
+    left without a fault."""
+    hidden, ffn = 256, 256
+    w_gu = dev(synth.weight_blocks(Q4_0, ffn, hidden, seed=3))
+    w_dn = dev(synth.weight_blocks(Q8_0, hidden, ffn, seed=4))
+    xq = Z.quantize_act_q8_0(dev(synth.activations(hidden, seed=5)))
+    n = 4000
+    idx = torch.zeros(n, dtype=torch.int32, device="cuda")
+    with pytest.raises(Z.ZdmmvError) as err:
+        Z.expert_ffn(Q4_0, w_gu, w_gu, 0, Q8_0, w_dn, 0, hidden, ffn, idx, 1, xq)
+    assert err.value.code == 2  # ZDMMV_ERR_SHAPE
+    assert Z.device_status() == 0
