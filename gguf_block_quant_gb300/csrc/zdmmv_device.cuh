@@ -267,14 +267,23 @@ __device__ __forceinline__ void quantize_quads_to_smem(const float *xf, int nqua
 #pragma unroll
             for (int u = 0; u < kRound; ++u) m[u] = fmaxf(m[u], __shfl_xor_sync(0xffffffffu, m[u], o));
         }
+        // the operations of quantize_q8_0_lane (IEEE division and reciprocal),
+        // once per block: lane j of the 8 sharing a block takes round j's block
+        // and the results are broadcast to the other 7
+        static_assert(kRound == 8, "one round per lane of a block's 8 lanes");
+        float mj = m[0];
+#pragma unroll
+        for (int u = 1; u < kRound; ++u) mj = j == u ? m[u] : mj;
+        const float dj = __fdiv_rn(mj, 127.0f);
+        const float idj = dj != 0.0f ? __frcp_rn(dj) : 0.0f;
+        const uint32_t dbj = __half_as_ushort(__float2half_rn(dj));
         float id[kRound];
         unsigned short db[kRound];
 #pragma unroll
         for (int u = 0; u < kRound; ++u) {
-            // the operations of quantize_q8_0_lane: IEEE division and reciprocal
-            const float d = __fdiv_rn(m[u], 127.0f);
-            id[u] = d != 0.0f ? __frcp_rn(d) : 0.0f;
-            db[u] = __half_as_ushort(__float2half_rn(d));
+            const int src = (lane & ~7) | u;
+            id[u] = __shfl_sync(0xffffffffu, idj, src);
+            db[u] = static_cast<unsigned short>(__shfl_sync(0xffffffffu, dbj, src));
         }
 #pragma unroll
         for (int u = 0; u < kRound; ++u) {
