@@ -813,11 +813,17 @@ def profile_mode(name: str):
         return
     workloads = {c.name: c for c in (synth.SSM_ALPHA_BETA, synth.DENSE_Q4_0, synth.LM_HEAD_Q4_0,
                                      *synth.BATCHED_Q8_0.values())}
-    cfg = workloads[name]
+    # "<workload>:xf32": the DMMV with the fp32 activation taken as is, 3 x 4 layers
+    xf32 = name.endswith(":xf32")
+    cfg = workloads[name[: -len(":xf32")] if xf32 else name]
     pool = DensePool(cfg, 4)
     for _ in range(3):
-        pool.step()
-        pool.step_unfused()
+        if xf32:
+            for l in range(4):
+                Z.dmmv_xf32(cfg.fmt, pool.w[l], cfg.rows, cfg.cols, pool.x[l], batch=cfg.batch, y=pool.y[l])
+        else:
+            pool.step()
+            pool.step_unfused()
     torch.cuda.synchronize()
     print(json.dumps({"profile": name, "layers": 4, "fault": Z.device_status()}))
 
