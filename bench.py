@@ -715,11 +715,14 @@ def gpu_arm(args):
                          "kernel": "dmmv_tma_kernel with the fused Q8_0 activation quantization (Q4_0, GGUF layout)",
                          "algorithmic_bytes_per_launch": nbytes,
                          "us_per_launch": round(per_launch_fused * 1e6, 3),
+                         # ncu's DRAM bytes per launch over the live launch time
+                         "dram_gbs": round(traffic / per_launch_fused / 1e9, 1) if traffic else None,
                          "peak_kind": f"{peak_kind} HBM copy bandwidth",
                          "dmmv_only_chain": {
                              "kernel": "dmmv_tma_kernel over pre-quantized activation blocks",
                              "achieved": round(achieved, 1), "frac": round(achieved / hbm_peak, 4),
-                             "us_per_launch": round(per_launch * 1e6, 3), "traffic": traffic_dmmv}},
+                             "us_per_launch": round(per_launch * 1e6, 3), "traffic": traffic_dmmv,
+                             "dram_gbs": round(traffic_dmmv / per_launch / 1e9, 1) if traffic_dmmv else None}},
             "cpu_baseline": cpu,
             "e2e": e2e,
             "two_kernel_chain_gbs": round(unfused_gbs, 2),
