@@ -158,7 +158,8 @@ zdmmv_status zdmmv_q4_0(const void *w, zdmmv_layout layout, int64_t rows, int64_
  * zdmmv_q4_0 on vector v. Widths of 8192 columns with batch > 4 stream the tile
  * through a kernel whose fp32 reduction order differs (deterministic, within
  * the stated tolerance); other widths run the single-vector computation once per
- * vector. batch == 1 is zdmmv_q8_0 / zdmmv_q4_0.
+ * vector. batch == 1 is zdmmv_q8_0 / zdmmv_q4_0. These are the default kernels;
+ * the environment variable ZDMMV_BATCH_KERNEL (above) selects others.
  * Errors: as zdmmv_q8_0, plus ERR_SHAPE for batch outside 1..8. */
 zdmmv_status zdmmv_q8_0_batched(const void *w, zdmmv_layout layout, int64_t rows,
                                 int64_t cols, const void *xq, int batch, float *y,
