@@ -361,7 +361,7 @@ def test_host_step_matches_oracle(fmt, rows, cols, batch):
 
 
 @pytest.mark.parametrize("fmt,rows,cols,batch", [(Q4_0, 4096, 4096, 1), (Q8_0, 1000, 4096, 4),
-                                                 (Q8_0, 33, 96, 2)])
+                                                 (Q8_0, 33, 96, 2), (Q4_0, 777, 2048, 8)])
 def test_host_step_mapped_and_copied_buffers_agree_bitwise(fmt, rows, cols, batch):
     """Page-locked host buffers are read and written by the kernels in place;
     pageable ones are copied through the workspace; an interior slice of a larger
@@ -403,7 +403,7 @@ def test_host_step_mapped_and_copied_buffers_agree_bitwise(fmt, rows, cols, batc
                                                  (Q8_0, 700, 512, 3), (Q4_0, 99, 8192, 8),
                                                  (Q8_0, 37, 96, 1), (Q4_0, 77, 160, 5), (Q8_0, 5, 14336, 2),
                                                  (Q8_0, 1434, 4096, 8), (Q4_0, 901, 2048, 4), (Q8_0, 333, 4096, 2),
-                                                 (Q4_0, 300, 8192, 3)])
+                                                 (Q4_0, 300, 8192, 3), (Q8_0, 517, 2048, 7), (Q4_0, 1000, 4096, 5)])
 def test_fused_f32_equals_quantize_then_dmmv_bitwise(fmt, rows, cols, batch, layout):
     w = synth.weight_blocks(fmt, rows, cols, seed=cols + batch)
     x = synth.activations(cols, seed=rows, batch=batch)
@@ -747,6 +747,26 @@ def test_expert_ffn_equals_swiglu_then_down_gather(fmt_gu, fmt_dn, hidden, ffn):
                                            ffn // 32 * 34)
     assert s == 0
     check_y(y, y_ref, e_ref)
+
+
+@pytest.mark.parametrize("n", [1, 40])
+def test_expert_ffn_selection_sizes(n):
+    """One selected expert (the whole grid on one expert's rows) and 40 (few CTAs
+    per expert, the gate/up share of the grid rounded down to a handful): h and y
+    equal the separate entry points bit for bit."""
+    fmt_gu, fmt_dn, hidden, ffn, n_exp = Q4_0, Q8_0, 1024, 256, 8
+    idx = [(7 * k + 3) % n_exp for k in range(n)]
+    c = _ffn_case(fmt_gu, fmt_dn, hidden, ffn, n_exp, idx, seed=n + 11)
+    gd, ud, dd, ia = dev(c["g"]), dev(c["u"]), dev(c["d"]), dev(c["idx"])
+    xq = Z.quantize_act_q8_0(dev(c["x"]))
+    y, h = Z.expert_ffn(fmt_gu, gd, ud, c["gu_per"], fmt_dn, dd, c["dn_per"], hidden, ffn, ia, n_exp, xq,
+                        y=nan_out(n, hidden))
+    h2 = Z.expert_swiglu(fmt_gu, gd, ud, ffn, hidden, xq, idx=ia, expert_stride=c["gu_per"], n_experts=n_exp)
+    y2 = Z.expert_gather(fmt_dn, dd, c["dn_per"], hidden, ffn, ia, n_exp, Z.quantize_act_q8_0(h2.reshape(-1)),
+                         ffn // 32 * 34)
+    torch.cuda.synchronize()
+    assert torch.equal(h, h2) and torch.equal(y, y2)
+    assert not torch.isnan(y).any()
 
 
 def test_expert_ffn_bad_index_then_reuse_workspace():
