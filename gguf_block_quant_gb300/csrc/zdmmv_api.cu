@@ -55,6 +55,8 @@ cudaError_t device_info(const DeviceInfo **out) {
     return cudaSuccess;
 }
 
+}  // namespace
+
 bool pdl_enabled() {
     static const bool on = [] {
         const char *v = std::getenv("ZDMMV_PDL");
@@ -70,7 +72,7 @@ bool pdl_enabled() {
 // on the MoE step: gate+up 9.3 -> 7.7 us from 2 to 5 CTAs per SM). The
 // environment variable ZDMMV_CTAS_PER_SM (1..8) overrides all three.
 constexpr int kCtasPerSmGathered = 8;  // capped by the occupancy of the kernel
-int ctas_per_sm_per_launch(int64_t weight_bytes, bool gathered = false) {
+int ctas_per_sm_per_launch(int64_t weight_bytes, bool gathered) {
     static const int forced = [] {
         const char *e = std::getenv("ZDMMV_CTAS_PER_SM");
         const int n = e ? std::atoi(e) : 0;
@@ -80,6 +82,8 @@ int ctas_per_sm_per_launch(int64_t weight_bytes, bool gathered = false) {
     if (gathered) return kCtasPerSmGathered;
     return weight_bytes >= kLargeLaunchBytes ? kCtasPerSmLarge : kCtasPerSmSmall;
 }
+
+namespace {
 
 // Batched calls stream the weights once (dmmv_batch_kernel) unless
 // ZDMMV_BATCH_SLOTS=1, which runs one single-vector slot per vector instead.
@@ -786,40 +790,8 @@ zdmmv_status argmax_entry(int fmt, const void *w, int layout, int64_t rows, int6
         (max_out && !aligned(max_out, 4)))
         return ZDMMV_ERR_ALIGN;
     if (workspace_bytes < ZDMMV_ARGMAX_WORKSPACE_BYTES) return ZDMMV_ERR_SIZE;
-    const DeviceInfo *dev = nullptr;
-    if (device_info(&dev) != cudaSuccess) return ZDMMV_ERR_CUDA;
-    DmmvArgs a{};
-    a.w = static_cast<const uint8_t *>(w);
-    a.xq = static_cast<const uint8_t *>(xq);
-    a.rows = rows;
-    a.nb = static_cast<int32_t>(cols / kQK);
-    a.batch = 1;
-    a.fault = dev->fault;
-    a.argmax_parts = static_cast<uint2 *>(workspace);
-    const TmaPlan p = tma_plan(fmt, layout, cols);
-    a.tile_rows = p.tile_rows;
-    a.stage_bytes = p.stage_bytes;
-    a.x_bytes_padded = p.x_bytes_padded;
-    int per_sm = fmt == kFmtQ8 ? tma_ctas_per_sm_q8(layout, p) : tma_ctas_per_sm_q4(layout, p);
-    const int want = ctas_per_sm_per_launch(rows * a.nb * static_cast<int64_t>(block_bytes(fmt)));
-    if (per_sm > want) per_sm = want;
-    int64_t ctas = static_cast<int64_t>(dev->sms) * per_sm;
-    if (ctas > rows) ctas = rows;
-    if (ctas > kArgmaxMaxCtas) ctas = kArgmaxMaxCtas;
-    cudaError_t e = fmt == kFmtQ8 ? launch_argmax_q8(a, p, layout, static_cast<int>(ctas), st, pdl_enabled())
-                                  : launch_argmax_q4(a, p, layout, static_cast<int>(ctas), st, pdl_enabled());
-    if (e != cudaSuccess) return ZDMMV_ERR_CUDA;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(1, 1, 1);
-    cfg.blockDim = dim3(256, 1, 1);
-    cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = pdl_enabled() ? 1 : 0;
-    return from_cuda(cudaLaunchKernelEx(&cfg, argmax_reduce_kernel, static_cast<const uint2 *>(a.argmax_parts),
-                                        static_cast<int>(ctas), argmax_out, max_out));
+    return from_cuda(launch_argmax_dmmv(fmt, layout, w, rows, cols, xq, argmax_out, max_out,
+                                        static_cast<uint2 *>(workspace), st));
 }
 
 }  // namespace
@@ -836,6 +808,35 @@ cudaError_t launch_argmax_reduce(const uint2 *parts, int n, int32_t *argmax_out,
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
     return cudaLaunchKernelEx(&cfg, argmax_reduce_kernel, parts, n, argmax_out, max_out);
+}
+
+cudaError_t launch_argmax_dmmv(int fmt, int layout, const void *w, int64_t rows, int64_t cols, const void *xq,
+                               int32_t *argmax_out, float *max_out, uint2 *parts, cudaStream_t st) {
+    const DeviceInfo *dev = nullptr;
+    cudaError_t e = device_info(&dev);
+    if (e != cudaSuccess) return e;
+    DmmvArgs a{};
+    a.w = static_cast<const uint8_t *>(w);
+    a.xq = static_cast<const uint8_t *>(xq);
+    a.rows = rows;
+    a.nb = static_cast<int32_t>(cols / kQK);
+    a.batch = 1;
+    a.fault = dev->fault;
+    a.argmax_parts = parts;
+    const TmaPlan p = tma_plan(fmt, layout, cols);
+    a.tile_rows = p.tile_rows;
+    a.stage_bytes = p.stage_bytes;
+    a.x_bytes_padded = p.x_bytes_padded;
+    int per_sm = fmt == kFmtQ8 ? tma_ctas_per_sm_q8(layout, p) : tma_ctas_per_sm_q4(layout, p);
+    const int want = ctas_per_sm_per_launch(rows * a.nb * static_cast<int64_t>(block_bytes(fmt)));
+    if (per_sm > want) per_sm = want;
+    int64_t ctas = static_cast<int64_t>(dev->sms) * per_sm;
+    if (ctas > rows) ctas = rows;
+    if (ctas > kArgmaxMaxCtas) ctas = kArgmaxMaxCtas;  // never more partials than `parts` holds
+    e = fmt == kFmtQ8 ? launch_argmax_q8(a, p, layout, static_cast<int>(ctas), st, pdl_enabled())
+                      : launch_argmax_q4(a, p, layout, static_cast<int>(ctas), st, pdl_enabled());
+    if (e != cudaSuccess) return e;
+    return launch_argmax_reduce(parts, static_cast<int>(ctas), argmax_out, max_out, st, pdl_enabled());
 }
 
 uint32_t *current_fault_word() {

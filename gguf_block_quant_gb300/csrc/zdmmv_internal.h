@@ -65,6 +65,13 @@ constexpr int64_t kLargeLaunchBytes = 32ll << 20;  // weight bytes per launch
 constexpr int kSmemPerCtaTarget = 54 * 1024;         // keeps 4 CTAs per SM possible
 constexpr int kTmaRowsIlp = 2;                       // rows per row group in flight
 
+// Whether launches carry the programmatic-dependent-launch attribute (on unless
+// the environment sets ZDMMV_PDL=0).
+bool pdl_enabled();
+// CTAs per SM a pipelined launch of this many weight bytes asks for (before the
+// kernel's occupancy caps it); ZDMMV_CTAS_PER_SM (1..8) overrides it.
+int ctas_per_sm_per_launch(int64_t weight_bytes, bool gathered = false);
+
 // Allow a kernel the device's opt-in shared memory minus its static shared memory.
 inline cudaError_t raise_dynamic_smem_limit(const void *fn, int dev) {
     int optin = 0;
@@ -148,6 +155,11 @@ int ffn_entry_status(int fmt_gu, const void *w_gate, const void *w_up, int64_t g
                      int n_experts, const void *xq, float *y, void *workspace, size_t workspace_bytes,
                      int32_t *status_dev, cudaStream_t st, bool pdl);
 
+// The argmax DMMV (per-CTA partials at `parts`, room for kArgmaxMaxCtas) and its
+// one-CTA reduce, on the current device; arguments already checked. Shared by the
+// workspace and the allocation-free argmax entry points.
+cudaError_t launch_argmax_dmmv(int fmt, int layout, const void *w, int64_t rows, int64_t cols, const void *xq,
+                               int32_t *argmax_out, float *max_out, uint2 *parts, cudaStream_t st);
 // The argmax epilogue's final pass (one CTA over n partials).
 cudaError_t launch_argmax_reduce(const uint2 *parts, int n, int32_t *argmax_out, float *max_out, cudaStream_t st,
                                  bool pdl);

@@ -22,7 +22,6 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
-#include <cstdlib>
 #include <mutex>
 
 #include "zdmmv.h"
@@ -32,7 +31,8 @@
 namespace zdmmv {
 namespace {
 
-constexpr int kNoAllocSlots = kArgmaxMaxCtas;  // 2048 partials x 8 bytes = 16 KiB
+// 2048 partials x 8 bytes = 16 KiB: as many as an argmax launch ever uses
+constexpr int kNoAllocSlots = kArgmaxMaxCtas;
 
 // The scratch: one (max bits, row) partial per CTA of a launch.
 static __device__ __align__(256) uint2 g_noalloc_argmax_scratch[kNoAllocSlots];
@@ -42,7 +42,6 @@ static __device__ __align__(256) uint2 g_noalloc_argmax_scratch[kNoAllocSlots];
 struct NoAllocDevice {
     bool ready = false;
     uint2 *scratch = nullptr;  // device address of g_noalloc_argmax_scratch
-    int sms = 0;
 };
 constexpr int kMaxDevices = 64;
 NoAllocDevice g_noalloc[kMaxDevices];
@@ -59,21 +58,11 @@ cudaError_t noalloc_setup(const NoAllocDevice **out) {
         void *p = nullptr;
         e = cudaGetSymbolAddress(&p, g_noalloc_argmax_scratch);  // this device is current
         if (e != cudaSuccess) return e;
-        e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
-        if (e != cudaSuccess) return e;
         d.scratch = static_cast<uint2 *>(p);
         d.ready = true;
     }
     *out = &d;
     return cudaSuccess;
-}
-
-bool noalloc_pdl() {
-    static const bool on = [] {
-        const char *v = std::getenv("ZDMMV_PDL");
-        return !(v && v[0] == '0');
-    }();
-    return on;
 }
 
 int block_bytes_of(int fmt) { return fmt == kFmtQ8 ? 34 : (fmt == kFmtQ4 ? 18 : 0); }
@@ -97,32 +86,8 @@ extern "C" zdmmv_status zdmmv_dmmv_argmax_noalloc(zdmmv_fmt fmt, const void *w, 
         return ZDMMV_ERR_ALIGN;
     const NoAllocDevice *nd = nullptr;
     if (noalloc_setup(&nd) != cudaSuccess) return ZDMMV_ERR_CUDA;
-    uint32_t *fault = current_fault_word();
-    if (!fault) return ZDMMV_ERR_CUDA;
-
-    DmmvArgs a{};
-    a.w = static_cast<const uint8_t *>(w);
-    a.xq = static_cast<const uint8_t *>(xq);
-    a.rows = rows;
-    a.nb = static_cast<int32_t>(cols / kQK);
-    a.batch = 1;
-    a.fault = fault;
-    a.argmax_parts = nd->scratch;
-    const TmaPlan p = tma_plan(fmt, layout, cols);
-    a.tile_rows = p.tile_rows;
-    a.stage_bytes = p.stage_bytes;
-    a.x_bytes_padded = p.x_bytes_padded;
-    int per_sm = fmt == kFmtQ8 ? tma_ctas_per_sm_q8(layout, p) : tma_ctas_per_sm_q4(layout, p);
-    const int64_t weight_bytes = rows * a.nb * static_cast<int64_t>(bb);
-    const int want = weight_bytes >= kLargeLaunchBytes ? kCtasPerSmLarge : kCtasPerSmSmall;
-    if (per_sm > want) per_sm = want;
-    int64_t ctas = static_cast<int64_t>(nd->sms) * per_sm;
-    if (ctas > rows) ctas = rows;
-    if (ctas > kNoAllocSlots) ctas = kNoAllocSlots;  // never more partials than the array holds
-    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    cudaError_t e = fmt == kFmtQ8 ? launch_argmax_q8(a, p, layout, static_cast<int>(ctas), st, noalloc_pdl())
-                                  : launch_argmax_q4(a, p, layout, static_cast<int>(ctas), st, noalloc_pdl());
-    if (e != cudaSuccess) return ZDMMV_ERR_CUDA;
-    e = launch_argmax_reduce(nd->scratch, static_cast<int>(ctas), argmax_out, max_out, st, noalloc_pdl());
-    return e == cudaSuccess ? ZDMMV_OK : ZDMMV_ERR_CUDA;
+    return launch_argmax_dmmv(fmt, layout, w, rows, cols, xq, argmax_out, max_out, nd->scratch,
+                              reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? ZDMMV_OK
+               : ZDMMV_ERR_CUDA;
 }
