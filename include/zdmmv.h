@@ -62,7 +62,9 @@
  *      ZDMMV_MMA_STAGES         pipeline stages of the "mma" kernel (2..6, default
  *                               as many as fit)
  *      ZDMMV_BATCH_SLOTS=1      the same as ZDMMV_BATCH_KERNEL=slots
- *      ZDMMV_VSPLIT_V=1         one vector per warp in the vector-split kernel
+ *      ZDMMV_VSPLIT_V=1         one vector per warp in the vector-split kernel;
+ *                               batches of more than 4 vectors then take the
+ *                               "stream" kernel (its fp32 reduction order)
  *      ZDMMV_BATCH_CTAS_PER_SM  CTAs per SM of the batched kernels (1..4)
  *      ZDMMV_FFN_STAGES=3       three pipeline stages in zdmmv_expert_ffn (default 2)
  *      ZDMMV_FFN_CTAS_PER_SM    CTAs per SM of zdmmv_expert_ffn (1..8, default as
