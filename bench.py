@@ -1,27 +1,29 @@
 #!/usr/bin/env python3
 """Benchmark of the GGUF Q4_0 / Q8_0 decode DMMV on GB300.
 
-Workload (default): the dense Q4_0 4096 x 4096 decode DMMV, batch 1. One STEP is
-LAYERS launches over LAYERS distinct weight matrices of that shape, each with its
-own fp32 activation (per layer: quantize the activation to Q8_0, then the DMMV,
-fused in one launch), ordered in one stream so that each launch waits for the
-previous grid before it reads its inputs, as the layers of a decode token do;
-every step streams LAYERS x 9.44 MB of weights. The stack (605 MB at 64 layers)
-is larger than 4x the 129 MB L2, so no layer's weights are L2-resident when it
-runs. Inputs are resident in HBM before the timed region; the step is captured
-once in a CUDA graph and replayed (decode chains are replayed as graphs: "RTX
-5090: Batched Prefill & CUDA Graphs in ZINC", "CUDA graphs -- the structural
-answer to launch latency").
+Headline workload: the LM head (vocab projection), Q4_0 248320 x 2048 (286 MB of
+weights), batch 1. One STEP is one decode token's projection: the token's fp32
+activation is quantized to Q8_0 and multiplied by the matrix (fused in one
+launch), producing 248320 fp32 logits. Steps alternate over LM_HEAD_COPIES
+distinct copies of the matrix (together more than 4x the 129 MB L2), so every
+step streams its weights from HBM. Inputs are resident in HBM before the timed
+region; the K timed steps are captured once in a CUDA graph and replayed (decode
+chains are replayed as graphs: "RTX 5090: Batched Prefill & CUDA Graphs in
+ZINC", "CUDA graphs -- the structural answer to launch latency"). The vocab
+projection is the pages' bandwidth showcase (habr ZINC article, "Утилизация
+полосы памяти по операциям").
 
-Printed: one JSON line (rank 0) with value = algorithmic GB/s over the whole job
-(weights read once + Q8_0 activation blocks + fp32 outputs), the
-roofline of the step's kernel (the fused quantize + DMMV; the DMMV over
-pre-quantized blocks beside it) against the measured HBM copy bandwidth, the CPU oracle as baseline, the end-to-end number through the
-host-buffer C-ABI call, clocks sampled during the timed region, and per-workload
-measurements of the other four decode workloads.
+Printed: ONE compact JSON line on stdout (rank 0): value = algorithmic GB/s
+over the whole job (weights read once + Q8_0 activation blocks + fp32 logits),
+the roofline of the step's kernel against the measured HBM copy bandwidth, the
+CPU oracle as baseline, the end-to-end number through the host-buffer C-ABI
+call, clocks sampled during the timed region, and a `summary` of every other
+workload ([microseconds, % of the copy peak] per variant). The full per-workload
+detail goes to stderr as one more JSON line prefixed "detail: ".
 
---impl reference times the CPU oracle on the same workload and metric: with no
-upstream code to run, the oracle is the reference implementation of the method.
+--impl reference times the CPU oracle on the same workload, config and metric:
+with no upstream code to run, the oracle is the reference implementation of the
+method.
 """
 from __future__ import annotations
 
@@ -46,11 +48,11 @@ FALLBACK_HBM_GBS = 6800.0
 def parse():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=2000)
+    p.add_argument("--steps", type=int, default=500)
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["zdmmv", "reference"], default="zdmmv")
-    p.add_argument("--layers", type=int, default=64, help="distinct weight matrices per step")
-    p.add_argument("--no-extra", action="store_true", help="skip the other four workloads")
+    p.add_argument("--layers", type=int, default=64, help="distinct weight matrices per step of the dense chain")
+    p.add_argument("--no-extra", action="store_true", help="skip the other workloads")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--eager", action="store_true", help="launch eagerly instead of graph replay")
     p.add_argument("--profile", default=None, metavar="WORKLOAD",
@@ -168,86 +170,116 @@ def barrier(world: int):
 
 
 # ------------------------------------------------------------------ CPU oracle
-def cpu_baseline_dense(cfg, layers_budget_s: float = 12.0):
-    """Time the oracle (as it stands, single thread) on a bounded sample of the
-    dense workload: whole layers (quantize + DMMV of one 4096 x 4096 matrix)
-    until about layers_budget_s of CPU work."""
-    import oracle
-    from gguf_block_quant_gb300 import synth
-    w = synth.weight_blocks(cfg.fmt, cfg.rows, cfg.cols, seed=cfg.seed)
-    x = synth.activations(cfg.cols, seed=cfg.seed, scale=cfg.x_scale)
-    oracle.lib()
-    done = 0
-    t0 = time.perf_counter()
-    while True:
-        xq = oracle.quantize_q8_0(x)
-        oracle.dmmv(cfg.fmt, w, cfg.rows, cfg.cols, xq)
-        done += 1
-        el = time.perf_counter() - t0
-        if el >= layers_budget_s or done >= 2000:
-            break
-    gbs = done * cfg.algorithmic_bytes() / el / 1e9
-    return {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": f"{done} layers ({cfg.name}: quantize + DMMV each) in {el:.1f} s, single-threaded C",
-            "rows_per_s": done * cfg.rows / el}
-
-
 # The oracle over row ranges in worker processes (spawned, never forked: the
-# parent may already hold a CUDA context). Each worker gets the whole matrix once.
+# parent may already hold a CUDA context). The matrix lives once in a shared
+# memory segment that every worker maps.
 _ORACLE_W = None
 
 
-def _oracle_worker_init(fmt, w_bytes, rows, cols):
+def _oracle_worker_init(fmt, shm_name, rows, row_bytes, cols):
     global _ORACLE_W
+    from multiprocessing import shared_memory
     import numpy as np
     import oracle
     oracle.lib()
-    _ORACLE_W = (fmt, np.frombuffer(w_bytes, dtype=np.uint8).reshape(rows, -1), cols)
+    shm = shared_memory.SharedMemory(name=shm_name)
+    _ORACLE_W = (fmt, np.ndarray((rows, row_bytes), dtype=np.uint8, buffer=shm.buf), cols, shm)
 
 
 def _oracle_worker_rows(task):
     import oracle
     r0, r1, xq = task
-    fmt, w, cols = _ORACLE_W
-    y, _ = oracle.dmmv(fmt, w[r0:r1].reshape(-1), r1 - r0, cols, xq)
+    fmt, w, cols, _ = _ORACLE_W
+    y, _ = oracle.dmmv(fmt, w[r0:r1], r1 - r0, cols, xq)
     return r0, y
 
 
-def cpu_baseline_parallel(cfg, budget_s: float = 12.0):
-    """The same oracle, unchanged, on every core this process may use: each layer's
-    rows are split over a pool of spawned worker processes (the per-row arithmetic
-    is unchanged, so the result is bit-identical to the single-threaded run)."""
-    import multiprocessing as mp
+class OracleStep:
+    """One step of a Dense workload on the CPU oracle, unchanged: quantize the
+    activation (oracle.quantize_q8_0), then the oracle DMMV with the rows split
+    over `workers` spawned processes (1: in this process). The per-row arithmetic
+    does not depend on the split, so every split gives the same bits."""
+
+    def __init__(self, cfg, workers: int):
+        import multiprocessing as mp
+        from multiprocessing import shared_memory
+        import numpy as np
+        import oracle
+        from gguf_block_quant_gb300 import synth
+        oracle.lib()
+        self.cfg, self.workers = cfg, workers
+        w = synth.weight_blocks(cfg.fmt, cfg.rows, cfg.cols, seed=cfg.seed)
+        self.x = synth.activations(cfg.cols, seed=cfg.seed, scale=cfg.x_scale)
+        self.pool = None
+        if workers == 1:
+            self.w = w
+            return
+        row_bytes = cfg.nb * synth.BLOCK_BYTES[cfg.fmt]
+        self.shm = shared_memory.SharedMemory(create=True, size=w.nbytes)
+        self.w = np.ndarray(w.shape, dtype=np.uint8, buffer=self.shm.buf)
+        self.w[:] = w
+        del w
+        self.bounds = [cfg.rows * i // workers for i in range(workers + 1)]
+        self.pool = mp.get_context("spawn").Pool(workers, initializer=_oracle_worker_init,
+                                                 initargs=(cfg.fmt, self.shm.name, cfg.rows, row_bytes, cfg.cols))
+
+    def __call__(self):
+        import numpy as np
+        import oracle
+        c = self.cfg
+        xq = oracle.quantize_q8_0(self.x)
+        if self.pool is None:
+            y, _ = oracle.dmmv(c.fmt, self.w, c.rows, c.cols, xq)
+            return y
+        y = np.empty(c.rows)
+        tasks = [(self.bounds[i], self.bounds[i + 1], xq) for i in range(self.workers)]
+        for r0, part in self.pool.map(_oracle_worker_rows, tasks):
+            y[r0:r0 + len(part)] = part
+        return y
+
+    def close(self):
+        if self.pool is not None:
+            self.pool.close()
+            self.pool.join()
+            self.w = None
+            self.shm.close()
+            self.shm.unlink()
+            self.pool = None
+
+
+def cpu_baseline(cfg, budget_s: float = 12.0):
+    """Time the oracle (as it stands) on a bounded sample of the workload: whole
+    steps (quantize + DMMV of the full matrix) until about budget_s of CPU time,
+    with the rows split over one spawned worker per core this process may use;
+    the same on one thread beside it. The parallel result is checked bit for bit
+    against the single-threaded one."""
     import numpy as np
-    import oracle
-    from gguf_block_quant_gb300 import synth
-    w = synth.weight_blocks(cfg.fmt, cfg.rows, cfg.cols, seed=cfg.seed)
-    x = synth.activations(cfg.cols, seed=cfg.seed, scale=cfg.x_scale)
     cores = len(os.sched_getaffinity(0))
-    bounds = [cfg.rows * i // cores for i in range(cores + 1)]
-    with mp.get_context("spawn").Pool(cores, initializer=_oracle_worker_init,
-                                      initargs=(cfg.fmt, w.tobytes(), cfg.rows, cfg.cols)) as pool:
-        def layer():
-            xq = oracle.quantize_q8_0(x)
-            y = np.empty(cfg.rows)
-            for r0, part in pool.map(_oracle_worker_rows, [(bounds[i], bounds[i + 1], xq) for i in range(cores)]):
-                y[r0:r0 + len(part)] = part
-            return y, xq
-        y, xq = layer()  # workers started and warm
-        y1, _ = oracle.dmmv(cfg.fmt, w, cfg.rows, cfg.cols, xq)
-        if not np.array_equal(y, y1):
-            raise RuntimeError("parallel oracle disagrees with the single-threaded oracle")
-        done = 0
-        t0 = time.perf_counter()
-        while True:
-            layer()
-            done += 1
-            el = time.perf_counter() - t0
-            if el >= budget_s or done >= 20000:
-                break
-    return {"value": done * cfg.algorithmic_bytes() / el / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
-            "sample": f"{done} layers ({cfg.name}: quantize + DMMV each) in {el:.1f} s, rows split over {cores} "
-                      f"worker processes", "rows_per_s": done * cfg.rows / el}
+    out = {}
+    for workers in dict.fromkeys((cores, 1)):
+        step = OracleStep(cfg, workers)
+        try:
+            y = step()   # workers started and warm
+            if "y" in out and not np.array_equal(y, out["y"]):
+                raise RuntimeError("parallel oracle disagrees with the single-threaded oracle")
+            out["y"] = y
+            done, t0 = 0, time.perf_counter()
+            while True:
+                step()
+                done += 1
+                el = time.perf_counter() - t0
+                if el >= budget_s or done >= 20000:
+                    break
+        finally:
+            step.close()
+        out[workers] = {"value": round(done * cfg.algorithmic_bytes() / el / 1e9, 3), "unit": "GB/s",
+                        "cores": workers, "kind": "oracle",
+                        "sample": f"{done} whole steps (quantize + DMMV) in {el:.1f} s"
+                                  + (f", rows over {workers} processes" if workers > 1 else ", one thread"),
+                        "rows_per_s": round(done * cfg.rows / el)}
+    res = out[cores]
+    res["single_thread"] = out[1]
+    return res
 
 
 # ----------------------------------------------------------------- GPU arm
@@ -444,10 +476,16 @@ def measure_argmax(cfg, layers, steps, warmup, world, device, eager):
             "launches": 2, "note": "DMMV with per-CTA (max, row) partials + one-CTA reduce; logits never written"}
 
 
+MOE_LAYERS = 40   # the pages' 35B-A3B model: 40 layers, each with its own experts
+
+
 def measure_moe(steps, warmup, world, device, eager, l2_bytes):
     """Config: 9 selected experts (8 routed + shared) of a 129-slot stack; one
-    step = gate, up (Q4_0 512x2048) and down (Q8_0 2048x512) gathers, each ONE
-    launch; stacks rotated over copies so that > 4x L2 is touched per pass."""
+    step = gate, up (Q4_0 512x2048) and down (Q8_0 2048x512) gathers over
+    MOE_LAYERS layers, each layer with its OWN stacks (296 MB per layer) and its
+    own routing, like a decode token. Between two reads of any expert (the shared
+    slot included) the step touches every other layer's experts, MOE_LAYERS x
+    20.6 MB, more than 4x L2, so every read comes from HBM."""
     import numpy as np
     import torch
     from gguf_block_quant_gb300 import synth
@@ -458,11 +496,10 @@ def measure_moe(steps, warmup, world, device, eager, l2_bytes):
                                               stream=synth.S_WEIGHT2)).cuda()
     down = torch.from_numpy(synth.weight_blocks(synth.Q8_0, m.n_slots * m.hidden, m.ffn, seed=m.seed,
                                                 stream=synth.S_WEIGHT3)).cuda()
-    # different routing per layer so touched experts differ; stacks are 296 MB per layer set
-    n_sets = 2
-    stacks = [(gate, up, down)] + [(gate.clone(), up.clone(), down.clone()) for _ in range(n_sets - 1)]
-    idxs = [torch.from_numpy(synth.expert_indices(m.seed + 100 * i, m.n_routed, m.top_k)).cuda()
-            for i in range(8)]
+    layers = MOE_LAYERS
+    stacks = [(gate, up, down)] + [(gate.clone(), up.clone(), down.clone()) for _ in range(layers - 1)]
+    idxs = [torch.from_numpy(synth.expert_indices(m.seed + 100 * l, m.n_routed, m.top_k)).cuda()
+            for l in range(layers)]
     x = torch.from_numpy(synth.activations(m.hidden, seed=m.seed)).cuda()
     xd = torch.from_numpy(np.ascontiguousarray(
         synth.activations(m.ffn, seed=m.seed, stream=synth.S_ACT2, batch=m.n_sel)).reshape(-1)).cuda()
@@ -473,12 +510,12 @@ def measure_moe(steps, warmup, world, device, eager, l2_bytes):
     yd = torch.empty(m.n_sel, m.hidden, device="cuda")
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
     gu, dn = m.gate_up_bytes(), m.down_bytes()
-    layers = 16
+    touched = m.n_sel * (2 * gu + dn)
 
     def step3():
         for l in range(layers):
-            g, u, d = stacks[l % n_sets]
-            idx = idxs[l % len(idxs)]
+            g, u, d = stacks[l]
+            idx = idxs[l]
             Z.expert_gather(Z.Q4_0, g, gu, m.ffn, m.hidden, idx, m.n_slots, xq, 0, y=yg, status=st)
             Z.expert_gather(Z.Q4_0, u, gu, m.ffn, m.hidden, idx, m.n_slots, xq, 0, y=yu, status=st)
             Z.expert_gather(Z.Q8_0, d, dn, m.hidden, m.ffn, idx, m.n_slots, xqd, (m.ffn // 32) * 34, y=yd,
@@ -486,8 +523,8 @@ def measure_moe(steps, warmup, world, device, eager, l2_bytes):
 
     def step2():
         for l in range(layers):
-            g, u, d = stacks[l % n_sets]
-            idx = idxs[l % len(idxs)]
+            g, u, d = stacks[l]
+            idx = idxs[l]
             Z.expert_gather2(Z.Q4_0, g, u, gu, m.ffn, m.hidden, idx, m.n_slots, xq, 0, y_a=yg, y_b=yu, status=st)
             Z.expert_gather(Z.Q8_0, d, dn, m.hidden, m.ffn, idx, m.n_slots, xqd, (m.ffn // 32) * 34, y=yd,
                             status=st)
@@ -496,8 +533,8 @@ def measure_moe(steps, warmup, world, device, eager, l2_bytes):
 
     def step_swiglu():
         for l in range(layers):
-            g, u, d = stacks[l % n_sets]
-            idx = idxs[l % len(idxs)]
+            g, u, d = stacks[l]
+            idx = idxs[l]
             Z.expert_swiglu(Z.Q4_0, g, u, m.ffn, m.hidden, xq, idx=idx, expert_stride=gu, n_experts=m.n_slots,
                             h=h, status=st)
             Z.expert_gather(Z.Q8_0, d, dn, m.hidden, m.ffn, idx, m.n_slots, xqd, (m.ffn // 32) * 34, y=yd,
@@ -508,8 +545,8 @@ def measure_moe(steps, warmup, world, device, eager, l2_bytes):
     def step_chain():
         # the same FFN through separate launches: SwiGLU, quantize h, down gather of h
         for l in range(layers):
-            g, u, d = stacks[l % n_sets]
-            idx = idxs[l % len(idxs)]
+            g, u, d = stacks[l]
+            idx = idxs[l]
             Z.expert_swiglu(Z.Q4_0, g, u, m.ffn, m.hidden, xq, idx=idx, expert_stride=gu, n_experts=m.n_slots,
                             h=h, status=st)
             Z.quantize_act_q8_0(h.reshape(-1), hq)
@@ -520,16 +557,17 @@ def measure_moe(steps, warmup, world, device, eager, l2_bytes):
 
     def step_ffn():
         for l in range(layers):
-            g, u, d = stacks[l % n_sets]
-            idx = idxs[l % len(idxs)]
-            Z.expert_ffn(Z.Q4_0, g, u, gu, Z.Q8_0, d, dn, m.hidden, m.ffn, idx, m.n_slots, xq, y=yd,
+            g, u, d = stacks[l]
+            Z.expert_ffn(Z.Q4_0, g, u, gu, Z.Q8_0, d, dn, m.hidden, m.ffn, idxs[l], m.n_slots, xq, y=yd,
                          workspace=ws, status=st)
 
     nbytes = m.algorithmic_bytes()
     # the SwiGLU epilogue writes h instead of the gate and up outputs
     nbytes_swiglu = nbytes - m.n_sel * m.ffn * 4
     out = {"layers": layers, "algorithmic_bytes": nbytes,
-           "note": "touched experts differ per layer; stack copies alternate (some L2 reuse possible)"}
+           "reuse_distance_bytes": layers * touched, "l2_bytes": l2_bytes,
+           "note": f"{layers} layers, each with its own 129-slot stacks and routing: "
+                   f"{layers * touched / 1e6:.0f} MB touched between two reads of any expert"}
     for name, fn, launches, nb_ in (("three_launch", step3, 3, nbytes), ("gate_up_fused", step2, 2, nbytes),
                                     ("gate_up_swiglu", step_swiglu, 2, nbytes_swiglu),
                                     ("ffn_chained_three_launch", step_chain, 3, nbytes_swiglu),
@@ -540,78 +578,133 @@ def measure_moe(steps, warmup, world, device, eager, l2_bytes):
         out[name] = {"us_per_token_layer": per_layer * 1e6, "gbs": nb_ / per_layer / 1e9,
                      "algorithmic_bytes": nb_,
                      "rows_per_s": m.n_sel * (2 * m.ffn + m.hidden) / per_layer, "launches_per_layer": launches}
+        del run
     out["ffn_one_launch"]["note"] = ("gate/up + SwiGLU and the down DMMV of the quantized SwiGLU output in one "
                                      "launch (the down input is h, not the independent activation)")
     out["ffn_chained_three_launch"]["note"] = "the same chained FFN as SwiGLU, quantize h, down gather"
-    out["gbs"] = max(out[k]["gbs"] for k in ("three_launch", "gate_up_fused", "gate_up_swiglu", "ffn_one_launch"))
+    if Z.device_status() != 0 or int(st.item()) != 0:
+        raise RuntimeError("MoE measurement: the device reported a fault or a bad expert index")
+    del stacks, gate, up, down
+    torch.cuda.empty_cache()
     return out
 
 
-def e2e_dense(cfg, layers, steps, warmup, world, device, eager=False):
-    """End to end through the public API: every step uploads the step's fp32
-    activations (one per layer) from pinned host memory, runs the fused
-    quantize + DMMV of every layer, and reads every layer's output back into
-    pinned host memory; copies and kernels are replayed as one graph (the pages
-    fold the token's upload and readback into the graph as copy nodes)."""
+def run_step_sequence(step_fn, k: int, w: int, world: int, device, eager: bool, sampler=None):
+    """Time EXACTLY k steps: step_fn(i) issues step i on the current stream.
+    The w warm-up steps and the k timed steps are each captured in one CUDA
+    graph (or issued eagerly with eager=True); the timed region, bracketed by a
+    barrier and a synchronize on both sides, is one replay of the k-step graph,
+    timed with CUDA events on the launching stream. Returns (ms, clocks), ms the
+    max over ranks."""
+    import torch
+
+    def seq(n, base):
+        def f():
+            for i in range(n):
+                step_fn(base + i)
+        return f
+
+    warm = graph_or_eager(seq(max(w, 1), 0), eager)
+    timed = graph_or_eager(seq(k, max(w, 1)), eager)
+    warm()
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    if sampler:
+        sampler.start()
+        time.sleep(0.05)
+    e0.record(stream)
+    timed()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop() if sampler else None
+    barrier(world)
+    return reduce_max(e0.elapsed_time(e1), world, device), clocks
+
+
+LM_HEAD_COPIES = 3   # 3 x 286 MB = 859 MB of distinct weights, more than 4x the 129 MB L2
+
+
+def headline_config(cfg, copies: int) -> dict:
+    """The headline workload's config, identical in both arms."""
+    return {"workload": cfg.name, "rows": cfg.rows, "cols": cfg.cols, "format": "Q4_0", "batch": 1,
+            "step": "one decode token's vocab projection: fp32 activation -> Q8_0 quantization + DMMV "
+                    "(one fused launch) -> fp32 logits",
+            "l2": f"inputs larger than L2: each step streams a {cfg.weight_bytes / 1e6:.0f} MB matrix; steps "
+                  f"alternate over {copies} distinct copies ({copies * cfg.weight_bytes / 1e6:.0f} MB, more than "
+                  f"4x the 129 MB L2)",
+            "parallelism": "replicas (one independent problem per GPU)"}
+
+
+def e2e_host_step(cfg, copies, k, w, world, device, eager=False):
+    """End to end through the host-buffer C-ABI call, one zdmmv_host_step per
+    step (step i on copy i % copies). The host buffers are page-locked, so the
+    call moves the data without copy calls: its quantizer reads the step's fp32
+    activation from host memory and its DMMV stores the step's output into host
+    memory."""
     import numpy as np
     import torch
     from gguf_block_quant_gb300 import synth
     from gguf_block_quant_gb300 import zdmmv as Z
-    w = torch.from_numpy(synth.weight_blocks(cfg.fmt, cfg.rows, cfg.cols, seed=cfg.seed)).cuda()
-    ws_ = [w] + [w.clone() for _ in range(layers - 1)]
+    wt = torch.from_numpy(synth.weight_blocks(cfg.fmt, cfg.rows, cfg.cols, seed=cfg.seed)).cuda()
+    ws_ = [wt] + [wt.clone() for _ in range(copies - 1)]
     x = synth.activations(cfg.cols, seed=cfg.seed, scale=cfg.x_scale)
-    xh = torch.from_numpy(np.ascontiguousarray(np.tile(x, (layers, 1)))).pin_memory()
-    yh = torch.empty(layers, cfg.rows, dtype=torch.float32).pin_memory()
-    xd = torch.empty(layers, cfg.cols, dtype=torch.float32, device="cuda")
-    yd = torch.empty(layers, cfg.rows, dtype=torch.float32, device="cuda")
-
-    def step():
-        xd.copy_(xh, non_blocking=True)
-        for l in range(layers):
-            Z.dmmv_f32(cfg.fmt, ws_[l], cfg.rows, cfg.cols, xd[l], y=yd[l])
-        yh.copy_(yd, non_blocking=True)
-
-    run = graph_or_eager(step, eager)
-    ms, _ = time_fn(run, steps, warmup, world, device)
-    per_step = ms / 1e3 / steps
-    return {"value": layers * cfg.algorithmic_bytes() * world / per_step / 1e9, "unit": "GB/s",
-            "h2d_bytes_per_step": xh.numel() * 4, "d2h_bytes_per_step": yh.numel() * 4,
-            "ms_per_step": ms / steps,
-            "launch": ("eager" if eager else "cuda_graph replay") +
-                      ": pinned H2D of the step's activations, fused quantize + DMMV per layer, pinned D2H of the outputs"}
-
-
-def e2e_host_step(cfg, layers, steps, warmup, world, device, eager=False):
-    """End to end through the host-buffer C-ABI call: one zdmmv_host_step per
-    layer. The buffers are page-locked, so the call moves the data without copy
-    calls: its quantizer reads the layer's fp32 activation from host memory and
-    its DMMV stores the layer's output into host memory."""
-    import numpy as np
-    import torch
-    from gguf_block_quant_gb300 import synth
-    from gguf_block_quant_gb300 import zdmmv as Z
-    w = torch.from_numpy(synth.weight_blocks(cfg.fmt, cfg.rows, cfg.cols, seed=cfg.seed)).cuda()
-    ws_ = [w] + [w.clone() for _ in range(layers - 1)]
-    x = synth.activations(cfg.cols, seed=cfg.seed, scale=cfg.x_scale)
-    xh = torch.from_numpy(np.ascontiguousarray(np.tile(x, (layers, 1)))).pin_memory()
-    yh = torch.empty(layers, cfg.rows, dtype=torch.float32).pin_memory()
+    xh = torch.from_numpy(np.ascontiguousarray(np.tile(x, (copies, 1)))).pin_memory()
+    yh = torch.empty(copies, cfg.rows, dtype=torch.float32).pin_memory()
     wsb = Z.host_step_workspace_bytes(cfg.rows, cfg.cols)
-    work = [torch.empty(wsb, dtype=torch.uint8, device="cuda") for _ in range(layers)]
+    work = [torch.empty(wsb, dtype=torch.uint8, device="cuda") for _ in range(copies)]
 
-    def step():
-        for l in range(layers):
-            Z.host_step(cfg.fmt, ws_[l], cfg.rows, cfg.cols, xh[l], yh[l], work[l])
+    def step(i):
+        c = i % copies
+        Z.host_step(cfg.fmt, ws_[c], cfg.rows, cfg.cols, xh[c], yh[c], work[c])
 
-    run = graph_or_eager(step, eager)
-    ms, _ = time_fn(run, steps, warmup, world, device)
-    per_step = ms / 1e3 / steps
-    return {"value": layers * cfg.algorithmic_bytes() * world / per_step / 1e9, "unit": "GB/s",
-            "h2d_bytes_per_step": xh.numel() * 4, "d2h_bytes_per_step": yh.numel() * 4,
-            "ms_per_step": ms / steps,
-            "launch": ("eager" if eager else "cuda_graph replay") +
-                      ": zdmmv_host_step per layer (quantizer reading the layer's activation from page-locked host "
-                      "memory, DMMV storing its output into page-locked host memory: host<->device traffic over the "
-                      "chip-to-chip link inside the kernels, no copy calls)"}
+    ms, _ = run_step_sequence(step, k, w, world, device, eager)
+    per_step = ms / 1e3 / k
+    out = {"value": round(cfg.algorithmic_bytes() * world / per_step / 1e9, 2), "unit": "GB/s",
+           "h2d_bytes_per_step": cfg.cols * 4, "d2h_bytes_per_step": cfg.rows * 4,
+           "ms_per_step": round(ms / k, 5),
+           "launch": ("eager" if eager else "graph") +
+                     " of zdmmv_host_step calls; page-locked x and y read/written by the kernels"}
+    del ws_, wt, work
+    torch.cuda.empty_cache()
+    return out
+
+
+def e2e_bulk_copies(cfg, copies, k, w, world, device, eager=False):
+    """The same step with explicit copies: a pinned H2D copy of the step's fp32
+    activation, the fused quantize + DMMV, a pinned D2H copy of the outputs."""
+    import numpy as np
+    import torch
+    from gguf_block_quant_gb300 import synth
+    from gguf_block_quant_gb300 import zdmmv as Z
+    wt = torch.from_numpy(synth.weight_blocks(cfg.fmt, cfg.rows, cfg.cols, seed=cfg.seed)).cuda()
+    ws_ = [wt] + [wt.clone() for _ in range(copies - 1)]
+    x = synth.activations(cfg.cols, seed=cfg.seed, scale=cfg.x_scale)
+    xh = torch.from_numpy(np.ascontiguousarray(np.tile(x, (copies, 1)))).pin_memory()
+    yh = torch.empty(copies, cfg.rows, dtype=torch.float32).pin_memory()
+    xd = torch.empty(copies, cfg.cols, dtype=torch.float32, device="cuda")
+    yd = torch.empty(copies, cfg.rows, dtype=torch.float32, device="cuda")
+
+    def step(i):
+        c = i % copies
+        xd[c].copy_(xh[c], non_blocking=True)
+        Z.dmmv_f32(cfg.fmt, ws_[c], cfg.rows, cfg.cols, xd[c], y=yd[c])
+        yh[c].copy_(yd[c], non_blocking=True)
+
+    ms, _ = run_step_sequence(step, k, w, world, device, eager)
+    per_step = ms / 1e3 / k
+    del ws_, wt
+    torch.cuda.empty_cache()
+    return {"value": round(cfg.algorithmic_bytes() * world / per_step / 1e9, 2), "unit": "GB/s",
+            "ms_per_step": round(ms / k, 5)}
+
+
+def pair(us: float, gbs: float, peak: float):
+    """[microseconds, % of the copy peak] for the compact summary."""
+    return [round(us, 2), round(100 * gbs / peak, 1)]
 
 
 def gpu_arm(args):
@@ -627,162 +720,174 @@ def gpu_arm(args):
     from gguf_block_quant_gb300 import zdmmv as Z
     Z.lib()
     l2 = torch.cuda.get_device_properties(device).L2_cache_size
-    cfg = synth.DENSE_Q4_0
-    layers = max(args.layers, layers_for(cfg, l2))
-    pool = DensePool(cfg, layers)
     hbm_peak, peak_kind = peaks()
-
-    # the DMMV kernel alone (activations pre-quantized): its average launch duration
-    run_dmmv = graph_or_eager(pool.dmmv_only, args.eager)
-    ms_dmmv, _ = time_fn(run_dmmv, args.steps, args.warmup, world, device)
-    per_launch = ms_dmmv / 1e3 / (args.steps * layers)
+    cfg = synth.LM_HEAD_Q4_0
+    copies = max(LM_HEAD_COPIES, layers_for(cfg, l2))
     nbytes = cfg.algorithmic_bytes()
-    achieved = nbytes / per_launch / 1e9
+    K, W = args.steps, max(args.warmup, 1)
 
-    # the two-kernel chain (quantize kernel, then DMMV kernel, per layer)
-    run_unfused = graph_or_eager(pool.step_unfused, args.eager)
-    ms_unfused, _ = time_fn(run_unfused, args.steps, args.warmup, world, device)
+    # ------------------------------------------------ the headline: LM-head tokens
+    pool = DensePool(cfg, copies)
 
-    # the headline: whole steps (fused quantize + DMMV per layer), clocks sampled meanwhile
-    run_step = graph_or_eager(pool.step, args.eager)
+    def fused_step(i):
+        c = i % copies
+        Z.dmmv_f32(cfg.fmt, pool.w[c], cfg.rows, cfg.cols, pool.x[c], y=pool.y[c])
+
+    def dmmv_step(i):
+        c = i % copies
+        Z.dmmv(cfg.fmt, pool.w[c], cfg.rows, cfg.cols, pool.xq[c], y=pool.y[c])
+
+    def two_kernel_step(i):
+        c = i % copies
+        Z.quantize_act_q8_0(pool.x[c], pool.xq[c])
+        Z.dmmv(cfg.fmt, pool.w[c], cfg.rows, cfg.cols, pool.xq[c], y=pool.y[c])
+
     sampler = ClockSampler(local)
-    ms, clocks = time_fn(run_step, args.steps, args.warmup, world, device, sampler)
-    ms_per_step = ms / args.steps
-    value = world * layers * nbytes / (ms_per_step / 1e3) / 1e9
-    rows_per_s = world * layers * cfg.rows / (ms_per_step / 1e3)
-    unfused_gbs = world * layers * nbytes / (ms_unfused / args.steps / 1e3) / 1e9
-    del pool, run_dmmv, run_step, run_unfused
+    ms, clocks = run_step_sequence(fused_step, K, W, world, device, args.eager, sampler)
+    ms_dmmv, _ = run_step_sequence(dmmv_step, K, W, world, device, args.eager)
+    ms_two, _ = run_step_sequence(two_kernel_step, K, W, world, device, args.eager)
+    if Z.device_status() != 0:
+        raise RuntimeError("the device reported a fault during the headline")
+    del pool
     torch.cuda.empty_cache()
+    ms_per_step = ms / K
+    per_launch = ms_per_step / 1e3          # one launch per step
+    achieved = nbytes / per_launch / 1e9
+    value = world * nbytes / per_launch / 1e9
+    detail = {"headline": {"fused_us": per_launch * 1e6, "dmmv_only_us": ms_dmmv / K * 1e3,
+                           "two_kernel_us_per_step": ms_two / K * 1e3, "copies": copies, "l2_bytes": l2}}
 
-    # end to end through the host-buffer C-ABI call, once per layer
-    e2e = e2e_host_step(cfg, min(layers, 64), max(3, args.steps // 4), args.warmup, world, device, args.eager)
-    # the same step with one bulk upload and one bulk readback around the device calls
-    e2e["bulk_copies"] = e2e_dense(cfg, min(layers, 64), max(3, args.steps // 4), args.warmup, world, device,
-                                   args.eager)
+    # ------------------------------------ end to end through the host-buffer call
+    e2e = e2e_host_step(cfg, copies, K, W, world, device, args.eager)
+    bulk = e2e_bulk_copies(cfg, copies, K, W, world, device, args.eager)
+    e2e["bulk_copies_gbs"] = bulk["value"]
 
-    workloads = {}
+    # ------------------------------------------------------------ other workloads
+    summary = {"unit": "[us (MoE: per token-layer), % of copy peak]",
+               cfg.name: {"fused": pair(per_launch * 1e6, achieved, hbm_peak),
+                          "dmmv": pair(ms_dmmv / K * 1e3, nbytes / (ms_dmmv / K / 1e3) / 1e9, hbm_peak),
+                          "two_kernel": pair(ms_two / K * 1e3, nbytes / (ms_two / K / 1e3) / 1e9, hbm_peak)}}
     if not args.no_extra:
-        for c in (synth.SSM_ALPHA_BETA, synth.LM_HEAD_Q4_0, *synth.BATCHED_Q8_0.values()):
-            workloads[c.name] = measure_dense(c, layers_for(c, l2), max(5, args.steps // 4), args.warmup,
-                                              world, device, args.eager)
-            workloads[c.name]["pct_of_peak"] = 100 * workloads[c.name]["dmmv_gbs"] / hbm_peak
-            rp = measure_dense(c, layers_for(c, l2), max(5, args.steps // 4), args.warmup, world, device,
-                               args.eager, layout=1)
-            workloads[c.name]["repacked_layout"] = {"dmmv_gbs": rp["dmmv_gbs"], "dmmv_us": rp["dmmv_us"],
-                                                    "pct_of_peak": 100 * rp["dmmv_gbs"] / hbm_peak}
-        for c in (synth.DENSE_Q4_0, synth.LM_HEAD_Q4_0, synth.BATCHED_Q8_0[1]):
-            xf = measure_xf32(c, layers_for(c, l2), max(5, args.steps // 4), args.warmup, world, device,
-                              args.eager)
-            xf["pct_of_peak"] = 100 * xf["gbs"] / hbm_peak
-            workloads.setdefault(c.name, {})["xf32_activation"] = xf
-        gr = measure_grouped(synth.DENSE_Q4_0, layers, max(5, args.steps // 4), args.warmup, world, device,
-                             args.eager)
-        gr["pct_of_peak"] = 100 * gr["gbs"] / hbm_peak
-        workloads.setdefault(synth.DENSE_Q4_0.name, {})["grouped_launch"] = gr
-        workloads["lm_head_q4_0_248320x2048"]["argmax_epilogue"] = measure_argmax(
-            synth.LM_HEAD_Q4_0, layers_for(synth.LM_HEAD_Q4_0, l2), max(5, args.steps // 4), args.warmup, world,
-            device, args.eager)
-        workloads["moe_experts_top8_plus_shared"] = measure_moe(max(5, args.steps // 4), args.warmup, world,
-                                                                device, args.eager, l2)
+        ns = max(5, K // 4)
+        lm = summary[cfg.name]
+        rp = measure_dense(cfg, copies, ns, W, world, device, args.eager, layout=1)
+        lm["repacked"] = pair(rp["dmmv_us"], rp["dmmv_gbs"], hbm_peak)
+        am = measure_argmax(cfg, copies, ns, W, world, device, args.eager)
+        lm["argmax"] = pair(am["us"], am["gbs"], hbm_peak)
+        xf = measure_xf32(cfg, copies, ns, W, world, device, args.eager)
+        lm["xf32"] = pair(xf["us"], xf["gbs"], hbm_peak)
+        detail[cfg.name] = {"repacked_layout": rp, "argmax_epilogue": am, "xf32_activation": xf}
+
+        d = synth.DENSE_Q4_0
+        dl = max(args.layers, layers_for(d, l2))
+        dn = measure_dense(d, dl, ns, W, world, device, args.eager)
+        gr = measure_grouped(d, dl, ns, W, world, device, args.eager)
+        dx = measure_xf32(d, dl, ns, W, world, device, args.eager)
+        summary[d.name] = {"fused_chain": pair(dn["fused_us_per_layer"], dn["fused_step_gbs"], hbm_peak),
+                           "dmmv_chain": pair(dn["dmmv_us"], dn["dmmv_gbs"], hbm_peak),
+                           "two_kernel_chain": pair(d.algorithmic_bytes() / dn["two_kernel_step_gbs"] / 1e3,
+                                                    dn["two_kernel_step_gbs"], hbm_peak),
+                           f"grouped_{dl}": pair(gr["us_per_matrix"], gr["gbs"], hbm_peak),
+                           "xf32_chain": pair(dx["us"], dx["gbs"], hbm_peak)}
+        detail[d.name] = {"chain": dn, "grouped_launch": gr, "xf32_activation": dx}
+
+        c = synth.SSM_ALPHA_BETA
+        sm = measure_dense(c, layers_for(c, l2), ns, W, world, device, args.eager)
+        summary[c.name] = {"dmmv_chain": pair(sm["dmmv_us"], sm["dmmv_gbs"], hbm_peak),
+                           "fused_chain": pair(sm["fused_us_per_layer"], sm["fused_step_gbs"], hbm_peak)}
+        detail[c.name] = sm
+
+        bsum, bdet = {}, {}
+        for b, c in synth.BATCHED_Q8_0.items():
+            r = measure_dense(c, layers_for(c, l2), ns, W, world, device, args.eager)
+            rp = measure_dense(c, layers_for(c, l2), ns, W, world, device, args.eager, layout=1)
+            bsum[f"b{b}"] = pair(r["dmmv_us"], r["dmmv_gbs"], hbm_peak)
+            bsum[f"b{b}_repacked"] = pair(rp["dmmv_us"], rp["dmmv_gbs"], hbm_peak)
+            bsum[f"b{b}_fused"] = pair(r["fused_us_per_layer"], r["fused_step_gbs"], hbm_peak)
+            bdet[c.name] = {"gguf": r, "repacked": rp}
+        c = synth.BATCHED_Q8_0[1]
+        bx = measure_xf32(c, layers_for(c, l2), ns, W, world, device, args.eager)
+        bsum["b1_xf32"] = pair(bx["us"], bx["gbs"], hbm_peak)
+        bdet["xf32_b1"] = bx
+        summary["batched_q8_0_14336x4096"] = bsum
+        detail["batched_q8_0_14336x4096"] = bdet
+
+        moe = measure_moe(ns, W, world, device, args.eager, l2)
+        summary["moe_experts_top8_plus_shared"] = {
+            k: pair(moe[k]["us_per_token_layer"], moe[k]["gbs"], hbm_peak)
+            for k in ("three_launch", "gate_up_fused", "gate_up_swiglu", "ffn_chained_three_launch",
+                      "ffn_one_launch")}
+        detail["moe_experts_top8_plus_shared"] = moe
+    if Z.device_status() != 0:
+        raise RuntimeError("the device reported a fault during the measurements")
 
     out = None
     if rank == 0:
-        cpu = None
-        if not args.no_cpu_baseline:
-            # the oracle on all the host cores this process may use; the single-threaded run beside it
-            cpu = cpu_baseline_parallel(cfg)
-            cpu["single_thread"] = cpu_baseline_dense(cfg)
+        cpu = None if args.no_cpu_baseline else cpu_baseline(cfg)
+        if cpu is not None:
+            cpu.pop("y", None)
         traffic = recorded_traffic(cfg.name)
-        traffic_dmmv = recorded_traffic(cfg.name + ":dmmv_only")
-        # the step's only kernel is the fused quantize + DMMV: its average launch
-        # duration inside the timed region
-        per_launch_fused = ms_per_step / 1e3 / layers
-        achieved_fused = nbytes / per_launch_fused / 1e9
         out = {
-            "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": K,
             "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "int8", "data": "synthetic",
-            "config": {"workload": cfg.name, "rows": cfg.rows, "cols": cfg.cols, "format": "Q4_0", "batch": 1,
-                       "layers_per_step": layers,
-                       "step": "per layer: fp32 activation -> Q8_0 quantization + DMMV (fused, one launch)",
-                       "l2": f"inputs larger than L2: {layers} distinct weight matrices "
-                             f"({layers * cfg.weight_bytes / 1e6:.0f} MB) per step, L2 {l2 / 1e6:.0f} MB",
-                       "launch": "eager" if args.eager else "cuda_graph replay", "parallelism": f"replicas x{world}"},
-            "pct_of_peak": round(100 * value / world / hbm_peak, 2),
-            "rows_per_s": rows_per_s,
-            "roofline": {"bound": "hbm", "achieved": round(achieved_fused, 1), "peak": hbm_peak, "unit": "GB/s",
-                         "frac": round(achieved_fused / hbm_peak, 4), "traffic": traffic,
-                         "kernel": "dmmv_tma_kernel with the fused Q8_0 activation quantization (Q4_0, GGUF layout)",
-                         "algorithmic_bytes_per_launch": nbytes,
-                         "us_per_launch": round(per_launch_fused * 1e6, 3),
-                         # ncu's DRAM bytes per launch over the live launch time
-                         "dram_gbs": round(traffic / per_launch_fused / 1e9, 1) if traffic else None,
-                         "peak_kind": f"{peak_kind} HBM copy bandwidth",
-                         "dmmv_only_chain": {
-                             "kernel": "dmmv_tma_kernel over pre-quantized activation blocks",
-                             "achieved": round(achieved, 1), "frac": round(achieved / hbm_peak, 4),
-                             "us_per_launch": round(per_launch * 1e6, 3), "traffic": traffic_dmmv,
-                             "dram_gbs": round(traffic_dmmv / per_launch / 1e9, 1) if traffic_dmmv else None}},
+            "config": headline_config(cfg, copies),
+            "pct_of_peak": round(100 * achieved / hbm_peak, 2),
+            "rows_per_s": round(world * cfg.rows / per_launch),
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
+                         "frac": round(achieved / hbm_peak, 4), "traffic": traffic,
+                         "kernel": "dmmv_tma_kernel (fused Q8_0 quantization)",
+                         "algorithmic_bytes_per_launch": nbytes, "us_per_launch": round(per_launch * 1e6, 3),
+                         "dram_gbs": round(traffic / per_launch / 1e9, 1) if traffic else None,
+                         "peak_kind": f"{peak_kind} HBM copy bandwidth"},
             "cpu_baseline": cpu,
             "e2e": e2e,
-            "two_kernel_chain_gbs": round(unfused_gbs, 2),
-            "gpu_launches": layers * args.steps,
+            "gpu_launches": K,
             "clocks": clocks,
-            "workloads": workloads,
+            "summary": summary,
         }
     if world > 1:
         import torch.distributed as dist
         dist.barrier()
         dist.destroy_process_group()
     if out is not None:
-        print(json.dumps(out), flush=True)
+        print("detail: " + json.dumps(detail), file=sys.stderr, flush=True)
+        print(json.dumps(out, separators=(",", ":")), flush=True)
 
 
 # ------------------------------------------------------------ reference arm
 def reference_arm(args):
+    """The CPU oracle on the headline's workload and config: each step is one
+    whole LM-head token (quantize + DMMV over all 248320 rows), rows split over
+    one spawned worker per host core. Rank 0 only."""
     world, rank, _ = dist_setup(args)
     if rank != 0:
         return
-    import multiprocessing as mp
-    import numpy as np
-    import oracle
     from gguf_block_quant_gb300 import synth
-    cfg = synth.DENSE_Q4_0
-    w = synth.weight_blocks(cfg.fmt, cfg.rows, cfg.cols, seed=cfg.seed)
-    x = synth.activations(cfg.cols, seed=cfg.seed, scale=cfg.x_scale)
-    oracle.lib()
-    layers_per_step = 8   # a bounded sample of the 64-layer step, so K steps finish in minutes
+    cfg = synth.LM_HEAD_Q4_0
     cores = len(os.sched_getaffinity(0))
-    bounds = [cfg.rows * i // cores for i in range(cores + 1)]
-    with mp.get_context("spawn").Pool(cores, initializer=_oracle_worker_init,
-                                      initargs=(cfg.fmt, w.tobytes(), cfg.rows, cfg.cols)) as pool:
-        def step():
-            for _ in range(layers_per_step):
-                xq = oracle.quantize_q8_0(x)
-                y = np.empty(cfg.rows)
-                for r0, part in pool.map(_oracle_worker_rows,
-                                         [(bounds[i], bounds[i + 1], xq) for i in range(cores)]):
-                    y[r0:r0 + len(part)] = part
-
+    step = OracleStep(cfg, cores)
+    try:
         for _ in range(max(1, args.warmup)):
             step()
         t0 = time.perf_counter()
         for _ in range(args.steps):
             step()
         el = time.perf_counter() - t0
+    finally:
+        step.close()
     ms_per_step = el * 1e3 / args.steps
-    value = layers_per_step * cfg.algorithmic_bytes() / (el / args.steps) / 1e9
+    value = cfg.algorithmic_bytes() / (el / args.steps) / 1e9
     print(json.dumps({
-        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "int8", "data": "synthetic",
-        "config": {"workload": cfg.name, "rows": cfg.rows, "cols": cfg.cols, "format": "Q4_0", "batch": 1,
-                   "layers_per_step": layers_per_step, "step": "quantize_act_q8_0 + DMMV per layer"},
-        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle",
-                         "sample": f"{layers_per_step} layers per step of {cfg.name}, C oracle with the rows "
-                                   f"split over {cores} worker processes"},
-        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
-    }), flush=True)
+        "config": headline_config(cfg, LM_HEAD_COPIES),
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{args.steps} whole steps of {cfg.name} (quantize + DMMV), C oracle with the "
+                                   f"rows split over {cores} worker processes"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }, separators=(",", ":")), flush=True)
 
 
 def profile_mode(name: str):

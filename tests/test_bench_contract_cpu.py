@@ -21,7 +21,12 @@ def test_reference_arm_json_line_has_the_contract_keys():
               "scaling", "vs_baseline", "dtype", "data", "config", "impl", "cpu_baseline", "e2e"):
         assert k in d, k
     assert d["impl"] == "reference" and d["value"] > 0 and d["steps"] == 1 and d["warmup"] == 0
-    assert d["higher_is_better"] is True and d["config"]["workload"] == "dense_q4_0_4096x4096"
+    assert d["higher_is_better"] is True and d["config"]["workload"] == "lm_head_q4_0_248320x2048"
+    # the GPU arm prints the same config dict for its headline
+    sys.path.insert(0, ROOT)
+    import bench
+    from gguf_block_quant_gb300 import synth
+    assert d["config"] == bench.headline_config(synth.LM_HEAD_Q4_0, bench.LM_HEAD_COPIES)
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"] and cb["sample"]
     e2e = d["e2e"]
