@@ -80,6 +80,32 @@ __device__ __forceinline__ float row_partial(const Pair<FMT, LAYOUT> (&xr)[PPL],
     return acc;
 }
 
+// The contributions of one lane to N rows i0, i0 + step, ... of a GGUF tile whose
+// rows and this lane's pairs all exist: every row's weight words of pair j are
+// loaded before any of them is used, then each row takes row_partial's updates in
+// row_partial's order (so the sums are the same bits).
+template <int FMT, int LPR, int PPL, int N>
+__device__ __forceinline__ void rows_partial_full(const Pair<FMT, kLayoutGguf> (&xr)[PPL], uint32_t stage, int i0,
+                                                  int step, int nb, int l, float (&acc)[N]) {
+    constexpr int kW = Pair<FMT, kLayoutGguf>::kWords;
+    const uint32_t row_bytes = static_cast<uint32_t>(nb * Fmt<FMT>::kBlockBytes);
+#pragma unroll
+    for (int r = 0; r < N; ++r) acc[r] = 0.0f;
+#pragma unroll
+    for (int j = 0; j < PPL; ++j) {
+        const uint32_t pofs = static_cast<uint32_t>(owned_pair<LPR>(l, j) * RowGeom<FMT, kLayoutGguf>::kPairBytes);
+        uint32_t w[N][kW];
+#pragma unroll
+        for (int r = 0; r < N; ++r) {
+            const uint32_t a = stage + static_cast<uint32_t>(i0 + r * step) * row_bytes + pofs;
+#pragma unroll
+            for (int k = 0; k < kW; ++k) w[r][k] = lds32(a + 4 * k);
+        }
+#pragma unroll
+        for (int r = 0; r < N; ++r) acc[r] = xr[j].fma_w(w[r], acc[r]);
+    }
+}
+
 // Bytes of tile t of a CTA's row range [r0, r1).
 template <int FMT>
 __device__ __forceinline__ uint32_t tile_bytes(const DmmvArgs &a, int64_t r0, int64_t r1, int t) {
@@ -248,6 +274,7 @@ __global__ void __launch_bounds__(kTmaThreads, MINB) dmmv_tma_kernel(const DmmvA
     const int g = tid / LPR;  // row group
     const int l = tid % LPR;  // lane inside the row group
     pdl_wait();               // outputs may still be read, and the activation written, by the preceding kernel
+    const bool full_pairs = (nb >> 1) == LPR * PPL;  // every lane owns PPL pairs of every row
     if constexpr (FX) {
         // quantize the fp32 activation into Q8_0 blocks in shared memory (nb is a
         // multiple of 8 on this path)
@@ -308,10 +335,22 @@ __global__ void __launch_bounds__(kTmaThreads, MINB) dmmv_tma_kernel(const DmmvA
             // shuffle trees interleave; every row still gets the same reduction tree
             for (int base = 0; base < nr; base += kRowsPar * kRowsIlp) {
                 float acc[kRowsIlp];
+                if constexpr (LAYOUT == kLayoutGguf) {
+                    if (full_pairs && base + kRowsPar * kRowsIlp <= nr) {
+                        rows_partial_full<FMT, LPR, PPL, kRowsIlp>(xr, st, base + g, kRowsPar, nb, l, acc);
+                    } else {
 #pragma unroll
-                for (int r = 0; r < kRowsIlp; ++r) {
-                    const int i = base + r * kRowsPar + g;
-                    acc[r] = i < nr ? row_partial<FMT, LAYOUT, LPR, PPL>(xr, st, i, T, nb, l) : 0.0f;
+                        for (int r = 0; r < kRowsIlp; ++r) {
+                            const int i = base + r * kRowsPar + g;
+                            acc[r] = i < nr ? row_partial<FMT, LAYOUT, LPR, PPL>(xr, st, i, T, nb, l) : 0.0f;
+                        }
+                    }
+                } else {
+#pragma unroll
+                    for (int r = 0; r < kRowsIlp; ++r) {
+                        const int i = base + r * kRowsPar + g;
+                        acc[r] = i < nr ? row_partial<FMT, LAYOUT, LPR, PPL>(xr, st, i, T, nb, l) : 0.0f;
+                    }
                 }
                 if constexpr (EPI == 0) {
                     // the rows' sums land on lanes 0, LPR/kRowsIlp, ... of the group
