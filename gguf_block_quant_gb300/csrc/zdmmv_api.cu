@@ -15,6 +15,7 @@
 #include "zdmmv_device.cuh"
 #include "zdmmv_internal.h"
 #include "zdmmv_mma.h"
+#include "zdmmv_xf32_mma.cuh"
 
 namespace zdmmv {
 
@@ -952,6 +953,23 @@ zdmmv_status dmmv_xf32_entry(int fmt, const void *w, int layout, int64_t rows, i
     a.nb = static_cast<int32_t>(cols / kQK);
     a.batch = 1;
     a.fault = dev->fault;
+    Xf32MmaPlan mp{};
+    if (xf32_mma_plan(fmt, layout, rows, cols, &mp)) {
+        // the fp16 tensor cores, the activation split into exact fp16 parts
+        Xf32MmaArgs m{};
+        m.w = a.w;
+        m.xf = x;
+        m.y = y;
+        m.fault = dev->fault;
+        m.rows = rows;
+        m.xf_stride = cols;
+        m.y_stride = rows;
+        m.nb = a.nb;
+        m.cb = mp.cb;
+        m.nchunks = mp.nchunks;
+        m.pitch = mp.pitch;
+        return from_cuda(launch_xf32_mma(fmt, m, mp, batch, st, pdl_enabled()));
+    }
     TmaPlan p{};
     if (xf32_plan(fmt, layout, cols, &p)) {
         a.tile_rows = p.tile_rows;

@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 namespace zdmmv {
@@ -30,6 +31,15 @@ struct MmaPlan {
     int smem_bytes;
 };
 bool mma_plan(int fmt, int layout, int64_t rows, int64_t cols, int batch, MmaPlan *out);
+
+// Shared by the tensor-core kernels. The weight rows (row_bytes each) as a 2D
+// tensor map of 8-byte elements with a box of {pitch / 8, box_rows}, cached per
+// calling thread. And the chunking of a row of nb blocks of bb bytes into the
+// fewest tensor copies whose shared-memory pitch (at most max_pitch bytes) is 4
+// mod 8 words (false when none fits).
+cudaError_t weight_map(const uint8_t *w, int64_t rows, int64_t row_bytes, int pitch, int box_rows,
+                       CUtensorMap *out);
+bool weight_chunk_plan(int nb, int bb, int max_pitch, int *cb, int *nchunks, int *pitch);
 cudaError_t launch_mma_q8(const MmaArgs &a, const MmaPlan &p, cudaStream_t st, bool pdl);
 cudaError_t launch_mma_q4(const MmaArgs &a, const MmaPlan &p, cudaStream_t st, bool pdl);
 

@@ -699,6 +699,86 @@ def test_xf32_ragged_tiles_and_zero_rows():
     Z.dmmv_xf32(fmt, dev(synth.weight_blocks(fmt, 1, cols, seed=1)), 0, cols, dev(x), y=nan_out(1))
 
 
+def _xf32_tall_rows(extra=0):
+    """Rows enough for the fp32-activation tensor-core kernel (it takes matrices
+    of at least 4 groups of 128 rows per SM), plus a ragged tail."""
+    return 4 * 128 * torch.cuda.get_device_properties(0).multi_processor_count + extra
+
+
+@pytest.mark.parametrize("fmt,cols,extra", [(Q4_0, 2048, 37), (Q8_0, 512, 0), (Q4_0, 8192, 129), (Q8_0, 768, 5)])
+def test_xf32_tall_matches_oracle(fmt, cols, extra):
+    """The tensor-core path of the fp32-activation DMMV (tall GGUF matrices):
+    every row within the tolerance of the oracle, a partial last row group
+    included, and two calls give the same bits."""
+    rows = _xf32_tall_rows(extra)
+    w = synth.weight_blocks(fmt, rows, cols, seed=cols + extra)
+    x = synth.activations(cols, seed=cols + 1)
+    y = nan_out(rows)
+    Z.dmmv_xf32(fmt, dev(w), rows, cols, dev(x), y=y)
+    y2 = nan_out(rows)
+    Z.dmmv_xf32(fmt, dev(w), rows, cols, dev(x), y=y2)
+    torch.cuda.synchronize()
+    assert torch.equal(y, y2), "two calls differ"
+    y_ref, e_ref = oracle.dmmv_xf32(fmt, w, rows, cols, x)
+    check_y(y, y_ref, e_ref)
+
+
+def test_xf32_tall_batched_slots():
+    fmt, cols, batch = Q4_0, 512, 3
+    rows = _xf32_tall_rows(64)
+    w = synth.weight_blocks(fmt, rows, cols, seed=9)
+    x = synth.activations(cols, seed=10, batch=batch)
+    y = nan_out(batch, rows)
+    Z.dmmv_xf32(fmt, dev(w), rows, cols, dev(x), batch=batch, y=y)
+    torch.cuda.synchronize()
+    for v in range(batch):
+        y_ref, e_ref = oracle.dmmv_xf32(fmt, w, rows, cols, np.asarray(x, dtype=np.float32)[v])
+        check_y(y[v], y_ref, e_ref)
+
+
+@pytest.mark.parametrize("fmt,cols", [(Q4_0, 2048), (Q8_0, 1024)])
+def test_xf32_wide_dynamic_range(fmt, cols):
+    """The tensor-core kernel splits each activation block, scaled by a power of
+    two, into three fp16 parts: blocks whose magnitudes span 1e-30 .. 1e30, a
+    1e12 range inside one block, all-zero blocks, signed zeros and blocks near
+    the fp32 normal limit still meet the tolerance."""
+    rows = _xf32_tall_rows()
+    w = synth.weight_blocks(fmt, rows, cols, seed=cols + 3)
+    g = np.random.Generator(np.random.PCG64(77))
+    nb = cols // 32
+    x = g.standard_normal(cols).astype(np.float64)
+    block_scale = 10.0 ** g.uniform(-30, 30, size=nb)
+    x *= np.repeat(block_scale, 32)
+    x[5 * 32:6 * 32] = 0.0                                   # an all-zero block
+    x[6 * 32:7 * 32] = -0.0
+    x[7 * 32:8 * 32] *= 10.0 ** g.uniform(-12, 0, size=32)   # 1e12 range inside a block
+    x[8 * 32:9 * 32] = g.standard_normal(32) * 1e-36         # near the fp32 normal limit
+    x[9 * 32] = 3.0e30                                       # one huge element, the rest tiny
+    x[9 * 32 + 1:10 * 32] = 1e-20
+    x = x.astype(np.float32)
+    y = nan_out(rows)
+    Z.dmmv_xf32(fmt, dev(w), rows, cols, dev(x), y=y)
+    torch.cuda.synchronize()
+    y_ref, e_ref = oracle.dmmv_xf32(fmt, w, rows, cols, x)
+    check_y(y, y_ref, e_ref)
+
+
+def test_xf32_exact_on_representable_activations():
+    """Unit weight scales and activations that are small integers times 2^-4:
+    every product and partial sum is an exact fp32 value, so the tensor-core
+    kernel's result equals the oracle's exactly."""
+    for fmt in (Q4_0, Q8_0):
+        rows, cols = _xf32_tall_rows(3), 512
+        w = synth.weight_blocks_small(fmt, rows, cols, seed=fmt, qmax=7)
+        g = np.random.Generator(np.random.PCG64(fmt + 1))
+        x = (g.integers(-15, 16, size=cols) / 16.0).astype(np.float32)
+        y = nan_out(rows)
+        Z.dmmv_xf32(fmt, dev(w), rows, cols, dev(x), y=y)
+        torch.cuda.synchronize()
+        y_ref, _ = oracle.dmmv_xf32(fmt, w, rows, cols, x)
+        assert np.array_equal(y.double().cpu().numpy(), y_ref), fmt
+
+
 # ------------------------------------------------- one-launch expert FFN
 def _ffn_case(fmt_gu, fmt_dn, hidden, ffn, n_exp, idx, seed):
     bgu = 18 if fmt_gu == Q4_0 else 34

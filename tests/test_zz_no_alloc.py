@@ -13,6 +13,7 @@ across a call. This file is collected last so that a run stopping at the first
 failure has run every other test; it also passes on its own in a fresh process.
 """
 import ctypes
+import gc
 
 import numpy as np
 import pytest
@@ -89,12 +90,20 @@ def test_no_alloc_argmax_allocates_nothing():
     assert _noalloc(L, fmt, wd, layout, rows, cols, xqd, idx, mx) == 0   # the first call sets the device up
     torch.cuda.synchronize()
     first = int(idx.item())
-    torch_before = torch.cuda.memory_allocated()
-    free_before, _ = torch.cuda.mem_get_info()
-    for _ in range(2):
-        assert _noalloc(L, fmt, wd, layout, rows, cols, xqd, idx, mx) == 0
-    torch.cuda.synchronize()
-    free_after, _ = torch.cuda.mem_get_info()
-    assert torch.cuda.memory_allocated() == torch_before
+    # tensors of earlier tests are freed by the garbage collector at arbitrary
+    # points: collect them now and keep the collector off while measuring
+    gc.collect()
+    gc.disable()
+    try:
+        torch_before = torch.cuda.memory_allocated()
+        free_before, _ = torch.cuda.mem_get_info()
+        for _ in range(2):
+            assert _noalloc(L, fmt, wd, layout, rows, cols, xqd, idx, mx) == 0
+        torch.cuda.synchronize()
+        free_after, _ = torch.cuda.mem_get_info()
+        torch_after = torch.cuda.memory_allocated()
+    finally:
+        gc.enable()
+    assert torch_after == torch_before
     assert free_after == free_before
     assert int(idx.item()) == first
