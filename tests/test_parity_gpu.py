@@ -215,7 +215,8 @@ def test_repack_bit_exact(fmt, rows, cols):
 # ----------------------------------------------------------------- batched
 @pytest.mark.parametrize("layout", [Z.GGUF, Z.REPACKED])
 @pytest.mark.parametrize("fmt,rows,cols", [(Q8_0, 1434, 4096), (Q4_0, 901, 2048), (Q8_0, 99, 160),
-                                           (Q4_0, 300, 8192), (Q8_0, 257, 3072), (Q8_0, 77, 512)])
+                                           (Q4_0, 300, 8192), (Q8_0, 257, 3072), (Q8_0, 77, 512),
+                                           (Q4_0, 411, 2304)])
 @pytest.mark.parametrize("batch", [1, 2, 3, 4, 7, 8])
 def test_batched_matches_oracle_and_single_calls(fmt, rows, cols, batch, layout):
     w = synth.weight_blocks(fmt, rows, cols, seed=batch)
