@@ -16,6 +16,7 @@
 #include "zdmmv_internal.h"
 #include "zdmmv_mma.h"
 #include "zdmmv_xf32_mma.cuh"
+#include "zdmmv_bmma.cuh"
 
 namespace zdmmv {
 
@@ -183,18 +184,26 @@ TmaPlan tma_plan(int fmt, int layout, int64_t cols, int halves) {
 }
 
 namespace {
-// Batched kernel choice (environment ZDMMV_BATCH_KERNEL): "vsplit" (default),
-// "mma" (the integer tensor-core kernel where it takes the shape, else the
-// vector split; slower on this part, kept for the measurement), "stream"
-// (dmmv_batch_kernel) or "slots" (single-vector slots, as ZDMMV_BATCH_SLOTS=1).
+// Batched kernel choice (environment ZDMMV_BATCH_KERNEL). Unset: the fp16
+// tensor-core kernel for kBmmaMinBatch..8 vectors where it takes the shape and
+// has a 32-row group for every SM, else the vector split, else the streaming
+// batch kernel. "vsplit": never the tensor-core kernel. "mma": the tensor-core
+// kernel wherever it takes the shape (2..8 vectors). "stream": dmmv_batch_kernel.
+// "slots": single-vector slots (as ZDMMV_BATCH_SLOTS=1).
+enum BatchChoice { kBatchAuto = 0, kBatchStream = 1, kBatchSlots = 2, kBatchMma = 3, kBatchVsplit = 4 };
+// From 5 vectors on the vector split is bound by its dp4a issue (Q8_0 14336 x
+// 4096: 10.8 / 11.8 / 15.2 / 15.3 us at 2 / 4 / 5 / 8 vectors) and the
+// tensor-core kernel is faster (12.7 us at any batch).
+constexpr int kBmmaMinBatch = 5;
 int batch_kernel_choice() {
     static const int v = [] {
         const char *e = std::getenv("ZDMMV_BATCH_KERNEL");
-        if (!e) return 0;
-        if (std::strcmp(e, "stream") == 0) return 1;
-        if (std::strcmp(e, "slots") == 0) return 2;
-        if (std::strcmp(e, "mma") == 0) return 3;
-        return 0;
+        if (!e) return static_cast<int>(kBatchAuto);
+        if (std::strcmp(e, "stream") == 0) return static_cast<int>(kBatchStream);
+        if (std::strcmp(e, "slots") == 0) return static_cast<int>(kBatchSlots);
+        if (std::strcmp(e, "mma") == 0) return static_cast<int>(kBatchMma);
+        if (std::strcmp(e, "vsplit") == 0) return static_cast<int>(kBatchVsplit);
+        return static_cast<int>(kBatchAuto);
     }();
     return v;
 }
@@ -678,29 +687,34 @@ zdmmv_status dmmv_entry(int fmt, const void *w, zdmmv_layout layout, int64_t row
     BatchPlan bp{};
     TmaPlan vp{};
     int vv = 0, nvg = 0;
-    const int choice = batch_slots_forced() ? 2 : batch_kernel_choice();
-    MmaPlan mp{};
-    if (batch >= 2 && choice == 3 && mma_plan(fmt, layout, rows, cols, batch, &mp)) {
-        // one weight stream, all vectors on the tensor cores
+    const int choice = batch_slots_forced() ? kBatchSlots : batch_kernel_choice();
+    BmmaPlan hp{};
+    if (batch >= 2 && (choice == kBatchMma || (choice == kBatchAuto && batch >= kBmmaMinBatch)) &&
+        bmma_plan(fmt, layout, rows, cols, batch, &hp)) {
+        // one weight stream, all vectors on the fp16 tensor cores (by default only
+        // where every SM gets a 32-row group: on fewer rows the vector split's
+        // finer row split keeps more SMs streaming)
         const DeviceInfo *dev = nullptr;
         if (device_info(&dev) != cudaSuccess) return ZDMMV_ERR_CUDA;
-        MmaArgs m{};
-        m.w = a.w;
-        m.xq = a.xq;
-        m.y = y;
-        m.fault = dev->fault;
-        m.rows = rows;
-        m.y_stride = rows;
-        m.nb = a.nb;
-        m.batch = batch;
-        m.cb = mp.cb;
-        m.nchunks = mp.nchunks;
-        m.pitch = mp.pitch;
-        m.x_region = mp.x_region;
-        cudaError_t e = fmt == kFmtQ8 ? launch_mma_q8(m, mp, st, pdl_enabled()) : launch_mma_q4(m, mp, st, pdl_enabled());
-        return from_cuda(e);
+        if (choice == kBatchMma || (rows + kBmGroupRows - 1) / kBmGroupRows >= dev->sms) {
+            BmmaArgs m{};
+            m.w = a.w;
+            m.xq = a.xq;
+            m.y = y;
+            m.fault = dev->fault;
+            m.rows = rows;
+            m.xq_stride = static_cast<int64_t>(a.nb) * 34;
+            m.y_stride = rows;
+            m.nb = a.nb;
+            m.batch = batch;
+            m.nchunks = hp.nchunks;
+            m.pitch = hp.pitch;
+            m.red_bufs = hp.red_bufs;
+            return from_cuda(launch_bmma(fmt, m, hp, st, pdl_enabled()));
+        }
     }
-    if (batch >= 2 && (choice == 0 || choice == 3) && vsplit_plan(fmt, layout, cols, batch, &vp, &vv, &nvg)) {
+    if (batch >= 2 && (choice == kBatchAuto || choice == kBatchMma || choice == kBatchVsplit) &&
+        vsplit_plan(fmt, layout, cols, batch, &vp, &vv, &nvg)) {
         // one weight stream, the vectors split over the warps
         const DeviceInfo *dev = nullptr;
         if (device_info(&dev) != cudaSuccess) return ZDMMV_ERR_CUDA;
@@ -716,7 +730,7 @@ zdmmv_status dmmv_entry(int fmt, const void *w, zdmmv_layout layout, int64_t row
                                       : launch_vsplit_q4(a, vp, layout, vv, nvg, cap, st, pdl_enabled());
         return from_cuda(e);
     }
-    if (batch >= 2 && choice != 2 && batch_plan(fmt, cols, batch, &bp)) {
+    if (batch >= 2 && choice != kBatchSlots && batch_plan(fmt, cols, batch, &bp)) {
         // one weight stream for all vectors
         const DeviceInfo *dev = nullptr;
         if (device_info(&dev) != cudaSuccess) return ZDMMV_ERR_CUDA;
@@ -1002,7 +1016,8 @@ zdmmv_status dmmv_f32_entry(int fmt, const void *w, int layout, int64_t rows, in
     a.nb = static_cast<int32_t>(cols / kQK);
     TmaPlan vp{};
     int vv = 0, nvg = 0;
-    if (batch >= 2 && !batch_slots_forced() && batch_kernel_choice() == 0 &&
+    if (batch >= 2 && !batch_slots_forced() &&
+        (batch_kernel_choice() == kBatchAuto || batch_kernel_choice() == kBatchVsplit) &&
         vsplit_plan(fmt, layout, cols, batch, &vp, &vv, &nvg)) {
         // one weight stream for the batch, its activations quantized in the prologue
         const DeviceInfo *dev = nullptr;

@@ -19,12 +19,11 @@
 // The order of the fp32 sums differs from the scalar kernel, so the results
 // agree with it within the fp32 tolerance, not bit for bit.
 //
-// The weights stream as in the integer tensor-core kernel (zdmmv_mma.cuh): a
-// producer warp issues one 2D tensor copy per stage (a group of 16-row slabs,
-// one per consumer warp, by a chunk of blocks) whose shared-memory pitch is 4
-// mod 8 words, so the fragment loads of the 8 rows of a lane quad hit distinct
-// banks; the lane loads the aligned words of each GGUF block pair that the
-// integer kernel's MmaRowPair loads (here at immediate offsets, 8 blocks per
+// The weights stream as described in zdmmv_mma.cuh: a producer warp issues one
+// 2D tensor copy per stage (a group of 16-row slabs, one per consumer warp, by a
+// chunk of blocks) whose shared-memory pitch is 4 mod 8 words, so the fragment
+// loads of the 8 rows of a lane quad hit distinct banks; the lane loads the
+// aligned words of each GGUF block pair (XmRow, at immediate offsets, 8 blocks per
 // stage, the pairs unrolled) and the k-slot of each code is chosen to match the
 // word it arrives in; the activation fragments use the same order.
 #pragma once
@@ -236,8 +235,13 @@ __device__ __forceinline__ uint4 ldsi128(uint32_t base) {
 }
 
 
-// One block pair P (blocks 2P, 2P + 1 of the chunk) of one row of a stage, the
-// loads of MmaRowPair at immediate offsets: r = the staged row, rt = r + 4t.
+// One block pair P (blocks 2P, 2P + 1 of the chunk) of one row of a stage, at
+// immediate offsets from r = the staged row and rt = r + 4t: both blocks' scales
+// and lane t's aligned code words. Q8_0: words (k-slots of MMA 0, of MMA 1) of the
+// even block, codes 2 + 4t.. and 18 + 4t.. (ea, eb; the last lane's eb completed
+// from the pair's first word) and of the odd block, codes 4t.. and 16 + 4t.. (oa,
+// ob). Q4_0: one word of quant bytes per block (ea, oa), its low nibbles for MMA
+// 0 and its high nibbles for MMA 1.
 template <int FMT> struct XmRow;
 template <> struct XmRow<kFmtQ4> {
     uint32_t ea, oa;

@@ -52,18 +52,20 @@
  *      ZDMMV_CTAS_PER_SM        CTAs per SM of the single-vector kernel (1..8;
  *                               default 2 below 32 MB of weights per launch, else 4;
  *                               expert gathers as many as fit)
- *      ZDMMV_BATCH_KERNEL       batched kernel: vsplit (default), mma, stream, or
- *                               slots (one single-vector slot per vector); "mma"
- *                               (integer tensor cores, GGUF rows of 256-column
- *                               multiples up to 4096 and >= 16 rows, else vsplit)
- *                               and "stream" change the fp32 reduction order of
- *                               batch > 1
- *      ZDMMV_MMA_WARPS=16       16 consumer warps in the "mma" kernel (default 8)
- *      ZDMMV_MMA_STAGES         pipeline stages of the "mma" kernel (2..6, default
- *                               as many as fit)
+ *      ZDMMV_BATCH_KERNEL       batched kernel (see zdmmv_q8_0_batched for the
+ *                               default choice): "vsplit" (the vector split, never
+ *                               the tensor-core kernel), "mma" (the tensor-core
+ *                               kernel wherever it takes the shape, 2..8 vectors,
+ *                               else the vector split), "stream", or "slots" (one
+ *                               single-vector slot per vector). Every choice keeps
+ *                               the result within the stated tolerance; the fp32
+ *                               reduction order of batch > 1 follows the kernel
+ *                               (for "vsplit" and "slots" it is the single-vector
+ *                               order)
  *      ZDMMV_BATCH_SLOTS=1      the same as ZDMMV_BATCH_KERNEL=slots
  *      ZDMMV_VSPLIT_V=1         one vector per warp in the vector-split kernel;
- *                               batches of more than 4 vectors then take the
+ *                               batches of more than 4 vectors that the
+ *                               tensor-core kernel does not take then take the
  *                               "stream" kernel (its fp32 reduction order)
  *      ZDMMV_BATCH_CTAS_PER_SM  CTAs per SM of the batched kernels (1..4)
  *      ZDMMV_FFN_STAGES=3       three pipeline stages in zdmmv_expert_ffn (default 2)
@@ -154,14 +156,24 @@ zdmmv_status zdmmv_q4_0(const void *w, zdmmv_layout layout, int64_t rows, int64_
  * xq is [batch][cols/32] Q8_0 blocks, y is [batch][rows] fp32. Each weight tile
  * is streamed from HBM once and dotted against every vector (concurrency
  * headroom of decode slots: habr article, section "RDNA4: что мы узнали о
- * железе"). For widths that are multiples of 256 up to 4096 columns (up to 8192
- * with batch <= 4) the consumer warps split the vectors and every vector's
- * result is the single-vector computation, bit for bit: y[v] equals zdmmv_q8_0 /
- * zdmmv_q4_0 on vector v. Widths of 8192 columns with batch > 4 stream the tile
- * through a kernel whose fp32 reduction order differs (deterministic, within
- * the stated tolerance); other widths run the single-vector computation once per
- * vector. batch == 1 is zdmmv_q8_0 / zdmmv_q4_0. These are the default kernels;
- * the environment variable ZDMMV_BATCH_KERNEL (above) selects others.
+ * железе"). Default kernels:
+ *  - batch 5..8, GGUF layout, widths that are multiples of 256 from 1280 to
+ *    4096 columns, and at least 32 rows per SM of the device (4864 rows on a
+ *    152-SM GB300): the fp16 tensor-core kernel. Each block's integer dot
+ *    product is exact (the pages' int32 block sum) and its scales are applied in
+ *    fp32, but the blocks of a row are summed in another order than the
+ *    single-vector kernel's: deterministic, within the stated tolerance, not
+ *    bit for bit zdmmv_q8_0 on each vector;
+ *  - other widths that are multiples of 256 up to 4096 columns (up to 8192 with
+ *    batch <= 4): the consumer warps split the vectors and every vector's result
+ *    is the single-vector computation, bit for bit: y[v] equals zdmmv_q8_0 /
+ *    zdmmv_q4_0 on vector v;
+ *  - widths of 8192 columns with batch > 4 stream the tile through a kernel
+ *    whose fp32 reduction order differs (deterministic, within the stated
+ *    tolerance); other widths run the single-vector computation once per
+ *    vector.
+ * batch == 1 is zdmmv_q8_0 / zdmmv_q4_0. The environment variable
+ * ZDMMV_BATCH_KERNEL (above) selects other kernels.
  * Errors: as zdmmv_q8_0, plus ERR_SHAPE for batch outside 1..8. */
 zdmmv_status zdmmv_q8_0_batched(const void *w, zdmmv_layout layout, int64_t rows,
                                 int64_t cols, const void *xq, int batch, float *y,

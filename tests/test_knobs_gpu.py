@@ -3,14 +3,16 @@
 reads them once per process), over one fixed set of cases: single-vector DMMVs
 in both layouts, the fused quantize + DMMV, batched calls of 2-8 vectors
 (widths the vector split, the streaming batch kernel and the tensor-core kernel
-take and do not take), an expert gather and the one-launch expert FFN.
+take and do not take, and a 6-vector call the tensor-core kernel takes by
+default), an expert gather and the one-launch expert FFN.
 
 Knobs documented as leaving the bits unchanged must give the default run's
-outputs bit for bit. The batched kernels that sum a row's blocks in another
-order ("stream", "mma", and one vector per warp, which sends batches of more
-than 4 vectors to "stream") are checked against the oracle within the DMMV
-tolerance, and must differ from the default somewhere (so the other kernel ran).
-The default run itself is checked against the oracle."""
+outputs bit for bit. The knobs that choose a batched kernel summing a row's
+blocks in another order than the default's ("stream", "mma", one vector per
+warp, which sends batches of more than 4 vectors to "stream", and "vsplit" and
+"slots", which take the 6-vector call off the tensor cores) are checked against
+the oracle within the DMMV tolerance, and must differ from the default somewhere
+(so the other kernel ran). The default run itself is checked against the oracle."""
 import os
 import subprocess
 import sys
@@ -37,9 +39,11 @@ DENSE_CASES = {
     "q4_2048_b5_repacked": (Q4, 777, 2048, 5, REPACKED, False),
     "q8_1280_b3": (Q8, 300, 1280, 3, GGUF, False),
     "q8_4096_b4_fused": (Q8, 1434, 4096, 4, GGUF, True),
+    # a 32-row group for each of the GB300's 152 SMs: the tensor-core kernel by default
+    "q8_4096_b6_tc": (Q8, 4900, 4096, 6, GGUF, False),
 }
-# batched calls over pre-quantized blocks: the only results "stream" and "mma" change
-REORDERED = {"q8_4096_b2", "q8_4096_b8", "q4_2048_b5_repacked", "q8_1280_b3"}
+# batched calls over pre-quantized blocks: the only results the batched-kernel knobs change
+REORDERED = {"q8_4096_b2", "q8_4096_b8", "q4_2048_b5_repacked", "q8_1280_b3", "q8_4096_b6_tc"}
 MOE = dict(hidden=2048, ffn=512, slots=12, sel=[7, 0, 11, 3, 5, 9, 2, 10, 1])
 
 _CHILD = r"""
@@ -143,8 +147,6 @@ SAME_BITS = [
     {"ZDMMV_STAGE_KB": "48"},
     {"ZDMMV_CTAS_PER_SM": "1"},
     {"ZDMMV_CTAS_PER_SM": "4"},
-    {"ZDMMV_BATCH_KERNEL": "slots"},
-    {"ZDMMV_BATCH_SLOTS": "1"},
     {"ZDMMV_BATCH_CTAS_PER_SM": "1"},
     {"ZDMMV_BATCH_CTAS_PER_SM": "4"},
     {"ZDMMV_FFN_STAGES": "3"},
@@ -163,10 +165,11 @@ def test_knob_keeps_the_bits(env, inputs, default_run, tmp_path):
 
 REORDERING = [
     {"ZDMMV_BATCH_KERNEL": "stream"},
-    {"ZDMMV_VSPLIT_V": "1"},          # more than 4 vectors: the "stream" kernel
+    {"ZDMMV_VSPLIT_V": "1"},          # more than 4 vectors off the tensor cores: the "stream" kernel
     {"ZDMMV_BATCH_KERNEL": "mma"},
-    {"ZDMMV_BATCH_KERNEL": "mma", "ZDMMV_MMA_WARPS": "16"},
-    {"ZDMMV_BATCH_KERNEL": "mma", "ZDMMV_MMA_STAGES": "2"},
+    {"ZDMMV_BATCH_KERNEL": "vsplit"},  # the 6-vector call: the single-vector order
+    {"ZDMMV_BATCH_KERNEL": "slots"},
+    {"ZDMMV_BATCH_SLOTS": "1"},
 ]
 
 

@@ -78,7 +78,8 @@ import sys, numpy as np, torch
 sys.path.insert(0, {root!r})
 from gguf_block_quant_gb300 import synth
 from gguf_block_quant_gb300 import zdmmv as Z
-for fmt, rows, cols, batch in [(Z.Q8_0, 1434, 4096, 8), (Z.Q4_0, 901, 2048, 3)]:
+# the last shape is the tensor-core kernel's by default (a 32-row group per SM)
+for fmt, rows, cols, batch in [(Z.Q8_0, 1434, 4096, 8), (Z.Q4_0, 901, 2048, 3), (Z.Q8_0, 4900, 4096, 8)]:
     w = torch.from_numpy(synth.weight_blocks(fmt, rows, cols, seed=batch)).cuda()
     xq = Z.quantize_act_q8_0(torch.from_numpy(synth.activations(cols, seed=batch + 3, batch=batch)).cuda())
     yb = Z.dmmv_batched(fmt, w, rows, cols, xq, batch)
@@ -93,8 +94,9 @@ print("ok")
 
 def test_vector_split_kernel_equals_single_vector_calls_bitwise():
     """ZDMMV_BATCH_KERNEL=vsplit (read once per process, hence a child process)
-    names the default explicitly: each vector's output equals its single-vector
-    call bit for bit."""
+    keeps every batch on the vector split, also those the tensor-core kernel
+    takes by default: each vector's output equals its single-vector call bit for
+    bit."""
     env = dict(os.environ, ZDMMV_BATCH_KERNEL="vsplit")
     r = subprocess.run([sys.executable, "-c", _CHILD_VSPLIT.format(root=ROOT)], env=env, capture_output=True,
                        text=True, timeout=600)
