@@ -232,30 +232,37 @@ __device__ __forceinline__ void bm_block(const uint32_t (&a0)[4], const uint32_t
 
 // Pair P (blocks 2P, 2P + 1 of the warp's four) for this lane: rows g (rg, rgt)
 // and g + 8 (rh, rht), fb / tb: the fragment and table addresses of the warp's
-// first block for this lane.
+// first block for this lane. A stage loads both pairs' operands first, then
+// computes them.
+template <int FMT> struct BmPair {
+    XmRow<FMT> wg, wh;
+    uint4 f0, f1, t0, t1;
+};
 template <int FMT, int P>
-__device__ __forceinline__ void bm_pair(uint32_t rg, uint32_t rgt, uint32_t rh, uint32_t rht, uint32_t fb,
-                                        uint32_t tb, uint32_t sel, float (&acc)[4]) {
+__device__ __forceinline__ void bm_pair_load(BmPair<FMT> &d, uint32_t rg, uint32_t rgt, uint32_t rh, uint32_t rht,
+                                             uint32_t fb, uint32_t tb, uint32_t sel) {
     constexpr int kF = 2 * P * kBmFragBytes;
     constexpr int kT = 2 * P * kBmTableBytes;
-    XmRow<FMT> wg, wh;
-    wg.template load<P>(rg, rgt, sel);
-    wh.template load<P>(rh, rht, sel);
-    const uint4 f0 = ldsi128<kF>(fb);
-    const uint4 f1 = ldsi128<kF + kBmFragBytes>(fb);
-    const uint4 t0 = ldsi128<kT>(tb);
-    const uint4 t1 = ldsi128<kT + kBmTableBytes>(tb);
+    d.wg.template load<P>(rg, rgt, sel);
+    d.wh.template load<P>(rh, rht, sel);
+    d.f0 = ldsi128<kF>(fb);
+    d.f1 = ldsi128<kF + kBmFragBytes>(fb);
+    d.t0 = ldsi128<kT>(tb);
+    d.t1 = ldsi128<kT + kBmTableBytes>(tb);
+}
+template <int FMT>
+__device__ __forceinline__ void bm_pair_compute(const BmPair<FMT> &d, float (&acc)[4]) {
     uint32_t a0[4], a1[4];
     if constexpr (FMT == kFmtQ4) {
-        BmFrags<kFmtQ4>::make(wg.ea, wh.ea, a0, a1);
-        bm_block(a0, a1, f0, t0, wg.d0, wh.d0, acc);
-        BmFrags<kFmtQ4>::make(wg.oa, wh.oa, a0, a1);
-        bm_block(a0, a1, f1, t1, wg.d1, wh.d1, acc);
+        BmFrags<kFmtQ4>::make(d.wg.ea, d.wh.ea, a0, a1);
+        bm_block(a0, a1, d.f0, d.t0, d.wg.d0, d.wh.d0, acc);
+        BmFrags<kFmtQ4>::make(d.wg.oa, d.wh.oa, a0, a1);
+        bm_block(a0, a1, d.f1, d.t1, d.wg.d1, d.wh.d1, acc);
     } else {
-        BmFrags<kFmtQ8>::make(wg.ea, wg.eb, wh.ea, wh.eb, a0, a1);
-        bm_block(a0, a1, f0, t0, wg.d0, wh.d0, acc);
-        BmFrags<kFmtQ8>::make(wg.oa, wg.ob, wh.oa, wh.ob, a0, a1);
-        bm_block(a0, a1, f1, t1, wg.d1, wh.d1, acc);
+        BmFrags<kFmtQ8>::make(d.wg.ea, d.wg.eb, d.wh.ea, d.wh.eb, a0, a1);
+        bm_block(a0, a1, d.f0, d.t0, d.wg.d0, d.wh.d0, acc);
+        BmFrags<kFmtQ8>::make(d.wg.oa, d.wg.ob, d.wh.oa, d.wh.ob, a0, a1);
+        bm_block(a0, a1, d.f1, d.t1, d.wg.d1, d.wh.d1, acc);
     }
 }
 
@@ -423,12 +430,17 @@ __global__ void __launch_bounds__((kBmWarps + 1) * 32, 1) dmmv_bmma_kernel(const
     int it = 0;
     for (int gi = 0; gi < my_groups; ++gi) {
         const int64_t r0 = (blockIdx.x + static_cast<int64_t>(gi) * gridDim.x) * kBmGroupRows;
+        // the warp's blocks 0, 1 of each chunk in acc, blocks 2, 3 in acc2 (two
+        // independent fma chains), added at the end of the group
         float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        float acc2[4] = {0.0f, 0.0f, 0.0f, 0.0f};
         for (int k = 0; k < a.nchunks; ++k, ++it) {
             const int s = it % STAGES;
-            // A timed-out wait marks the CTA aborted: the warps skip all further
-            // waits and work but keep meeting at the consumer barrier.
-            if (ok && __any_sync(0xffffffffu, *abort_flag != 0)) ok = false;
+            // A timed-out wait ends this warp's work (every later wait of the
+            // other warps is bounded too) and marks the CTA aborted, so no output
+            // is stored; the warp keeps meeting the others at the consumer barrier.
+            // (The flag is not polled per stage: that vote and shared load on every
+            // stage's critical path cost 0.2 us per launch.)
             if (ok) {
                 ok = __all_sync(0xffffffffu, mbar_wait(&full[s], static_cast<uint32_t>(it / STAGES) & 1u));
                 if (!ok) {
@@ -443,11 +455,16 @@ __global__ void __launch_bounds__((kBmWarps + 1) * 32, 1) dmmv_bmma_kernel(const
             const uint32_t rht = rh + static_cast<uint32_t>(4 * t);
             const uint32_t fb = fb0 + static_cast<uint32_t>(k * kBmChunkBlocks * kBmFragBytes);
             const uint32_t tb = tb0 + static_cast<uint32_t>(k * kBmChunkBlocks * kBmTableBytes);
-            bm_pair<FMT, 0>(rg, rgt, rh, rht, fb, tb, sel, acc);
-            bm_pair<FMT, 1>(rg, rgt, rh, rht, fb, tb, sel, acc);
+            BmPair<FMT> p0, p1;
+            bm_pair_load<FMT, 0>(p0, rg, rgt, rh, rht, fb, tb, sel);
+            bm_pair_load<FMT, 1>(p1, rg, rgt, rh, rht, fb, tb, sel);
+            bm_pair_compute<FMT>(p0, acc);
+            bm_pair_compute<FMT>(p1, acc2);
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[s]);
         }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) acc[q] = __fadd_rn(acc[q], acc2[q]);
         // the slab's 8 partial sums, added in part order: thread o < 256 takes
         // output (slab o / 128, vector (o % 128) / 16, row o % 16)
         const uint32_t rb = smem_addr(red) + static_cast<uint32_t>((a.red_bufs == 2 ? (gi & 1) : 0) * kBmRedBytes);
