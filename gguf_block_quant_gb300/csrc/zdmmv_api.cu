@@ -147,7 +147,7 @@ bool tma_shape_ok(int fmt, int64_t cols) {
     return nb % 8 == 0 && nb / 2 <= 128;
 }
 
-TmaPlan tma_plan(int fmt, int layout, int64_t cols, int halves) {
+TmaPlan tma_plan(int fmt, int layout, int64_t cols, int halves, int unit_max_bytes) {
     (void)layout;
     TmaPlan p{};
     const int nb = static_cast<int>(cols / kQK);
@@ -168,9 +168,11 @@ TmaPlan tma_plan(int fmt, int layout, int64_t cols, int halves) {
     // a pair stage (halves = 2) holds the same rows of two matrices
     const int stage_target = stage_target_bytes() / halves;
     // a tile is a whole number of passes of the row groups (kTmaRowsIlp rows each
-    // when that fits the stage target)
+    // when that fits the stage target, or unit_max_bytes where the caller allows
+    // more)
     int unit_rows = rows_par * kTmaRowsIlp;
-    if (unit_rows * row_bytes > stage_target) unit_rows = rows_par;
+    const int unit_cap = unit_max_bytes > stage_target ? unit_max_bytes : stage_target;
+    if (unit_rows * row_bytes > unit_cap) unit_rows = rows_par;
     const int unit = unit_rows * row_bytes;
     const int m = unit >= stage_target ? 1 : stage_target / unit;
     p.tile_rows = unit_rows * m;
@@ -638,7 +640,7 @@ zdmmv_status run_dmmv(int fmt, int layout, DmmvArgs a, int slots, cudaStream_t s
     if (a.rows == 0 || slots == 0) return ZDMMV_OK;
     const int64_t cols = static_cast<int64_t>(a.nb) * kQK;
     if (tma_shape_ok(fmt, cols) && a.batch == 1) {
-        const TmaPlan p = tma_plan(fmt, layout, cols);
+        const TmaPlan p = tma_plan(fmt, layout, cols, 1, kTmaWholeUnitMaxBytes);
         a.tile_rows = p.tile_rows;
         a.stage_bytes = p.stage_bytes;
         a.x_bytes_padded = p.x_bytes_padded;
@@ -838,7 +840,7 @@ cudaError_t launch_argmax_dmmv(int fmt, int layout, const void *w, int64_t rows,
     a.batch = 1;
     a.fault = dev->fault;
     a.argmax_parts = parts;
-    const TmaPlan p = tma_plan(fmt, layout, cols);
+    const TmaPlan p = tma_plan(fmt, layout, cols, 1, kTmaWholeUnitMaxBytes);
     a.tile_rows = p.tile_rows;
     a.stage_bytes = p.stage_bytes;
     a.x_bytes_padded = p.x_bytes_padded;
@@ -881,7 +883,7 @@ zdmmv_status acc_entry(int fmt, const void *w, int layout, int64_t rows, int64_t
     a.accumulate = 1;
     a.fault = dev->fault;
     if (!tma_shape_ok(fmt, cols)) return from_cuda(launch_plain(fmt, layout, a, 1, st));
-    const TmaPlan p = tma_plan(fmt, layout, cols);
+    const TmaPlan p = tma_plan(fmt, layout, cols, 1, kTmaWholeUnitMaxBytes);
     a.tile_rows = p.tile_rows;
     a.stage_bytes = p.stage_bytes;
     a.x_bytes_padded = p.x_bytes_padded;

@@ -86,7 +86,12 @@ inline cudaError_t raise_dynamic_smem_limit(const void *fn, int dev) {
 
 // Whether the pipelined kernel takes this shape, and its plan.
 bool tma_shape_ok(int fmt, int64_t cols);
-TmaPlan tma_plan(int fmt, int layout, int64_t cols, int halves = 1);
+// unit_max_bytes: a tile of one pass of every row group with kTmaRowsIlp rows in
+// flight is kept up to this size even above the stage target (single-vector
+// launches: Q8_0 14336 x 4096 10.46 -> 10.0 us with 8-row tiles of 34.8 KB
+// instead of 4-row ones; the vector split is slower with the larger tiles).
+constexpr int kTmaWholeUnitMaxBytes = 40 * 1024;
+TmaPlan tma_plan(int fmt, int layout, int64_t cols, int halves = 1, int unit_max_bytes = 0);
 
 // Launchers of the pipelined kernel (one translation unit per format).
 // fused_x: the kernel quantizes the fp32 activation a.xf itself (no a.xq).
