@@ -458,10 +458,15 @@ __global__ void __launch_bounds__((kBmWarps + 1) * 32, 1) dmmv_bmma_kernel(const
             BmPair<FMT> p0, p1;
             bm_pair_load<FMT, 0>(p0, rg, rgt, rh, rht, fb, tb, sel);
             bm_pair_load<FMT, 1>(p1, rg, rgt, rh, rht, fb, tb, sel);
-            bm_pair_compute<FMT>(p0, acc);
-            bm_pair_compute<FMT>(p1, acc2);
+            // The warp's bytes of the stage are in registers now: the stage is
+            // released before the arithmetic (the arrival's release semantics
+            // order the warp's shared loads before it, and the producer fences
+            // the async proxy before it copies into the stage again), so it is
+            // held for the loads only and the ring keeps more copies in flight.
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[s]);
+            bm_pair_compute<FMT>(p0, acc);
+            bm_pair_compute<FMT>(p1, acc2);
         }
 #pragma unroll
         for (int q = 0; q < 4; ++q) acc[q] = __fadd_rn(acc[q], acc2[q]);
