@@ -712,7 +712,7 @@ zdmmv_status dmmv_entry(int fmt, const void *w, zdmmv_layout layout, int64_t row
             m.nchunks = hp.nchunks;
             m.pitch = hp.pitch;
             m.red_bufs = hp.red_bufs;
-            return from_cuda(launch_bmma(fmt, m, hp, st, pdl_enabled()));
+            return from_cuda(launch_bmma(fmt, m, hp, false, st, pdl_enabled()));
         }
     }
     if (batch >= 2 && (choice == kBatchAuto || choice == kBatchMma || choice == kBatchVsplit) &&
@@ -1018,8 +1018,31 @@ zdmmv_status dmmv_f32_entry(int fmt, const void *w, int layout, int64_t rows, in
     a.nb = static_cast<int32_t>(cols / kQK);
     TmaPlan vp{};
     int vv = 0, nvg = 0;
-    if (batch >= 2 && !batch_slots_forced() &&
-        (batch_kernel_choice() == kBatchAuto || batch_kernel_choice() == kBatchVsplit) &&
+    const int choice = batch_slots_forced() ? kBatchSlots : batch_kernel_choice();
+    BmmaPlan hp{};
+    if (batch >= 2 && (choice == kBatchMma || (choice == kBatchAuto && batch >= kBmmaMinBatch)) &&
+        bmma_plan(fmt, layout, rows, cols, batch, &hp)) {
+        // the batched call's tensor-core kernel with the quantization in its
+        // prologue: the bits of the quantizer followed by zdmmv_q{8,4}_0_batched
+        const DeviceInfo *dev = nullptr;
+        if (device_info(&dev) != cudaSuccess) return ZDMMV_ERR_CUDA;
+        if (choice == kBatchMma || (rows + kBmGroupRows - 1) / kBmGroupRows >= dev->sms) {
+            BmmaArgs m{};
+            m.w = a.w;
+            m.xf = x;
+            m.y = y;
+            m.fault = dev->fault;
+            m.rows = rows;
+            m.y_stride = rows;
+            m.nb = a.nb;
+            m.batch = batch;
+            m.nchunks = hp.nchunks;
+            m.pitch = hp.pitch;
+            m.red_bufs = hp.red_bufs;
+            return from_cuda(launch_bmma(fmt, m, hp, true, st, pdl_enabled()));
+        }
+    }
+    if (batch >= 2 && (choice == kBatchAuto || choice == kBatchVsplit) &&
         vsplit_plan(fmt, layout, cols, batch, &vp, &vv, &nvg)) {
         // one weight stream for the batch, its activations quantized in the prologue
         const DeviceInfo *dev = nullptr;

@@ -54,14 +54,14 @@ bool bmma_plan(int fmt, int layout, int64_t rows, int64_t cols, int batch, BmmaP
     return true;
 }
 
-template <int FMT>
+template <int FMT, bool FX>
 cudaError_t launch_bmma_fmt(const BmmaArgs &a, const BmmaPlan &p, cudaStream_t st, bool pdl) {
     CUtensorMap map;
     const cudaError_t e = weight_map(a.w, a.rows, static_cast<int64_t>(a.nb) * Fmt<FMT>::kBlockBytes, p.pitch,
                                      kBmGroupRows, &map);
     if (e != cudaSuccess) return e;
 #define ZDMMV_BM(S_) \
-    if (p.stages == S_) return BmmaInst<FMT, S_>::launch(a, map, p.smem_bytes, st, pdl);
+    if (p.stages == S_) return BmmaInst<FMT, S_, FX>::launch(a, map, p.smem_bytes, st, pdl);
     ZDMMV_BM(2)
     ZDMMV_BM(3)
     ZDMMV_BM(4)
@@ -71,8 +71,10 @@ cudaError_t launch_bmma_fmt(const BmmaArgs &a, const BmmaPlan &p, cudaStream_t s
     return cudaErrorInvalidConfiguration;
 }
 
-cudaError_t launch_bmma(int fmt, const BmmaArgs &a, const BmmaPlan &p, cudaStream_t st, bool pdl) {
-    return fmt == kFmtQ8 ? launch_bmma_fmt<kFmtQ8>(a, p, st, pdl) : launch_bmma_fmt<kFmtQ4>(a, p, st, pdl);
+cudaError_t launch_bmma(int fmt, const BmmaArgs &a, const BmmaPlan &p, bool fused_x, cudaStream_t st, bool pdl) {
+    if (fused_x)
+        return fmt == kFmtQ8 ? launch_bmma_fmt<kFmtQ8, true>(a, p, st, pdl) : launch_bmma_fmt<kFmtQ4, true>(a, p, st, pdl);
+    return fmt == kFmtQ8 ? launch_bmma_fmt<kFmtQ8, false>(a, p, st, pdl) : launch_bmma_fmt<kFmtQ4, false>(a, p, st, pdl);
 }
 
 }  // namespace zdmmv

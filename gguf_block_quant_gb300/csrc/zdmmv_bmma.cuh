@@ -48,6 +48,7 @@ namespace zdmmv {
 struct BmmaArgs {
     const uint8_t *w;    // GGUF rows
     const uint8_t *xq;   // Q8_0 activation of vector 0; vector v at xq + v * xq_stride
+    const float *xf;     // FX: fp32 activations [batch][nb * 32], quantized by the kernel
     float *y;            // output of vector 0; vector v at y + v * y_stride
     uint32_t *fault;     // device fault word
     int64_t rows;
@@ -274,7 +275,11 @@ __device__ __forceinline__ void bm_consumer_barrier() {
 // 32-row groups c, c + gridDim.x, ..., each in a.nchunks stages of kBmChunkBlocks
 // blocks per row. wmap: the weight rows as a 2D tensor of 8-byte elements, box
 // {a.pitch / 8, kBmGroupRows}.
-template <int FMT, int STAGES>
+// FX = true: the consumers quantize the fp32 activations (a.xf) into the staged
+// Q8_0 blocks themselves, with the stand-alone quantizer's arithmetic
+// (quantize_quads_to_smem), so the results are the bits of the quantizer followed
+// by the FX = false kernel.
+template <int FMT, int STAGES, bool FX>
 __global__ void __launch_bounds__((kBmWarps + 1) * 32, 1) dmmv_bmma_kernel(const BmmaArgs a,
                                                                           const __grid_constant__ CUtensorMap wmap) {
     constexpr int kBB = Fmt<FMT>::kBlockBytes;
@@ -284,6 +289,7 @@ __global__ void __launch_bounds__((kBmWarps + 1) * 32, 1) dmmv_bmma_kernel(const
     uint64_t *full = reinterpret_cast<uint64_t *>(smem);
     uint64_t *empty = full + STAGES;
     uint64_t *xbar = empty + STAGES;  // the staged activation has landed
+    uint64_t *xready = xbar + 1;      // FX: the activation is quantized (its loads are done)
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kBarrierBytes - 8);
     const int nb_pad = a.nchunks * kBmChunkBlocks;
     uint8_t *frag = smem + kBarrierBytes;
@@ -296,9 +302,10 @@ __global__ void __launch_bounds__((kBmWarps + 1) * 32, 1) dmmv_bmma_kernel(const
     // consumer loads its share into registers, and after a barrier the fragments
     // overwrite it, so the whole ring is free for weights from the start. Vector v
     // at xs + v * x_pitch: a Q8_0 row plus 16 bytes (4 mod 32 words), so the 8
-    // vectors' words of one block fall in distinct banks.
+    // vectors' words of one block fall in distinct banks (FX: the quantizer writes
+    // the rows back to back).
     const int x_row = a.nb * 34;
-    const int x_pitch = x_row + 16;
+    const int x_pitch = FX ? x_row : x_row + 16;
     uint8_t *xs = frag + (static_cast<size_t>(nb_pad) * kBmFragBytes - static_cast<size_t>(a.batch) * x_pitch);
 
     const int tid = threadIdx.x;
@@ -322,6 +329,7 @@ __global__ void __launch_bounds__((kBmWarps + 1) * 32, 1) dmmv_bmma_kernel(const
             mbar_init(&empty[s], kBmWarps);
         }
         mbar_init(xbar, 1);
+        mbar_init(xready, 1);
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -349,16 +357,22 @@ __global__ void __launch_bounds__((kBmWarps + 1) * 32, 1) dmmv_bmma_kernel(const
         const int nring = items < STAGES ? items : STAGES;
         issue(0);
         int issued = 1;
-        pdl_wait();  // the activations may be written by the preceding kernel
-        // one bulk copy per vector (whole Q8_0 rows: 16-byte multiples at 16-byte
-        // aligned addresses), all on xbar
-        mbar_arrive_expect_tx(xbar, static_cast<uint32_t>(a.batch * x_row));
-        for (int v = 0; v < a.batch; ++v)
-            bulk_copy_g2s(xs + static_cast<size_t>(v) * x_pitch, a.xq + static_cast<int64_t>(v) * a.xq_stride,
-                          static_cast<uint32_t>(x_row), xbar, l2_evict_last_policy());
-        for (; issued < nring; ++issued) issue(issued);
         bool ok = true;
-        for (int it = issued; it < items; ++it) {
+        if constexpr (FX) {
+            // the consumers' loads of the fp32 activation go out first too: the rest
+            // of the ring waits until they are done
+            ok = mbar_wait(xready, 0);
+        } else {
+            pdl_wait();  // the activations may be written by the preceding kernel
+            // one bulk copy per vector (whole Q8_0 rows: 16-byte multiples at 16-byte
+            // aligned addresses), all on xbar
+            mbar_arrive_expect_tx(xbar, static_cast<uint32_t>(a.batch * x_row));
+            for (int v = 0; v < a.batch; ++v)
+                bulk_copy_g2s(xs + static_cast<size_t>(v) * x_pitch, a.xq + static_cast<int64_t>(v) * a.xq_stride,
+                              static_cast<uint32_t>(x_row), xbar, l2_evict_last_policy());
+        }
+        for (; ok && issued < nring; ++issued) issue(issued);
+        for (int it = issued; ok && it < items; ++it) {
             const int s = it % STAGES;
             if (!mbar_wait(&empty[s], static_cast<uint32_t>((it / STAGES) - 1) & 1u)) {
                 ok = false;
@@ -374,7 +388,7 @@ __global__ void __launch_bounds__((kBmWarps + 1) * 32, 1) dmmv_bmma_kernel(const
             const int t_last = (issued - 1 - s) >= 0 ? ((issued - 1 - s) / STAGES) * STAGES + s : -1;
             if (t_last >= 0) (void)mbar_wait(&full[s], static_cast<uint32_t>(t_last / STAGES) & 1u);
         }
-        (void)mbar_wait(xbar, 0);
+        if constexpr (!FX) (void)mbar_wait(xbar, 0);
         return;
     }
 
@@ -384,13 +398,23 @@ __global__ void __launch_bounds__((kBmWarps + 1) * 32, 1) dmmv_bmma_kernel(const
     const int g = lane >> 2;
     const int t = lane & 3;
     const uint32_t sel = mma_even_sel(t);
-    pdl_wait();  // outputs may still be read by the preceding kernel
-    // A timed-out wait marks the CTA aborted: the warps skip all further waits
-    // and work but keep meeting at the consumer barrier.
-    bool ok = __all_sync(0xffffffffu, mbar_wait(xbar, 0));
-    if (!ok) {
-        if (lane == 0) atomicOr(a.fault, 1u);
-        *abort_flag = 1;
+    // the activations may be written, and outputs still read, by the preceding kernel
+    pdl_wait();
+    bool ok = true;
+    if constexpr (FX) {
+        // every vector's blocks back to back ([batch][nb] Q8_0 blocks); nb is a
+        // multiple of 8, so no quad of blocks straddles two vectors
+        quantize_quads_to_smem<kBmWarps>(a.xf, a.batch * (a.nb >> 2), xs, warp, lane);
+        bm_consumer_barrier();
+        if (tid == 0) mbar_arrive(xready);
+    } else {
+        // A timed-out wait marks the CTA aborted: the warps skip all further waits
+        // and work but keep meeting at the consumer barrier.
+        ok = __all_sync(0xffffffffu, mbar_wait(xbar, 0));
+        if (!ok) {
+            if (lane == 0) atomicOr(a.fault, 1u);
+            *abort_flag = 1;
+        }
     }
     // Fragments and table from the staged activation: the warp's blocks w, w +
     // kBmWarps, ... (at most kBmMaxBlocks / kBmWarps of them, the plan's limit),
@@ -494,9 +518,9 @@ __global__ void __launch_bounds__((kBmWarps + 1) * 32, 1) dmmv_bmma_kernel(const
     }
 }
 
-template <int FMT, int STAGES>
+template <int FMT, int STAGES, bool FX>
 struct BmmaInst {
-    static constexpr auto kKernel = &dmmv_bmma_kernel<FMT, STAGES>;
+    static constexpr auto kKernel = &dmmv_bmma_kernel<FMT, STAGES, FX>;
     // one CTA per SM (at most one per 32-row group)
     static cudaError_t launch(const BmmaArgs &a, const CUtensorMap &wmap, int smem_bytes, cudaStream_t st, bool pdl) {
         static std::atomic<bool> done[64];  // smem limit raised, per device

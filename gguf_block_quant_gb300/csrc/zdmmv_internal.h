@@ -168,7 +168,7 @@ struct BmmaPlan {
     int stages, smem_bytes;
 };
 bool bmma_plan(int fmt, int layout, int64_t rows, int64_t cols, int batch, BmmaPlan *out);
-cudaError_t launch_bmma(int fmt, const BmmaArgs &a, const BmmaPlan &p, cudaStream_t st, bool pdl);
+cudaError_t launch_bmma(int fmt, const BmmaArgs &a, const BmmaPlan &p, bool fused_x, cudaStream_t st, bool pdl);
 
 // The one-launch expert FFN (gate/up + SwiGLU, then down): workspace size,
 // shapes it takes, and the launcher (FfnArgs: zdmmv_ffn.cuh; the launcher fills

@@ -182,16 +182,19 @@ zdmmv_status zdmmv_q4_0_batched(const void *w, zdmmv_layout layout, int64_t rows
                                 int64_t cols, const void *xq, int batch, float *y,
                                 zdmmv_stream_t stream);
 
-/* Fused decode step: for each of the batch vectors the same result as
- * zdmmv_quantize_act_q8_0 followed by zdmmv_q{8,4}_0, bit for bit, in ONE launch. Each CTA quantizes the
- * fp32 activation to Q8_0 blocks in shared memory itself, so a chain of decode
- * layers pays one kernel per layer instead of two (per-token launch chains:
- * "RTX 5090: Batched Prefill & CUDA Graphs in ZINC", "CUDA graphs -- the
- * structural answer to launch latency").
+/* Fused decode step: the same result as zdmmv_quantize_act_q8_0 followed by
+ * zdmmv_q{8,4}_0_batched (zdmmv_q{8,4}_0 for batch 1), bit for bit, in ONE
+ * launch. Each CTA quantizes the fp32 activation to Q8_0 blocks in shared memory
+ * itself, so a chain of decode layers pays one kernel per layer instead of two
+ * (per-token launch chains: "RTX 5090: Batched Prefill & CUDA Graphs in ZINC",
+ * "CUDA graphs -- the structural answer to launch latency"). So where the
+ * batched call is the single-vector computation per vector, so is this one;
+ * where it takes the tensor-core kernel (5..8 vectors, see
+ * zdmmv_q8_0_batched), this one does too.
  *   fmt    ZDMMV_Q8_0 or ZDMMV_Q4_0 weights; w, layout, rows, cols as zdmmv_q8_0.
  *   x      device fp32 [batch][cols], 16-byte aligned; batch 1..8.
  *   y      device fp32 [batch][rows].
- * Batches of 2..8 on the batched kernel's shapes stream the weights once (every
+ * Batches of 2..8 on the batched kernels' shapes stream the weights once (every
  * CTA quantizes the whole batch); other batches run one fused launch with a
  * slot per vector. For batches the two calls (zdmmv_quantize_act_q8_0, then
  * zdmmv_q{8,4}_0_batched) are faster: the quantization is done once instead of

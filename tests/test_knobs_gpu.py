@@ -42,8 +42,9 @@ DENSE_CASES = {
     # a 32-row group for each of the GB300's 152 SMs: the tensor-core kernel by default
     "q8_4096_b6_tc": (Q8, 4900, 4096, 6, GGUF, False),
 }
-# batched calls over pre-quantized blocks: the only results the batched-kernel knobs change
-REORDERED = {"q8_4096_b2", "q8_4096_b8", "q4_2048_b5_repacked", "q8_1280_b3", "q8_4096_b6_tc"}
+# the batched calls (and, under "mma", the fused batched one): the only results the
+# batched-kernel knobs change
+REORDERED = {"q8_4096_b2", "q8_4096_b8", "q4_2048_b5_repacked", "q8_1280_b3", "q8_4096_b6_tc", "q8_4096_b4_fused"}
 MOE = dict(hidden=2048, ffn=512, slots=12, sel=[7, 0, 11, 3, 5, 9, 2, 10, 1])
 
 _CHILD = r"""
@@ -182,7 +183,8 @@ def test_other_batched_kernel_within_tolerance(env, inputs, default_run, tmp_pat
         if name not in REORDERED:
             assert np.array_equal(out[name], default_run[name]), name
             continue
-        y_ref, e_ref = oracle.dmmv_batched(fmt, arrs[name + ":w"], rows, cols, arrs[name + ":xq"], batch)
+        xq = oracle.quantize_q8_0(arrs[name + ":x"]) if fused else arrs[name + ":xq"]
+        y_ref, e_ref = oracle.dmmv_batched(fmt, arrs[name + ":w"], rows, cols, xq, batch)
         ok, worst = oracle.within_tolerance(out[name].reshape(batch, rows), y_ref, e_ref)
         assert ok, (name, worst)
         differs |= not np.array_equal(out[name], default_run[name])

@@ -6,7 +6,9 @@ a child process): results against the oracle on ragged and chunked shapes for
 and that the tensor-core kernel is the one that ran (its results are not bitwise
 the single-vector calls', as the vector split's are). In the default process:
 the kernel is chosen for 5..8 vectors on matrices with a 32-row group for every
-SM, and the vector split (bitwise the single-vector calls) below that."""
+SM, and the vector split (bitwise the single-vector calls) below that; the fused
+entry point (fp32 activations) then gives the bits of the quantizer followed by
+the batched call."""
 import os
 import subprocess
 import sys
@@ -69,6 +71,16 @@ for fmt in (Q8, Q4):
             y_ref, _ = oracle.dmmv_batched(fmt, w, rows, cols, xq, batch)
             assert np.array_equal(y.double().cpu().numpy().reshape(batch, rows), y_ref), (fmt, cols, batch)
             checked += 1
+# the fused entry point takes the same kernel with the quantization in its
+# prologue: the bits of the quantizer followed by the batched call
+for fmt, rows, cols, batch in [(Q8, 300, 2304, 2), (Q4, 65, 4096, 3), (Q8, 1434, 1280, 8)]:
+    w = torch.from_numpy(synth.weight_blocks(fmt, rows, cols, seed=rows)).cuda()
+    x = torch.from_numpy(synth.activations(cols, seed=cols + batch, batch=batch)).cuda()
+    yf = Z.dmmv_f32(fmt, w, rows, cols, x, batch=batch)
+    yb = Z.dmmv_batched(fmt, w, rows, cols, Z.quantize_act_q8_0(x.reshape(-1)), batch)
+    torch.cuda.synchronize()
+    assert torch.equal(yf.reshape(batch, rows), yb.reshape(batch, rows)), (fmt, rows, cols, batch)
+    checked += 1
 # the launch is the tensor-core kernel: the vector split gives every vector's
 # single-vector result bit for bit; the tensor-core kernel sums the blocks of a
 # row in another order, so some output bits differ
@@ -88,7 +100,7 @@ def test_tensor_core_batched_kernel():
     r = subprocess.run([sys.executable, "-c", _CHILD.format(root=ROOT)], env=env, capture_output=True, text=True,
                        timeout=900)
     assert r.returncode == 0, r.stderr[-3000:]
-    assert r.stdout.strip().splitlines()[-1] == "ok 36"
+    assert r.stdout.strip().splitlines()[-1] == "ok 39"
 
 
 def _rows_for_every_sm(extra):
@@ -128,3 +140,26 @@ def test_default_smaller_batches_and_matrices_keep_the_vector_split(fmt, extra, 
     bitwise the single-vector calls."""
     y, ys = _batched_and_singles(fmt, _rows_for_every_sm(extra), cols, batch, seed=extra + cols + 1)
     assert torch.equal(y, ys)
+
+
+@pytest.mark.parametrize("fmt,extra,cols,batch", [(synth.Q8_0, 37, 4096, 5), (synth.Q8_0, 0, 4096, 8),
+                                                  (synth.Q4_0, 129, 2304, 6), (synth.Q4_0, 5, 1280, 7),
+                                                  (synth.Q8_0, 37, 4096, 4)])
+def test_fused_entry_equals_quantize_then_batched(fmt, extra, cols, batch):
+    """zdmmv_dmmv_f32 with 4..8 vectors: bit for bit the quantizer followed by the
+    batched call (the tensor-core kernel from 5 vectors on these shapes, the
+    vector split at 4), and within the oracle's tolerance."""
+    rows = _rows_for_every_sm(extra)
+    w = synth.weight_blocks(fmt, rows, cols, seed=extra + 3)
+    x = synth.activations(cols, seed=extra + 4, batch=batch)
+    wd = torch.from_numpy(w).cuda()
+    xd = torch.from_numpy(x).cuda()
+    yf = torch.full((batch, rows), float("nan"), device="cuda")
+    Z.dmmv_f32(fmt, wd, rows, cols, xd, batch=batch, y=yf)
+    yb = torch.full((batch, rows), float("nan"), device="cuda")
+    Z.dmmv_batched(fmt, wd, rows, cols, Z.quantize_act_q8_0(xd.reshape(-1)), batch, y=yb)
+    torch.cuda.synchronize()
+    assert torch.equal(yf, yb)
+    y_ref, e_ref = oracle.dmmv_batched(fmt, w, rows, cols, oracle.quantize_q8_0(x), batch)
+    ok, worst = oracle.within_tolerance(yf.double().cpu().numpy(), y_ref, e_ref)
+    assert ok, worst
