@@ -146,29 +146,7 @@ cudaError_t launch_xf32_q4(const DmmvArgs &a, const TmaPlan &p, int layout, int 
                            cudaStream_t st, bool pdl);
 cudaError_t launch_xf32_plain_q8(const DmmvArgs &a, int layout, int sms, int slots, cudaStream_t st, bool pdl);
 cudaError_t launch_xf32_plain_q4(const DmmvArgs &a, int layout, int sms, int slots, cudaStream_t st, bool pdl);
-// The same product on the fp16 tensor cores (GGUF rows of 256-column multiples,
-// at least 128 rows): plan (false when it does not take the shape) and launcher
-// (Xf32MmaArgs: zdmmv_xf32_mma.cuh).
-struct Xf32MmaArgs;
-struct Xf32MmaPlan {
-    int cb, nchunks, pitch;  // blocks per stage row, stages per row group, staged row pitch (bytes)
-    int stages, smem_bytes;
-};
-bool xf32_mma_plan(int fmt, int layout, int64_t rows, int64_t cols, Xf32MmaPlan *out);
-cudaError_t launch_xf32_mma(int fmt, const Xf32MmaArgs &a, const Xf32MmaPlan &p, int slots, cudaStream_t st,
-                            bool pdl);
-
-// The batched DMMV (1..8 Q8_0 vectors, GGUF rows of 256-column multiples) on
-// the fp16 tensor cores: plan (false when it does not take the shape) and
-// launcher (BmmaArgs: zdmmv_bmma.cuh).
-struct BmmaArgs;
-struct BmmaPlan {
-    int nchunks, pitch;   // stages per 32-row group, staged row pitch (bytes)
-    int red_bufs;         // buffers of warp partial sums (1 or 2)
-    int stages, smem_bytes;
-};
-bool bmma_plan(int fmt, int layout, int64_t rows, int64_t cols, int batch, BmmaPlan *out);
-cudaError_t launch_bmma(int fmt, const BmmaArgs &a, const BmmaPlan &p, bool fused_x, cudaStream_t st, bool pdl);
+// The tensor-core kernels' plans and launchers: zdmmv_mma.h.
 
 // The one-launch expert FFN (gate/up + SwiGLU, then down): workspace size,
 // shapes it takes, and the launcher (FfnArgs: zdmmv_ffn.cuh; the launcher fills
