@@ -122,17 +122,20 @@ __global__ void __launch_bounds__(kTmaThreads, 3) dmmv_vsplit_kernel(const DmmvA
         // ------------------------------------------------------- producer
         if (tid != kConsumerThreads) return;
         const uint64_t wpol = l2_evict_first_policy();
-        const int npre = ntiles < STAGES ? ntiles : STAGES;
-        for (int t = 0; t < npre; ++t) issue_tile<FMT, LAYOUT>(a, a.w, r0, r1, t, t, stage0, full, wpol);
-        int issued = npre;
+        // one tile before the dependency wait, then the activation copy, then the
+        // rest of the ring (this CTA's copies are served in issue order)
+        const int nring = ntiles < STAGES ? ntiles : STAGES;
+        issue_tile<FMT, LAYOUT>(a, a.w, r0, r1, 0, 0, stage0, full, wpol);
+        int issued = 1;
         pdl_wait();  // the activations may be written by the preceding kernel
         if constexpr (!FX) {
             const uint32_t xbytes = static_cast<uint32_t>(a.batch) * static_cast<uint32_t>(nb) * 34u;
             mbar_arrive_expect_tx(xbar, xbytes);
             bulk_copy_g2s(xs, a.xq, xbytes, xbar, l2_evict_last_policy());
         }
+        for (; issued < nring; ++issued) issue_tile<FMT, LAYOUT>(a, a.w, r0, r1, issued, issued, stage0, full, wpol);
         bool ok = true;
-        for (int t = npre; t < ntiles; ++t) {
+        for (int t = issued; t < ntiles; ++t) {
             const int s = t % STAGES;
             if (!mbar_wait(&empty[s], static_cast<uint32_t>((t / STAGES) - 1) & 1u)) {
                 ok = false;
