@@ -113,6 +113,7 @@ __global__ void __launch_bounds__(kTmaThreads, 3) dmmv_xf32_kernel(const DmmvArg
     extern __shared__ __align__(128) uint8_t smem[];
     uint64_t *full = reinterpret_cast<uint64_t *>(smem);
     uint64_t *empty = full + STAGES;
+    uint64_t *xready = empty + STAGES;  // the consumers have staged the activation
     uint8_t *xs = smem + kBarrierBytes;
     uint8_t *stage0 = xs + a.x_bytes_padded;
 
@@ -136,6 +137,7 @@ __global__ void __launch_bounds__(kTmaThreads, 3) dmmv_xf32_kernel(const DmmvArg
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], kConsumerThreads / 32);
         }
+        mbar_init(xready, 1);
         fence_barrier_init();
     }
     __syncthreads();
@@ -144,11 +146,15 @@ __global__ void __launch_bounds__(kTmaThreads, 3) dmmv_xf32_kernel(const DmmvArg
         // ------------------------------------------------------- producer
         if (tid != kConsumerThreads) return;
         const uint64_t wpol = l2_evict_first_policy();
-        const int npre = ntiles < STAGES ? ntiles : STAGES;
-        for (int t = 0; t < npre; ++t) issue_tile<FMT, LAYOUT>(a, a.w, r0, r1, t, t, stage0, full, wpol);
-        int issued = npre;
-        bool ok = true;
-        for (int t = npre; t < ntiles; ++t) {
+        // One tile streams before the consumers' activation loads, the rest of the
+        // ring once the activation is staged: loads issued behind the whole ring
+        // of this CTA's weight copies would wait for all of them.
+        const int nring = ntiles < STAGES ? ntiles : STAGES;
+        issue_tile<FMT, LAYOUT>(a, a.w, r0, r1, 0, 0, stage0, full, wpol);
+        int issued = 1;
+        bool ok = mbar_wait(xready, 0);
+        for (; ok && issued < nring; ++issued) issue_tile<FMT, LAYOUT>(a, a.w, r0, r1, issued, issued, stage0, full, wpol);
+        for (int t = issued; ok && t < ntiles; ++t) {
             const int s = t % STAGES;
             if (!mbar_wait(&empty[s], static_cast<uint32_t>((t / STAGES) - 1) & 1u)) {
                 ok = false;
@@ -179,6 +185,7 @@ __global__ void __launch_bounds__(kTmaThreads, 3) dmmv_xf32_kernel(const DmmvArg
             sts128(xsa + static_cast<uint32_t>((q >> 3) * kXf32BlockStride + (q & 7) * 16), x4[q]);
     }
     consumer_barrier();
+    if (tid == 0) mbar_arrive(xready);
     const int bpl = nb / LPR;  // nb is a multiple of LPR on this path
 
     for (int t = 0; t < ntiles; ++t) {

@@ -318,6 +318,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, 2) dmmv_xf32_mma_kernel(const X
     extern __shared__ __align__(128) uint8_t smem[];
     uint64_t *full = reinterpret_cast<uint64_t *>(smem);
     uint64_t *empty = full + STAGES;
+    uint64_t *xready = empty + STAGES;  // the consumers have built the activation fragments
     uint8_t *frag = smem + kBarrierBytes;
     uint8_t *stage0 = frag + static_cast<size_t>(a.nb) * kXmFragBytes;
     const int stage_bytes = kGroupRows * a.pitch;
@@ -345,6 +346,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, 2) dmmv_xf32_mma_kernel(const X
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], NW);
         }
+        mbar_init(xready, 1);
         fence_barrier_init();
     }
     __syncthreads();
@@ -362,12 +364,16 @@ __global__ void __launch_bounds__((NW + 1) * 32, 2) dmmv_xf32_mma_kernel(const X
             tensor_copy_2d(stage0 + static_cast<size_t>(s) * stage_bytes, &wmap, k * a.cb * kBB / 8,
                            static_cast<int>(group * kGroupRows), &full[s], wpol);
         };
-        // weights are read-only parameters: the first stages stream before the dependency wait
-        const int npre = items < STAGES ? items : STAGES;
-        for (int it = 0; it < npre; ++it) issue(it);
-        int issued = npre;
-        bool ok = true;
-        for (int it = npre; it < items; ++it) {
+        // Weights are read-only parameters: one stage streams before the
+        // consumers' activation loads, the rest of the ring once the fragments are
+        // built (loads issued behind the whole ring of this CTA's weight copies
+        // would wait for all of them).
+        const int nring = items < STAGES ? items : STAGES;
+        issue(0);
+        int issued = 1;
+        bool ok = mbar_wait(xready, 0);
+        for (; ok && issued < nring; ++issued) issue(issued);
+        for (int it = issued; ok && it < items; ++it) {
             const int s = it % STAGES;
             if (!mbar_wait(&empty[s], static_cast<uint32_t>((it / STAGES) - 1) & 1u)) {
                 ok = false;
@@ -408,6 +414,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, 2) dmmv_xf32_mma_kernel(const X
         }
     }
     mma_consumer_barrier<NW>();
+    if (tid == 0) mbar_arrive(xready);
 
     // lanes of quads 0..2 hold activation parts 0..2; the others load 16 zero bytes
     const uint32_t frag_l = smem_addr(frag) + static_cast<uint32_t>(g < 3 ? lane * 16 : kXmZeroOfs);
