@@ -148,16 +148,22 @@ __global__ void __launch_bounds__(kTmaThreads, 3) moe_ffn_kernel(const FfnArgs f
             else
                 issue_tile<FDN, kLayoutGguf>(a, w, r0, r1, t, s, stage0, full, wpol);
         };
-        const int npre = ntiles < STAGES ? ntiles : STAGES;
-        for (int t = 0; t < npre; ++t) issue(t, t);
+        // gate/up CTAs: one tile, the activation copy, then the rest of the ring
+        // (this CTA's copies are served in issue order and no tile can be used
+        // before the activation); down CTAs: the whole ring (their activation, h,
+        // comes later from the gate/up CTAs)
+        const int nring = ntiles < STAGES ? ntiles : STAGES;
+        int issued = 0;
         if (gu) {
+            issue(0, 0);
+            issued = 1;
             const uint32_t xbytes = static_cast<uint32_t>(nb) * 34u;
             mbar_arrive_expect_tx(xbar, xbytes);
             bulk_copy_g2s(xs, f.xq, xbytes, xbar, l2_evict_last_policy());
         }
-        int issued = npre;
+        for (; issued < nring; ++issued) issue(issued, issued);
         bool ok = true;
-        for (int t = npre; t < ntiles; ++t) {
+        for (int t = issued; t < ntiles; ++t) {
             const int s = t % STAGES;
             if (!mbar_wait(&empty[s], static_cast<uint32_t>((t / STAGES) - 1) & 1u)) {
                 ok = false;
