@@ -236,6 +236,67 @@ __device__ __forceinline__ uint32_t quantize_q8_0_quad(float4 v, unsigned short 
     return q0 | (q1 << 8) | (q2 << 16) | (q3 << 24);
 }
 
+// One round of quantize_quads_to_smem: the loads of kRound quads of the warp
+// (quads q0, q0 + kWarps, ...; zeros past nquads, no access).
+template <int kWarps, int kRound>
+__device__ __forceinline__ void quantize_round_load(const float *xf, int nquads, int q0, int sub, int j,
+                                                    float4 (&v)[kRound]) {
+#pragma unroll
+    for (int u = 0; u < kRound; ++u) {
+        const int qd = q0 + u * kWarps;
+        v[u] = qd < nquads ? *reinterpret_cast<const float4 *>(xf + static_cast<int64_t>(4 * qd + sub) * kQK + 4 * j)
+                           : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+}
+
+// The rest of a round: block maxima, scales and codes, stored into xs.
+template <int kWarps, int kRound>
+__device__ __forceinline__ void quantize_round_store(const float4 (&v)[kRound], int nquads, int q0, uint8_t *xs,
+                                                     int lane, int sub, int j) {
+    float m[kRound];
+#pragma unroll
+    for (int u = 0; u < kRound; ++u)
+        m[u] = fmaxf(fmaxf(fabsf(v[u].x), fabsf(v[u].y)), fmaxf(fabsf(v[u].z), fabsf(v[u].w)));
+#pragma unroll
+    for (int o = 1; o < 8; o <<= 1) {
+#pragma unroll
+        for (int u = 0; u < kRound; ++u) m[u] = fmaxf(m[u], __shfl_xor_sync(0xffffffffu, m[u], o));
+    }
+    // the operations of quantize_q8_0_lane (IEEE division and reciprocal),
+    // once per block: lane j of the 8 sharing a block takes round j's block
+    // and the results are broadcast to the other 7
+    static_assert(kRound == 8, "one round per lane of a block's 8 lanes");
+    float mj = m[0];
+#pragma unroll
+    for (int u = 1; u < kRound; ++u) mj = j == u ? m[u] : mj;
+    const float dj = __fdiv_rn(mj, 127.0f);
+    const float idj = dj != 0.0f ? __frcp_rn(dj) : 0.0f;
+    const uint32_t dbj = __half_as_ushort(__float2half_rn(dj));
+    float id[kRound];
+    unsigned short db[kRound];
+#pragma unroll
+    for (int u = 0; u < kRound; ++u) {
+        const int src = (lane & ~7) | u;
+        id[u] = __shfl_sync(0xffffffffu, idj, src);
+        db[u] = static_cast<unsigned short>(__shfl_sync(0xffffffffu, dbj, src));
+    }
+#pragma unroll
+    for (int u = 0; u < kRound; ++u) {
+        const int qd = q0 + u * kWarps;
+        if (qd < nquads) {  // warp-uniform
+            const uint32_t c0 = static_cast<uint8_t>(static_cast<int8_t>(static_cast<int>(roundf(__fmul_rn(v[u].x, id[u])))));
+            const uint32_t c1 = static_cast<uint8_t>(static_cast<int8_t>(static_cast<int>(roundf(__fmul_rn(v[u].y, id[u])))));
+            const uint32_t c2 = static_cast<uint8_t>(static_cast<int8_t>(static_cast<int>(roundf(__fmul_rn(v[u].z, id[u])))));
+            const uint32_t c3 = static_cast<uint8_t>(static_cast<int8_t>(static_cast<int>(roundf(__fmul_rn(v[u].w, id[u])))));
+            uint8_t *blk = xs + 34 * (4 * qd + sub);
+            uint16_t *dst = reinterpret_cast<uint16_t *>(blk + 2 + 4 * j);  // 2-byte aligned
+            dst[0] = static_cast<uint16_t>(c0 | (c1 << 8));
+            dst[1] = static_cast<uint16_t>(c2 | (c3 << 8));
+            if (j == 0) *reinterpret_cast<unsigned short *>(blk) = db[u];
+        }
+    }
+}
+
 // Quantize 4 * nquads consecutive Q8_0 blocks of the fp32 values at xf into
 // shared memory at xs (34 bytes per block), with the stand-alone quantizer's
 // arithmetic (quantize_q8_0_lane: fp32 amax, IEEE d = amax / 127 and 1 / d,
@@ -243,62 +304,34 @@ __device__ __forceinline__ uint32_t quantize_q8_0_quad(float4 v, unsigned short 
 // that quantizer's. The kWarps warps of the calling group (this one is `warp`)
 // each take four blocks per iteration (16-byte loads, 8 lanes per block),
 // kRound iterations at a time in phases (all loads, all block maxima, all
-// scales, all codes) so independent blocks overlap. The caller synchronizes the
-// group before the blocks are read.
-template <int kWarps, int kRound = 8>
+// scales, all codes) so independent blocks overlap. kAhead: each round's loads
+// are issued before the previous round is quantized, so a warp with several
+// rounds (batches of vectors) does not wait a whole load latency per round; it
+// costs kRound float4 registers. The vector-split kernel turns it on (Q8_0
+// 14336 x 4096, 2 / 4 vectors: 12.66 -> 12.32 / 15.69 -> 15.10 us per fused
+// launch); the tensor-core batched kernel measured slower with it (8 vectors:
+// 16.07 -> 16.38 us) and leaves it off, as do the single-vector callers (one
+// round per warp). The caller synchronizes the group before the blocks are read.
+template <int kWarps, int kRound = 8, bool kAhead = false>
 __device__ __forceinline__ void quantize_quads_to_smem(const float *xf, int nquads, uint8_t *xs, int warp,
                                                        int lane) {
     const int sub = lane >> 3;  // block within the quad
     const int j = lane & 7;     // 4-element group within the block
-    for (int q0 = warp; q0 < nquads; q0 += kWarps * kRound) {
-        float4 v[kRound];
-        float m[kRound];
+    constexpr int kStep = kWarps * kRound;
+    if constexpr (kAhead) {
+        float4 v[kRound], next[kRound];
+        quantize_round_load<kWarps, kRound>(xf, nquads, warp, sub, j, v);
+        for (int q0 = warp; q0 < nquads; q0 += kStep) {
+            quantize_round_load<kWarps, kRound>(xf, nquads, q0 + kStep, sub, j, next);
+            quantize_round_store<kWarps, kRound>(v, nquads, q0, xs, lane, sub, j);
 #pragma unroll
-        for (int u = 0; u < kRound; ++u) {
-            const int qd = q0 + u * kWarps;
-            v[u] = qd < nquads ? *reinterpret_cast<const float4 *>(xf + static_cast<int64_t>(4 * qd + sub) * kQK + 4 * j)
-                               : make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int u = 0; u < kRound; ++u) v[u] = next[u];
         }
-#pragma unroll
-        for (int u = 0; u < kRound; ++u)
-            m[u] = fmaxf(fmaxf(fabsf(v[u].x), fabsf(v[u].y)), fmaxf(fabsf(v[u].z), fabsf(v[u].w)));
-#pragma unroll
-        for (int o = 1; o < 8; o <<= 1) {
-#pragma unroll
-            for (int u = 0; u < kRound; ++u) m[u] = fmaxf(m[u], __shfl_xor_sync(0xffffffffu, m[u], o));
-        }
-        // the operations of quantize_q8_0_lane (IEEE division and reciprocal),
-        // once per block: lane j of the 8 sharing a block takes round j's block
-        // and the results are broadcast to the other 7
-        static_assert(kRound == 8, "one round per lane of a block's 8 lanes");
-        float mj = m[0];
-#pragma unroll
-        for (int u = 1; u < kRound; ++u) mj = j == u ? m[u] : mj;
-        const float dj = __fdiv_rn(mj, 127.0f);
-        const float idj = dj != 0.0f ? __frcp_rn(dj) : 0.0f;
-        const uint32_t dbj = __half_as_ushort(__float2half_rn(dj));
-        float id[kRound];
-        unsigned short db[kRound];
-#pragma unroll
-        for (int u = 0; u < kRound; ++u) {
-            const int src = (lane & ~7) | u;
-            id[u] = __shfl_sync(0xffffffffu, idj, src);
-            db[u] = static_cast<unsigned short>(__shfl_sync(0xffffffffu, dbj, src));
-        }
-#pragma unroll
-        for (int u = 0; u < kRound; ++u) {
-            const int qd = q0 + u * kWarps;
-            if (qd < nquads) {  // warp-uniform
-                const uint32_t c0 = static_cast<uint8_t>(static_cast<int8_t>(static_cast<int>(roundf(__fmul_rn(v[u].x, id[u])))));
-                const uint32_t c1 = static_cast<uint8_t>(static_cast<int8_t>(static_cast<int>(roundf(__fmul_rn(v[u].y, id[u])))));
-                const uint32_t c2 = static_cast<uint8_t>(static_cast<int8_t>(static_cast<int>(roundf(__fmul_rn(v[u].z, id[u])))));
-                const uint32_t c3 = static_cast<uint8_t>(static_cast<int8_t>(static_cast<int>(roundf(__fmul_rn(v[u].w, id[u])))));
-                uint8_t *blk = xs + 34 * (4 * qd + sub);
-                uint16_t *dst = reinterpret_cast<uint16_t *>(blk + 2 + 4 * j);  // 2-byte aligned
-                dst[0] = static_cast<uint16_t>(c0 | (c1 << 8));
-                dst[1] = static_cast<uint16_t>(c2 | (c3 << 8));
-                if (j == 0) *reinterpret_cast<unsigned short *>(blk) = db[u];
-            }
+    } else {
+        for (int q0 = warp; q0 < nquads; q0 += kStep) {
+            float4 v[kRound];
+            quantize_round_load<kWarps, kRound>(xf, nquads, q0, sub, j, v);
+            quantize_round_store<kWarps, kRound>(v, nquads, q0, xs, lane, sub, j);
         }
     }
 }

@@ -165,7 +165,7 @@ __global__ void __launch_bounds__(kTmaThreads, 3) dmmv_vsplit_kernel(const DmmvA
     pdl_wait();  // outputs may still be read, and the activations written, by the preceding kernel
     if constexpr (FX) {
         // nb is a multiple of 8 on this path: whole quads of blocks per vector
-        quantize_quads_to_smem<kWarps>(a.xf, a.batch * (nb >> 2), xs, warp, lane);
+        quantize_quads_to_smem<kWarps, 8, true>(a.xf, a.batch * (nb >> 2), xs, warp, lane);
         consumer_barrier();
     } else {
         // waits are warp-uniform so a timeout can never split a warp before its shuffles
