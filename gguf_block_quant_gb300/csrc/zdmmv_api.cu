@@ -646,7 +646,11 @@ zdmmv_status run_dmmv(int fmt, int layout, DmmvArgs a, int slots, cudaStream_t s
         a.x_bytes_padded = p.x_bytes_padded;
         int per_sm = fmt == kFmtQ8 ? tma_ctas_per_sm_q8(layout, p) : tma_ctas_per_sm_q4(layout, p);
         const int64_t launch_bytes = a.rows * a.nb * static_cast<int64_t>(block_bytes(fmt)) * slots;
-        const int want = ctas_per_sm_per_launch(launch_bytes, a.idx != nullptr);
+        // a gather that reads its indices before the dependency wait streams its
+        // weights early like a plain DMMV and takes the plain launch's CTAs per SM
+        // (MoE down gather after gate/up: 2 per SM 7.15 us per token-layer, as many
+        // as fit 7.29 us)
+        const int want = ctas_per_sm_per_launch(launch_bytes, a.idx != nullptr && !a.idx_ready);
         if (per_sm > want) per_sm = want;
         const int64_t total = static_cast<int64_t>(dev->sms) * per_sm;
         int64_t ctas = total / slots;
@@ -763,7 +767,7 @@ zdmmv_status dmmv_entry(int fmt, const void *w, zdmmv_layout layout, int64_t row
 zdmmv_status gather_entry(int fmt, const void *w_stack, const void *w_stack_b, int64_t expert_stride_bytes,
                           int layout, int64_t rows, int64_t cols, const int32_t *idx, int n, int n_experts,
                           const void *xq, int64_t xq_stride_bytes, float *y, float *y_b, int32_t *status_dev,
-                          cudaStream_t st) {
+                          cudaStream_t st, bool idx_ready = false) {
     zdmmv_status s = check_matrix(fmt, w_stack, layout, rows, cols, xq, y);
     if (s != ZDMMV_OK) return s;
     if (n < 0 || n > 32767 || n_experts < 0) return ZDMMV_ERR_SHAPE;
@@ -793,6 +797,7 @@ zdmmv_status gather_entry(int fmt, const void *w_stack, const void *w_stack_b, i
     a.rows = rows;
     a.nb = static_cast<int32_t>(nb);
     a.batch = 1;
+    a.idx_ready = idx_ready ? 1 : 0;
     return run_dmmv(fmt, layout, a, w_stack_b ? 2 * n : n, st);
 }
 
@@ -1141,6 +1146,14 @@ zdmmv_status zdmmv_expert_gather(zdmmv_fmt fmt, const void *w_stack, int64_t exp
                                  int32_t *status_dev, zdmmv_stream_t stream) {
     return gather_entry(fmt, w_stack, nullptr, expert_stride_bytes, layout, rows, cols, idx, n, n_experts, xq,
                         xq_stride_bytes, y, nullptr, status_dev, reinterpret_cast<cudaStream_t>(stream));
+}
+
+zdmmv_status zdmmv_expert_gather_ready(zdmmv_fmt fmt, const void *w_stack, int64_t expert_stride_bytes,
+                                       zdmmv_layout layout, int64_t rows, int64_t cols, const int32_t *idx, int n,
+                                       int n_experts, const void *xq, int64_t xq_stride_bytes, float *y,
+                                       int32_t *status_dev, zdmmv_stream_t stream) {
+    return gather_entry(fmt, w_stack, nullptr, expert_stride_bytes, layout, rows, cols, idx, n, n_experts, xq,
+                        xq_stride_bytes, y, nullptr, status_dev, reinterpret_cast<cudaStream_t>(stream), true);
 }
 
 zdmmv_status zdmmv_expert_gather2(zdmmv_fmt fmt, const void *w_stack_a, const void *w_stack_b,

@@ -35,6 +35,7 @@ struct DmmvArgs {
     uint2 *argmax_parts;     // argmax epilogue: per-CTA (max bits, row), or nullptr
     const float *gate;       // accumulate epilogue: device scalar g, y += sigmoid(g) * W.x; nullptr: y += W.x
     int32_t accumulate;      // plain kernel: accumulate epilogue instead of store
+    int32_t idx_ready;       // gather: the index list is complete when the grid starts (read before the wait)
 };
 
 // Most CTAs an argmax launch uses (its workspace holds one 8-byte partial each).

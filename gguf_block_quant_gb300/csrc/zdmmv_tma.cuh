@@ -191,8 +191,12 @@ __global__ void __launch_bounds__(kTmaThreads, MINB) dmmv_tma_kernel(const DmmvA
     const int nb = a.nb;
 
     // Dependent launches may start as soon as every CTA of this grid is resident;
-    // what they do before their own dependency wait is stream weights only.
-    pdl_launch_dependents();
+    // what they do before their own dependency wait is stream weights only. A
+    // gather that waits for its index list lets them start only after that wait:
+    // then the list is complete whenever a later launch starts, and a later
+    // gather of the same selection may read it at once (a.idx_ready).
+    const bool early_idx = a.idx != nullptr && a.idx_ready != 0;
+    if (a.idx == nullptr || early_idx) pdl_launch_dependents();
 
     // a second stack (e.g. the up projections next to the gates) takes the slots
     // from slots_a on, with the same selected experts and activations
@@ -202,9 +206,16 @@ __global__ void __launch_bounds__(kTmaThreads, MINB) dmmv_tma_kernel(const DmmvA
     const uint8_t *w = second ? a.w_b : a.w;
     const uint8_t *w_up = EPI == 3 ? a.w_b : nullptr;  // SwiGLU pair: the up matrix
     if (a.idx != nullptr) {
-        pdl_wait();  // the index list may be written by the preceding kernel
-        const int e = a.idx[sel];
+        int e;
+        if (early_idx) {
+            e = __ldcg(a.idx + sel);  // complete since an earlier gather's wait; L2, not a stale L1 line
+        } else {
+            pdl_wait();  // the index list may be written by the preceding kernel
+            e = a.idx[sel];
+            pdl_launch_dependents();
+        }
         if (e < 0 || e >= a.n_experts) {
+            if (early_idx) pdl_wait();  // y may still be read by the preceding kernel
             for (int64_t r = r0 + tid; r < r1; r += blockDim.x) y[r] = __int_as_float(0x7fc00000);
             if (tid == 0 && a.status != nullptr) atomicExch(a.status, 1);
             return;

@@ -62,6 +62,8 @@ _SIGS = {
     "zdmmv_dmmv_argmax_noalloc": ([_int, _vp, _int, _i64, _i64, _vp, _vp, _vp, _vp], _int),
     "zdmmv_expert_gather": ([_int, _vp, _i64, _int, _i64, _i64, _vp, _int, _int, _vp, _i64, _vp, _vp, _vp],
                             _int),
+    "zdmmv_expert_gather_ready": ([_int, _vp, _i64, _int, _i64, _i64, _vp, _int, _int, _vp, _i64, _vp, _vp,
+                                   _vp], _int),
     "zdmmv_expert_gather2": ([_int, _vp, _vp, _i64, _int, _i64, _i64, _vp, _int, _int, _vp, _i64, _vp, _vp,
                               _vp, _vp], _int),
     "zdmmv_expert_swiglu": ([_int, _vp, _vp, _i64, _int, _i64, _i64, _vp, _int, _int, _vp, _i64, _vp, _vp,
@@ -239,13 +241,15 @@ def dmmv_argmax_noalloc(fmt: int, w, rows: int, cols: int, xq, out=None, max_out
 
 
 def expert_gather(fmt: int, w_stack, expert_stride: int, rows: int, cols: int, idx, n_experts: int, xq,
-                  xq_stride: int, y=None, status=None, layout: int = GGUF, stream=None):
+                  xq_stride: int, y=None, status=None, layout: int = GGUF, stream=None, idx_ready: bool = False):
+    """idx_ready=True calls zdmmv_expert_gather_ready: an earlier expert call on
+    the stream has read the same final index list (see include/zdmmv.h)."""
     n = idx.numel()
     if idx.dtype != torch.int32:
         raise ValueError("expert_gather: idx must be int32")
     y = _out(y, (n, rows), w_stack.device)
-    _call("zdmmv_expert_gather", fmt, _ptr(w_stack), expert_stride, layout, rows, cols, _ptr(idx), n,
-          n_experts, _ptr(xq), xq_stride, _ptr(y), _ptr(status), _stream(stream))
+    _call("zdmmv_expert_gather_ready" if idx_ready else "zdmmv_expert_gather", fmt, _ptr(w_stack), expert_stride,
+          layout, rows, cols, _ptr(idx), n, n_experts, _ptr(xq), xq_stride, _ptr(y), _ptr(status), _stream(stream))
     return y
 
 

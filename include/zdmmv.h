@@ -385,6 +385,30 @@ zdmmv_status zdmmv_expert_gather(zdmmv_fmt fmt, const void *w_stack,
                                  int n_experts, const void *xq, int64_t xq_stride_bytes,
                                  float *y, int32_t *status_dev, zdmmv_stream_t stream);
 
+/* zdmmv_expert_gather for a selection that an earlier expert call has already
+ * read: the down projections after the gate/up launch of the same experts, or
+ * the up projections after the gates' gather (the MoE step's gate/up DMMV, then
+ * the down DMMV of the same routed experts: "CUDA backend for ZINC", "5. The
+ * target model & milestone ordering", M1). zdmmv_expert_gather must wait for
+ * the preceding kernel before it reads idx, so its weights cannot stream until
+ * then; this call reads idx as soon as its kernel starts and streams its first
+ * weight tiles while the preceding kernel still runs. It waits for that kernel
+ * before it reads xq or writes y, so xq (and y) may be written (read) by it.
+ *   Arguments, results (bit for bit) and errors as zdmmv_expert_gather.
+ *   Requirement on idx: an earlier call among zdmmv_expert_gather,
+ *   zdmmv_expert_gather2, zdmmv_expert_swiglu and zdmmv_expert_gather_ready that
+ *   this call is ordered after (the same stream, or an event) read the same
+ *   device list, with its final contents, and nothing has written the list since.
+ *   Those calls let later launches start only once their own index list is
+ *   complete (after their dependency wait), so the list this call reads is
+ *   complete too. Without that earlier call the kernel may read a list that the
+ *   preceding kernel is still writing: use zdmmv_expert_gather. */
+zdmmv_status zdmmv_expert_gather_ready(zdmmv_fmt fmt, const void *w_stack,
+                                       int64_t expert_stride_bytes, zdmmv_layout layout,
+                                       int64_t rows, int64_t cols, const int32_t *idx, int n,
+                                       int n_experts, const void *xq, int64_t xq_stride_bytes,
+                                       float *y, int32_t *status_dev, zdmmv_stream_t stream);
+
 /* Two expert stacks of the same shape and format against the same selected
  * experts and activations, in ONE launch: y_a[k] = A_{idx[k]} . x_k and
  * y_b[k] = B_{idx[k]} . x_k (the gate and up projections of the routed experts,

@@ -68,13 +68,16 @@ def test_other_argument_checks(L):
     assert L.zdmmv_quantize_act_q8_0(FAKE, 33, FAKE, None) == 2
     assert L.zdmmv_quantize_act_q8_0(None, 64, FAKE, None) == 1
     assert L.zdmmv_quantize_act_q8_0(FAKE + 2, 64, FAKE, None) == 3
-    g = L.zdmmv_expert_gather
-    assert g(3, FAKE, 1 << 16, 0, 4, 64, FAKE, 2, 8, FAKE, 0, FAKE, None, None) == 5      # format
-    assert g(2, FAKE, 1 << 16, 0, 4, 64, None, 2, 8, FAKE, 0, FAKE, None, None) == 1      # idx null
-    assert g(2, FAKE, 8, 0, 4, 64, FAKE, 2, 8, FAKE, 0, FAKE, None, None) == 2            # stride < matrix
-    assert g(2, FAKE, 1 << 16, 0, 4, 64, FAKE, 2, 8, FAKE, 40, FAKE, None, None) == 2     # xq stride < vector
-    assert g(2, FAKE, (1 << 16) + 8, 0, 4, 64, FAKE, 2, 8, FAKE, 0, FAKE, None, None) == 3  # stride % 16
-    assert g(2, FAKE, 1 << 16, 0, 4, 64, FAKE, -1, 8, FAKE, 0, FAKE, None, None) == 2     # n < 0
+    # the ready gather (indices already read by an earlier expert call) checks the same arguments
+    for g in (L.zdmmv_expert_gather, L.zdmmv_expert_gather_ready):
+        assert g(3, FAKE, 1 << 16, 0, 4, 64, FAKE, 2, 8, FAKE, 0, FAKE, None, None) == 5      # format
+        assert g(2, FAKE, 1 << 16, 0, 4, 64, None, 2, 8, FAKE, 0, FAKE, None, None) == 1      # idx null
+        assert g(2, FAKE, 8, 0, 4, 64, FAKE, 2, 8, FAKE, 0, FAKE, None, None) == 2            # stride < matrix
+        assert g(2, FAKE, 1 << 16, 0, 4, 64, FAKE, 2, 8, FAKE, 40, FAKE, None, None) == 2     # xq stride < vector
+        assert g(2, FAKE, (1 << 16) + 8, 0, 4, 64, FAKE, 2, 8, FAKE, 0, FAKE, None, None) == 3  # stride % 16
+        assert g(2, FAKE, 1 << 16, 0, 4, 64, FAKE, -1, 8, FAKE, 0, FAKE, None, None) == 2     # n < 0
+        assert g(2, FAKE, 1 << 16, 0, 4, 64, FAKE + 2, 2, 8, FAKE, 0, FAKE, None, None) == 3  # idx misaligned
+        assert g(2, FAKE, 1 << 16, 0, 4, 64, FAKE, 0, 8, FAKE, 0, FAKE, None, None) == 0      # n == 0
     assert L.zdmmv_repack(8, FAKE, 4, 64, FAKE + 4096, 10, None) == 6                     # dst too small
     assert L.zdmmv_repack(8, FAKE, 4, 64, FAKE + 16, 4096, None) == 2                     # overlap
     assert L.zdmmv_repack(3, FAKE, 4, 64, FAKE + 4096, 4096, None) == 5
