@@ -560,6 +560,17 @@ def measure_moe(steps, warmup, world, device, eager, l2_bytes):
             Z.expert_gather(Z.Q8_0, d, dn, m.hidden, m.ffn, idx, m.n_slots, hq, (m.ffn // 32) * 34, y=yd,
                             status=st)
 
+    def step_ffn2():
+        # the same FFN in two launches: SwiGLU, then the down gather of h (fp32,
+        # quantized in the gather's prologue), which reads its indices at once
+        for l in range(layers):
+            g, u, d = stacks[l]
+            idx = idxs[l]
+            Z.expert_swiglu(Z.Q4_0, g, u, m.ffn, m.hidden, xq, idx=idx, expert_stride=gu, n_experts=m.n_slots,
+                            h=h, status=st)
+            Z.expert_gather_f32(Z.Q8_0, d, dn, m.hidden, m.ffn, idx, m.n_slots, h, m.ffn, y=yd, status=st,
+                                idx_ready=True)
+
     ws = Z.expert_ffn_workspace(m.n_sel, m.ffn)
 
     def step_ffn():
@@ -578,6 +589,7 @@ def measure_moe(steps, warmup, world, device, eager, l2_bytes):
     for name, fn, launches, nb_ in (("three_launch", step3, 3, nbytes), ("gate_up_fused", step2, 2, nbytes),
                                     ("gate_up_swiglu", step_swiglu, 2, nbytes_swiglu),
                                     ("ffn_chained_three_launch", step_chain, 3, nbytes_swiglu),
+                                    ("ffn_chained_two_launch", step_ffn2, 2, nbytes_swiglu),
                                     ("ffn_one_launch", step_ffn, 1, nbytes_swiglu)):
         run = graph_or_eager(fn, eager)
         ms, _ = time_fn(run, steps, warmup, world, device)
@@ -589,6 +601,8 @@ def measure_moe(steps, warmup, world, device, eager, l2_bytes):
     out["ffn_one_launch"]["note"] = ("gate/up + SwiGLU and the down DMMV of the quantized SwiGLU output in one "
                                      "launch (the down input is h, not the independent activation)")
     out["ffn_chained_three_launch"]["note"] = "the same chained FFN as SwiGLU, quantize h, down gather"
+    out["ffn_chained_two_launch"]["note"] = ("the same chained FFN as SwiGLU, then the down gather of the fp32 h "
+                                             "(quantized in its prologue; indices read at once)")
     for k in ("three_launch", "gate_up_fused", "gate_up_swiglu"):
         out[k]["note"] = ("the calls after a layer's first read its index list at once "
                           "(zdmmv_expert_gather_ready) and stream their weights during the previous launch")
@@ -826,7 +840,7 @@ def gpu_arm(args):
         summary["moe_experts_top8_plus_shared"] = {
             k: pair(moe[k]["us_per_token_layer"], moe[k]["gbs"], hbm_peak)
             for k in ("three_launch", "gate_up_fused", "gate_up_swiglu", "ffn_chained_three_launch",
-                      "ffn_one_launch")}
+                      "ffn_chained_two_launch", "ffn_one_launch")}
         detail["moe_experts_top8_plus_shared"] = moe
     if Z.device_status() != 0:
         raise RuntimeError("the device reported a fault during the measurements")

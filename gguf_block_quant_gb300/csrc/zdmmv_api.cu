@@ -801,6 +801,45 @@ zdmmv_status gather_entry(int fmt, const void *w_stack, const void *w_stack_b, i
     return run_dmmv(fmt, layout, a, w_stack_b ? 2 * n : n, st);
 }
 
+// Expert gather over fp32 activations: the pipelined kernel's fused-quantization
+// variant with one slot per selected expert (each CTA quantizes its slot's
+// activation with the stand-alone quantizer's arithmetic, so the result is the
+// quantizer followed by the gather, bit for bit).
+zdmmv_status gather_f32_entry(int fmt, const void *w_stack, int64_t expert_stride_bytes, int layout, int64_t rows,
+                              int64_t cols, const int32_t *idx, int n, int n_experts, const float *x,
+                              int64_t x_stride, float *y, int32_t *status_dev, bool idx_ready, cudaStream_t st) {
+    if (block_bytes(fmt) == 0) return ZDMMV_ERR_FORMAT;
+    if (layout != ZDMMV_LAYOUT_GGUF && layout != ZDMMV_LAYOUT_REPACKED) return ZDMMV_ERR_LAYOUT;
+    if (rows < 0 || cols <= 0 || cols % kQK || n < 0 || n > 32767 || n_experts < 0) return ZDMMV_ERR_SHAPE;
+    if (n == 0 || rows == 0) return ZDMMV_OK;
+    if (!tma_shape_ok(fmt, cols)) return ZDMMV_ERR_SHAPE;  // the pipelined widths (multiples of 256, <= 8192)
+    if (!w_stack || !idx || !x || !y) return ZDMMV_ERR_NULL;
+    if (!aligned(w_stack, 16) || !aligned(x, 16) || !aligned(y, 4) || !aligned(idx, 4) ||
+        (status_dev && !aligned(status_dev, 4)))
+        return ZDMMV_ERR_ALIGN;
+    const int64_t nb = cols / kQK;
+    const int64_t mat_bytes = rows * nb * block_bytes(fmt);
+    if (expert_stride_bytes < 0 || x_stride < 0) return ZDMMV_ERR_SHAPE;
+    if (n_experts > 1 && expert_stride_bytes < mat_bytes) return ZDMMV_ERR_SHAPE;
+    if (x_stride != 0 && x_stride < cols) return ZDMMV_ERR_SHAPE;
+    if (expert_stride_bytes % 16 || x_stride % 4) return ZDMMV_ERR_ALIGN;
+    DmmvArgs a{};
+    a.w = static_cast<const uint8_t *>(w_stack);
+    a.expert_stride = expert_stride_bytes;
+    a.idx = idx;
+    a.n_experts = n_experts;
+    a.status = status_dev;
+    a.xf = x;
+    a.xf_stride = x_stride;
+    a.y = y;
+    a.y_stride = rows;
+    a.rows = rows;
+    a.nb = static_cast<int32_t>(nb);
+    a.batch = 1;
+    a.idx_ready = idx_ready ? 1 : 0;
+    return run_dmmv(fmt, layout, a, n, st, true);
+}
+
 zdmmv_status argmax_entry(int fmt, const void *w, int layout, int64_t rows, int64_t cols, const void *xq,
                           int32_t *argmax_out, float *max_out, void *workspace, size_t workspace_bytes,
                           cudaStream_t st) {
@@ -1154,6 +1193,14 @@ zdmmv_status zdmmv_expert_gather_ready(zdmmv_fmt fmt, const void *w_stack, int64
                                        int32_t *status_dev, zdmmv_stream_t stream) {
     return gather_entry(fmt, w_stack, nullptr, expert_stride_bytes, layout, rows, cols, idx, n, n_experts, xq,
                         xq_stride_bytes, y, nullptr, status_dev, reinterpret_cast<cudaStream_t>(stream), true);
+}
+
+zdmmv_status zdmmv_expert_gather_f32(zdmmv_fmt fmt, const void *w_stack, int64_t expert_stride_bytes,
+                                     zdmmv_layout layout, int64_t rows, int64_t cols, const int32_t *idx, int n,
+                                     int n_experts, const float *x, int64_t x_stride, float *y,
+                                     int32_t *status_dev, int idx_ready, zdmmv_stream_t stream) {
+    return gather_f32_entry(fmt, w_stack, expert_stride_bytes, layout, rows, cols, idx, n, n_experts, x, x_stride,
+                            y, status_dev, idx_ready != 0, reinterpret_cast<cudaStream_t>(stream));
 }
 
 zdmmv_status zdmmv_expert_gather2(zdmmv_fmt fmt, const void *w_stack_a, const void *w_stack_b,

@@ -64,6 +64,8 @@ _SIGS = {
                             _int),
     "zdmmv_expert_gather_ready": ([_int, _vp, _i64, _int, _i64, _i64, _vp, _int, _int, _vp, _i64, _vp, _vp,
                                    _vp], _int),
+    "zdmmv_expert_gather_f32": ([_int, _vp, _i64, _int, _i64, _i64, _vp, _int, _int, _vp, _i64, _vp, _vp,
+                                 _int, _vp], _int),
     "zdmmv_expert_gather2": ([_int, _vp, _vp, _i64, _int, _i64, _i64, _vp, _int, _int, _vp, _i64, _vp, _vp,
                               _vp, _vp], _int),
     "zdmmv_expert_swiglu": ([_int, _vp, _vp, _i64, _int, _i64, _i64, _vp, _int, _int, _vp, _i64, _vp, _vp,
@@ -250,6 +252,20 @@ def expert_gather(fmt: int, w_stack, expert_stride: int, rows: int, cols: int, i
     y = _out(y, (n, rows), w_stack.device)
     _call("zdmmv_expert_gather_ready" if idx_ready else "zdmmv_expert_gather", fmt, _ptr(w_stack), expert_stride,
           layout, rows, cols, _ptr(idx), n, n_experts, _ptr(xq), xq_stride, _ptr(y), _ptr(status), _stream(stream))
+    return y
+
+
+def expert_gather_f32(fmt: int, w_stack, expert_stride: int, rows: int, cols: int, idx, n_experts: int, x,
+                      x_stride: int, y=None, status=None, layout: int = GGUF, stream=None, idx_ready: bool = False):
+    """Gather over fp32 activations (slot k: x + k*x_stride floats), quantized in the launch."""
+    n = idx.numel()
+    if idx.dtype != torch.int32:
+        raise ValueError("expert_gather_f32: idx must be int32")
+    if x.dtype != torch.float32:
+        raise ValueError("expert_gather_f32: x must be float32")
+    y = _out(y, (n, rows), w_stack.device)
+    _call("zdmmv_expert_gather_f32", fmt, _ptr(w_stack), expert_stride, layout, rows, cols, _ptr(idx), n,
+          n_experts, _ptr(x), x_stride, _ptr(y), _ptr(status), 1 if idx_ready else 0, _stream(stream))
     return y
 
 

@@ -409,6 +409,31 @@ zdmmv_status zdmmv_expert_gather_ready(zdmmv_fmt fmt, const void *w_stack,
                                        int n_experts, const void *xq, int64_t xq_stride_bytes,
                                        float *y, int32_t *status_dev, zdmmv_stream_t stream);
 
+/* Expert gather over fp32 activations, quantized to Q8_0 inside the launch: the
+ * MoE step's down DMMV of the SwiGLU output h without a separate quantizer
+ * launch (M1's gate/up DMMV, swiglu, down DMMV: "CUDA backend for ZINC", "5. The
+ * target model & milestone ordering"; fewer dispatches per token: habr article,
+ * "Gap analysis"). Each CTA quantizes its slot's activation into shared memory
+ * with the arithmetic of zdmmv_quantize_act_q8_0, so slot k's result equals
+ * zdmmv_quantize_act_q8_0 of x_k followed by zdmmv_expert_gather, bit for bit.
+ *   fmt, w_stack, expert_stride_bytes, layout, rows, idx, n, n_experts,
+ *   status_dev   as zdmmv_expert_gather; cols a multiple of 256 and at most 8192
+ *                (else ERR_SHAPE).
+ *   x            device fp32, 16-byte aligned; slot k reads x + k*x_stride
+ *                (x_stride in floats: 0 = one activation shared by all slots,
+ *                else a multiple of 4 and >= cols). x may be written by the
+ *                preceding kernel in the stream (e.g. zdmmv_expert_swiglu's h).
+ *   y            device fp32 [n][rows].
+ *   idx_ready    0: read idx after waiting for the preceding kernel, as
+ *                zdmmv_expert_gather; nonzero: read it at once and stream weights
+ *                early, under zdmmv_expert_gather_ready's requirement on idx.
+ * Errors: ERR_NULL, ERR_SHAPE, ERR_ALIGN, ERR_LAYOUT, ERR_FORMAT, ERR_CUDA. */
+zdmmv_status zdmmv_expert_gather_f32(zdmmv_fmt fmt, const void *w_stack,
+                                     int64_t expert_stride_bytes, zdmmv_layout layout,
+                                     int64_t rows, int64_t cols, const int32_t *idx, int n,
+                                     int n_experts, const float *x, int64_t x_stride, float *y,
+                                     int32_t *status_dev, int idx_ready, zdmmv_stream_t stream);
+
 /* Two expert stacks of the same shape and format against the same selected
  * experts and activations, in ONE launch: y_a[k] = A_{idx[k]} . x_k and
  * y_b[k] = B_{idx[k]} . x_k (the gate and up projections of the routed experts,

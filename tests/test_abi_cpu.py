@@ -78,6 +78,16 @@ def test_other_argument_checks(L):
         assert g(2, FAKE, 1 << 16, 0, 4, 64, FAKE, -1, 8, FAKE, 0, FAKE, None, None) == 2     # n < 0
         assert g(2, FAKE, 1 << 16, 0, 4, 64, FAKE + 2, 2, 8, FAKE, 0, FAKE, None, None) == 3  # idx misaligned
         assert g(2, FAKE, 1 << 16, 0, 4, 64, FAKE, 0, 8, FAKE, 0, FAKE, None, None) == 0      # n == 0
+    gf = L.zdmmv_expert_gather_f32
+    assert gf(2, FAKE, 1 << 16, 0, 4, 256, FAKE, 0, 8, FAKE, 0, FAKE, None, 0, None) == 0      # n == 0
+    assert gf(3, FAKE, 1 << 16, 0, 4, 256, FAKE, 2, 8, FAKE, 0, FAKE, None, 0, None) == 5      # format
+    assert gf(2, FAKE, 1 << 16, 0, 4, 96, FAKE, 2, 8, FAKE, 0, FAKE, None, 0, None) == 2       # off the pipelined widths
+    assert gf(2, FAKE, 1 << 16, 0, 4, 256, None, 2, 8, FAKE, 0, FAKE, None, 1, None) == 1      # idx null
+    assert gf(2, FAKE, 1 << 16, 0, 4, 256, FAKE, 2, 8, FAKE + 4, 0, FAKE, None, 0, None) == 3  # x not 16-byte aligned
+    assert gf(2, FAKE, 1 << 16, 0, 4, 256, FAKE, 2, 8, FAKE, 258, FAKE, None, 0, None) == 3    # x stride % 4
+    assert gf(2, FAKE, 1 << 16, 0, 4, 256, FAKE, 2, 8, FAKE, 128, FAKE, None, 0, None) == 2    # x stride < cols
+    assert gf(2, FAKE, 8, 0, 4, 256, FAKE, 2, 8, FAKE, 0, FAKE, None, 0, None) == 2            # stride < matrix
+    assert gf(2, FAKE, 1 << 16, 2, 4, 256, FAKE, 2, 8, FAKE, 0, FAKE, None, 0, None) == 4      # layout
     assert L.zdmmv_repack(8, FAKE, 4, 64, FAKE + 4096, 10, None) == 6                     # dst too small
     assert L.zdmmv_repack(8, FAKE, 4, 64, FAKE + 16, 4096, None) == 2                     # overlap
     assert L.zdmmv_repack(3, FAKE, 4, 64, FAKE + 4096, 4096, None) == 5

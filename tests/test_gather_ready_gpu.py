@@ -1,6 +1,9 @@
 """zdmmv_expert_gather_ready: the expert gather that reads its index list as soon
 as its kernel starts, for a list an earlier expert call on the stream has read
-(the down projections after the gate/up launch of the same experts).
+(the down projections after the gate/up launch of the same experts); and
+zdmmv_expert_gather_f32, the gather over fp32 activations quantized in the
+launch (the down projection of the SwiGLU output without a quantizer launch),
+which reads its list either way.
 
 Its results must be those of zdmmv_expert_gather bit for bit (same kernel
 arithmetic), NaN rows and the status word for an out-of-range index included;
@@ -139,3 +142,97 @@ def test_ready_gather_sees_each_layers_list(graph):
                               y=nan_out(n, hidden))
         torch.cuda.synchronize()
         assert torch.equal(ys[l], ref), f"layer {l}: the ready gather did not use that layer's list"
+
+
+@pytest.mark.parametrize("ready", [0, 1])
+@pytest.mark.parametrize("layout", [Z.GGUF, Z.REPACKED])
+@pytest.mark.parametrize("fmt,rows,cols,shared", [(Q8_0, 2048, 512, False), (Q4_0, 512, 2048, False),
+                                                  (Q8_0, 300, 4096, True), (Q4_0, 1000, 256, False)])
+def test_gather_f32_equals_quantize_then_gather(fmt, rows, cols, shared, layout, ready):
+    """Slot k of the fp32-activation gather equals zdmmv_quantize_act_q8_0 of its
+    activation followed by zdmmv_expert_gather, bit for bit (the same quantizer
+    arithmetic in the kernel's prologue); per-slot activations at a padded stride
+    or one shared activation; an out-of-range index gives NaN rows and status 1."""
+    n_exp = 9
+    _, d_gu, per_gu = _stack(fmt, rows, cols, n_exp, seed=81, layout=layout)
+    s_dn, d_dn, per_dn = _stack(fmt, rows, cols, n_exp, seed=82, layout=layout, stream=synth.S_WEIGHT3)
+    idx = np.array([3, 8, 0, 9, 5, 5, 1], dtype=np.int32)   # 9 is out of range
+    n = len(idx)
+    xs = 0 if shared else cols + 8                         # floats; a multiple of 4
+    xv = synth.activations(cols, seed=83, batch=1 if shared else n).reshape(1 if shared else n, cols)
+    xpad = np.zeros((xv.shape[0], cols if shared else xs), dtype=np.float32)
+    xpad[:, :cols] = xv
+    di, dx = dev(idx), dev(xpad.reshape(-1))
+    st_gu = torch.zeros(1, dtype=torch.int32, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    st_ref = torch.zeros(1, dtype=torch.int32, device="cuda")
+    # an earlier expert call of the same list (the ready read's requirement)
+    Z.expert_gather2(fmt, d_gu, d_gu, per_gu, rows, cols, di, n_exp, Z.quantize_act_q8_0(dev(xv[0])), 0,
+                     status=st_gu, layout=layout)
+    y = Z.expert_gather_f32(fmt, d_dn, per_dn, rows, cols, di, n_exp, dx, xs, y=nan_out(n, rows), status=st,
+                            layout=layout, idx_ready=bool(ready))
+    xq = Z.quantize_act_q8_0(dev(np.ascontiguousarray(xv)))
+    y_ref = Z.expert_gather(fmt, d_dn, per_dn, rows, cols, di, n_exp, xq, 0 if shared else cols // 32 * 34,
+                            y=nan_out(n, rows), status=st_ref, layout=layout)
+    torch.cuda.synchronize()
+    assert st.item() == 1 and st_ref.item() == 1
+    good = [k for k in range(n) if idx[k] < n_exp]
+    assert torch.isnan(y[3]).all()
+    assert torch.equal(y[good], y_ref[good])
+    xq_o = oracle.quantize_q8_0(xv.reshape(-1))
+    assert np.array_equal(xq.cpu().numpy(), xq_o)
+    yo, eo, _ = oracle.expert_gather(fmt, s_dn, per_dn, rows, cols, idx, n_exp, xq_o,
+                                     0 if shared else cols // 32 * 34)
+    ok, worst = oracle.within_tolerance(y[good].double().cpu().numpy(), yo[good], eo[good])
+    assert ok, worst
+
+
+@pytest.mark.parametrize("graph", [False, True])
+def test_two_launch_ffn_equals_one_launch_ffn(graph):
+    """The selected experts' FFN as two launches, zdmmv_expert_swiglu (h) then the
+    ready fp32-activation down gather of h, in a 10-layer loop that rewrites one
+    index buffer by a kernel before every layer: each layer's y equals the
+    one-launch zdmmv_expert_ffn of that layer's list, and its h, bit for bit."""
+    hidden, ffn, n_exp, layers, n = 2048, 512, 33, 10, 9
+    _, d_g, per_gu = _stack(Q4_0, ffn, hidden, n_exp, seed=91, layout=Z.GGUF)
+    _, d_u, _ = _stack(Q4_0, ffn, hidden, n_exp, seed=92, layout=Z.GGUF, stream=synth.S_WEIGHT2)
+    _, d_d, per_dn = _stack(Q8_0, hidden, ffn, n_exp, seed=93, layout=Z.GGUF, stream=synth.S_WEIGHT3)
+    lists = np.stack([synth.expert_indices(200 + l, n_routed=n_exp - 1, top_k=n - 1) for l in range(layers)])
+    src = dev(lists.astype(np.int32))
+    idx = torch.zeros(n, dtype=torch.int32, device="cuda")
+    xq = dev(oracle.quantize_q8_0(synth.activations(hidden, seed=94)))
+    hs = [torch.full((n, ffn), float("nan"), device="cuda") for _ in range(layers)]
+    ys = [nan_out(n, hidden) for _ in range(layers)]
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+
+    def run():
+        for l in range(layers):
+            torch.add(src[l], 0, out=idx)     # the "router"
+            Z.expert_swiglu(Q4_0, d_g, d_u, ffn, hidden, xq, idx=idx, expert_stride=per_gu, n_experts=n_exp,
+                            h=hs[l], status=st)
+            Z.expert_gather_f32(Q8_0, d_d, per_dn, hidden, ffn, idx, n_exp, hs[l], ffn, y=ys[l], status=st,
+                                idx_ready=True)
+
+    if graph:
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            run()
+        torch.cuda.current_stream().wait_stream(s)
+        for t in hs + ys:
+            t.fill_(float("nan"))
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            run()
+        g.replay()
+    else:
+        run()
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    ws = Z.expert_ffn_workspace(n, ffn)
+    for l in range(layers):
+        y1, h1 = Z.expert_ffn(Q4_0, d_g, d_u, per_gu, Q8_0, d_d, per_dn, hidden, ffn, src[l].clone(), n_exp, xq,
+                              y=nan_out(n, hidden), workspace=ws)
+        torch.cuda.synchronize()
+        assert torch.equal(hs[l], h1), f"layer {l}: h differs"
+        assert torch.equal(ys[l], y1), f"layer {l}: y differs from the one-launch FFN"
