@@ -923,7 +923,8 @@ def profile_mode(name: str):
     from gguf_block_quant_gb300 import zdmmv as Z
     Z.lib()
     if name == synth.MOE.name:
-        # the MoE step three ways, 3 times: gate/up+SwiGLU, quantize h, down gather; then the one-launch FFN
+        # the MoE FFN three ways, 3 times: gate/up+SwiGLU, quantize h, down gather; the one-launch FFN;
+        # gate/up+SwiGLU, then the down gather of the fp32 h (indices read at once)
         m = synth.MOE
         gate = torch.from_numpy(synth.weight_blocks(synth.Q4_0, m.n_slots * m.ffn, m.hidden, seed=m.seed)).cuda()
         up = torch.from_numpy(synth.weight_blocks(synth.Q4_0, m.n_slots * m.ffn, m.hidden, seed=m.seed,
@@ -940,6 +941,9 @@ def profile_mode(name: str):
             hq = Z.quantize_act_q8_0(h.reshape(-1))
             Z.expert_gather(Z.Q8_0, down, dn, m.hidden, m.ffn, idx, m.n_slots, hq, (m.ffn // 32) * 34)
             Z.expert_ffn(Z.Q4_0, gate, up, gu, Z.Q8_0, down, dn, m.hidden, m.ffn, idx, m.n_slots, xq, workspace=ws)
+            h2 = Z.expert_swiglu(Z.Q4_0, gate, up, m.ffn, m.hidden, xq, idx=idx, expert_stride=gu,
+                                 n_experts=m.n_slots)
+            Z.expert_gather_f32(Z.Q8_0, down, dn, m.hidden, m.ffn, idx, m.n_slots, h2, m.ffn, idx_ready=True)
         torch.cuda.synchronize()
         print(json.dumps({"profile": name, "fault": Z.device_status()}))
         return
