@@ -40,7 +40,10 @@
  *  - Weight matrices are treated as read-only model parameters: with
  *    programmatic dependent launch the DMMV kernels start streaming weight
  *    tiles before the preceding kernel in the stream has finished (activations,
- *    expert indices and outputs are touched only after it has). A weight buffer
+ *    expert indices and outputs are touched only after it has, except the index
+ *    list of the ready gathers, zdmmv_expert_gather_ready and
+ *    zdmmv_expert_gather_f32 with idx_ready, under their stated requirement). A
+ *    weight buffer
  *    must therefore be complete before the DMMV that reads it is enqueued
  *    behind a kernel still writing it; enqueue an event or synchronize in
  *    between if weights are produced on the device (zdmmv_repack's output may
@@ -51,7 +54,8 @@
  *      ZDMMV_STAGE_KB           target KiB per pipeline stage (4..64, default 20)
  *      ZDMMV_CTAS_PER_SM        CTAs per SM of the single-vector kernel (1..8;
  *                               default 2 below 32 MB of weights per launch, else 4;
- *                               expert gathers as many as fit)
+ *                               expert gathers that wait for their indices as many
+ *                               as fit)
  *      ZDMMV_BATCH_KERNEL       batched kernel (see zdmmv_q8_0_batched for the
  *                               default choice): "vsplit" (the vector split, never
  *                               the tensor-core kernel), "mma" (the tensor-core
