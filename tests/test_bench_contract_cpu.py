@@ -1,5 +1,5 @@
 """bench.py's reference arm (the CPU oracle on the host cores) runs without a
-GPU: run it as the driver does, with a tiny step count, and check that its one
+GPU: run it from the command line, with a tiny step count, and check that its one
 JSON line carries every key of the bench contract with the reference arm's
 additions (impl, cpu_baseline describing the run, an e2e with no transfers)."""
 import json
