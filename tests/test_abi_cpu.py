@@ -21,6 +21,36 @@ def test_every_declared_function_is_exported(L):
     assert set(names) == set(zdmmv._SIGS), "binding and header disagree"
 
 
+def _header_params():
+    """{function: [C type of each parameter]} parsed from include/zdmmv.h."""
+    import os
+    import re
+    from gguf_block_quant_gb300 import _build
+    text = open(os.path.join(_build.INCLUDE, "zdmmv.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    out = {}
+    for name, params in re.findall(r"\b(zdmmv_[a-z0-9_]+)\s*\(([^;{]*?)\)\s*;", text, flags=re.S):
+        ps = [" ".join(p.split()) for p in params.split(",")] if params.strip() not in ("", "void") else []
+        out[name] = ["ptr" if "*" in p else p.rsplit(" ", 1)[0] for p in ps]
+    return out
+
+
+def test_binding_signatures_match_the_header():
+    """Every ctypes signature in the binding has the header's parameter count and,
+    parameter by parameter, the matching ctypes type (pointers and streams as
+    void*, int64_t, size_t, and int for int and the enums)."""
+    want = {"ptr": ctypes.c_void_p, "zdmmv_stream_t": ctypes.c_void_p, "int64_t": ctypes.c_int64,
+            "size_t": ctypes.c_size_t, "int": ctypes.c_int, "zdmmv_fmt": ctypes.c_int,
+            "zdmmv_layout": ctypes.c_int, "zdmmv_status": ctypes.c_int}
+    hdr = _header_params()
+    assert set(hdr) == set(zdmmv._SIGS)
+    for name, (args, _res) in zdmmv._SIGS.items():
+        assert len(args) == len(hdr[name]), (name, len(args), len(hdr[name]))
+        for i, (a, c) in enumerate(zip(args, hdr[name])):
+            typed_ptr = c == "ptr" and isinstance(a, type) and issubclass(a, ctypes._Pointer)
+            assert a is want[c] or typed_ptr, (name, i, c, a)
+
+
 def test_status_strings_and_sizes(L):
     assert L.zdmmv_status_str(0) == b"ok"
     assert L.zdmmv_status_str(2) == b"bad shape"
