@@ -4,7 +4,9 @@ reads them once per process), over one fixed set of cases: single-vector DMMVs
 in both layouts, the fused quantize + DMMV, batched calls of 2-8 vectors
 (widths the vector split, the streaming batch kernel and the tensor-core kernel
 take and do not take, and a 6-vector call the tensor-core kernel takes by
-default), an expert gather and the one-launch expert FFN.
+default), an expert gather, the one-launch expert FFN, the same FFN in two
+launches (SwiGLU, then the fp32-activation gather reading its indices at once)
+and a ready gather.
 
 Knobs documented as leaving the bits unchanged must give the default run's
 outputs bit for bit. The knobs that choose a batched kernel summing a row's
@@ -77,6 +79,11 @@ gu, dn = f_ * (h_ // 32) * 18, h_ * (f_ // 32) * 34
 out["gather"] = Z.expert_gather(Z.Q4_0, gate, gu, f_, h_, idx, moe["slots"], xq, 0)
 y, h = Z.expert_ffn(Z.Q4_0, gate, up, gu, Z.Q8_0, down, dn, h_, f_, idx, moe["slots"], xq)
 out["ffn_y"], out["ffn_h"] = y, h.clone()
+# the same FFN in two launches (the down gather of the fp32 h, indices read at once),
+# then a gate gather of the same selection reading its indices at once
+h2 = Z.expert_swiglu(Z.Q4_0, gate, up, f_, h_, xq, idx=idx, expert_stride=gu, n_experts=moe["slots"])
+out["ffn2_y"] = Z.expert_gather_f32(Z.Q8_0, down, dn, h_, f_, idx, moe["slots"], h2, f_, idx_ready=True)
+out["gather_ready"] = Z.expert_gather(Z.Q4_0, gate, gu, f_, h_, idx, moe["slots"], xq, 0, idx_ready=True)
 torch.cuda.synchronize()
 assert Z.device_status() == 0
 np.savez({dst!r}, **{{k: v.cpu().numpy() for k, v in out.items()}})
@@ -140,6 +147,9 @@ def default_run(inputs, tmp_path_factory):
     assert st == 0
     ok, worst = oracle.within_tolerance(out["ffn_y"], y_ref, e_ref)
     assert ok, ("ffn", worst)
+    # the two-launch FFN and the ready gather: the one-launch FFN's and the gather's bits
+    assert np.array_equal(out["ffn2_y"], out["ffn_y"])
+    assert np.array_equal(out["gather_ready"], out["gather"])
     return out
 
 
@@ -189,5 +199,5 @@ def test_other_batched_kernel_within_tolerance(env, inputs, default_run, tmp_pat
         assert ok, (name, worst)
         differs |= not np.array_equal(out[name], default_run[name])
     assert differs, "the selected kernel gave the default kernel's bits everywhere"
-    for k in ("gather", "ffn_y", "ffn_h"):
+    for k in ("gather", "gather_ready", "ffn_y", "ffn_h", "ffn2_y"):
         assert np.array_equal(out[k], default_run[k]), k
