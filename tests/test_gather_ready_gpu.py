@@ -236,3 +236,64 @@ def test_two_launch_ffn_equals_one_launch_ffn(graph):
         torch.cuda.synchronize()
         assert torch.equal(hs[l], h1), f"layer {l}: h differs"
         assert torch.equal(ys[l], y1), f"layer {l}: y differs from the one-launch FFN"
+
+
+@pytest.mark.parametrize("graph", [False, True])
+def test_ready_gather_after_a_device_router(graph):
+    """The index list written by a kernel that lets its dependents start before it
+    writes: the argmax DMMV (a 33-row router, top-1 pick) releases the next launch
+    before its reduction stores the index. Per layer: the router's argmax writes
+    one index into a shared buffer, a gate+up gather2 reads it after its wait, and
+    the ready down gather reads it at once. If the gather2 let the down gather
+    start before its own wait, the down gather could read the previous layer's
+    pick; each layer's down rows must equal a separate gather with that layer's
+    pick, bit for bit, eager and as a replayed CUDA graph."""
+    hidden, ffn, n_exp, layers = 2048, 512, 33, 16
+    r_np = synth.weight_blocks(Q8_0, n_exp, hidden, seed=101)
+    router = dev(r_np)
+    _, d_g, per_gu = _stack(Q4_0, ffn, hidden, n_exp, seed=102, layout=Z.GGUF)
+    _, d_u, _ = _stack(Q4_0, ffn, hidden, n_exp, seed=103, layout=Z.GGUF, stream=synth.S_WEIGHT2)
+    _, d_d, per_dn = _stack(Q8_0, hidden, ffn, n_exp, seed=104, layout=Z.GGUF, stream=synth.S_WEIGHT3)
+    xqs = [dev(oracle.quantize_q8_0(synth.activations(hidden, seed=110 + l))) for l in range(layers)]
+    xqd = dev(oracle.quantize_q8_0(synth.activations(ffn, seed=105)))
+    idx = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ws = torch.empty(Z.ARGMAX_WORKSPACE_BYTES, dtype=torch.uint8, device="cuda")
+    ya = torch.empty(1, ffn, device="cuda")
+    yb = torch.empty(1, ffn, device="cuda")
+    ys = [nan_out(1, hidden) for _ in range(layers)]
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+
+    def run():
+        for l in range(layers):
+            Z.dmmv_argmax(Q8_0, router, n_exp, hidden, xqs[l], workspace=ws, out=idx)
+            Z.expert_gather2(Q4_0, d_g, d_u, per_gu, ffn, hidden, idx, n_exp, xqs[l], 0, y_a=ya, y_b=yb,
+                             status=st)
+            Z.expert_gather(Q8_0, d_d, per_dn, hidden, ffn, idx, n_exp, xqd, 0, y=ys[l], status=st,
+                            idx_ready=True)
+
+    if graph:
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            run()
+        torch.cuda.current_stream().wait_stream(s)
+        for y in ys:
+            y.fill_(float("nan"))
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            run()
+        g.replay()
+    else:
+        run()
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    picks = []
+    for l in range(layers):
+        logits = Z.dmmv(Q8_0, router, n_exp, hidden, xqs[l]).cpu().numpy()   # the argmax kernel's fp32 logits
+        pick = int(np.argmax(logits))                                       # first index of the maximum
+        picks.append(pick)
+        ref = Z.expert_gather(Q8_0, d_d, per_dn, hidden, ffn, torch.tensor([pick], dtype=torch.int32,
+                              device="cuda"), n_exp, xqd, 0, y=nan_out(1, hidden))
+        torch.cuda.synchronize()
+        assert torch.equal(ys[l], ref), f"layer {l}: the ready gather did not use that layer's pick {pick}"
+    assert len(set(picks)) >= 4, picks   # the picks change from layer to layer

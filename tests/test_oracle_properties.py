@@ -13,7 +13,8 @@ only the seeded distributions of the workloads.
   rounding) of x / d, and the stored scale is numpy's IEEE binary16 rounding of
   the fp32 amax / 127.
 Each property also catches, by itself, planted mistakes from the mutant harness
-(test_properties_catch_planted_mistake). Skipped where hypothesis is missing.
+(test_properties_catch_planted_mistake). Not collected where hypothesis is missing
+(tests/conftest.py).
 """
 from fractions import Fraction
 
